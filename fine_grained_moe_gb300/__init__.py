@@ -1,0 +1,262 @@
+"""Python binding of the GB300 batch-1 fine-grained MoE verify-step library.
+
+A thin ctypes layer over the C ABI in ``include/fgm.h``: it turns torch CUDA
+tensors into device pointers, picks the current CUDA stream and raises on a
+non-zero status. Every stage of the step runs in the CUDA library
+``libfgm.so``; there is no other implementation in this package, so calling
+any function without the built library raises.
+
+Build the library with ``python -m fine_grained_moe_gb300.build`` (or the
+repository's ``__graft_entry__.build()``).
+"""
+
+from __future__ import annotations
+
+import ctypes
+import os
+from dataclasses import dataclass
+
+import torch
+
+from . import traffic  # noqa: F401  (byte accounting used by the benchmark)
+
+HIDDEN = 2816
+FFN = 704
+EXPERTS = 128
+N_EXPERTS = 129
+TOPK = 8
+MAX_M = 8
+MAX_LAYERS = 48
+
+STATUS_NONFINITE_LOGITS = 1
+STATUS_WAIT_TIMEOUT = 2
+
+_PKG = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_PKG, "libfgm.so")
+_lib = None
+
+
+class FgmError(RuntimeError):
+    pass
+
+
+class fgm_layer(ctypes.Structure):
+    _fields_ = [(n, ctypes.c_void_p) for n in
+                ("router_w", "router_b", "gate_q", "gate_s", "up_q", "up_s", "down_q", "down_s")]
+
+
+def lib() -> ctypes.CDLL:
+    """The loaded CUDA library; raises if it has not been built."""
+    global _lib
+    if _lib is None:
+        if not os.path.exists(LIB_PATH):
+            raise FgmError(f"CUDA library not built: {LIB_PATH} is missing "
+                           "(run python -m fine_grained_moe_gb300.build)")
+        L = ctypes.CDLL(LIB_PATH)
+        vp, ci, i64, sz = ctypes.c_void_p, ctypes.c_int, ctypes.c_int64, ctypes.c_size_t
+        LP = ctypes.POINTER(fgm_layer)
+        sig = {
+            "fgm_workspace_bytes": (sz, [ci, i64]),
+            "fgm_workspace_init": (ci, [vp, sz, vp]),
+            "fgm_moe_layer_fwd": (ci, [LP, vp, vp, ci, vp, vp, vp, sz, vp]),
+            "fgm_moe_stack_fwd": (ci, [LP, ci, vp, vp, ci, vp, vp, sz, vp]),
+            "fgm_lm_head_argmax": (ci, [vp, i64, vp, ci, vp, vp, vp, sz, vp]),
+            "fgm_spec_verify": (ci, [vp, vp, ci, vp, vp]),
+            "fgm_verify_step": (ci, [LP, ci, vp, i64, vp, vp, ci, vp, vp, vp, sz, vp]),
+            "fgm_verify_step_host": (ci, [LP, ci, vp, i64, vp, vp, ci, vp, vp, sz, vp]),
+            "fgm_read_status": (ci, [vp, sz, ci, vp, vp]),
+            "fgm_last_error": (ctypes.c_char_p, []),
+            "fgm_version": (ci, []),
+        }
+        for name, (res, args) in sig.items():
+            f = getattr(L, name)
+            f.restype = res
+            f.argtypes = args
+        _lib = L
+    return _lib
+
+
+def _check(rc: int) -> None:
+    if rc != 0:
+        msg = lib().fgm_last_error().decode(errors="replace")
+        raise FgmError(f"fgm error {rc}: {msg}")
+
+
+def _ptr(t: torch.Tensor | None):
+    if t is None:
+        return None
+    if not t.is_cuda:
+        raise FgmError("expected a CUDA tensor")
+    if not t.is_contiguous():
+        raise FgmError("expected a contiguous tensor")
+    return ctypes.c_void_p(t.data_ptr())
+
+
+def _stream(stream) -> ctypes.c_void_p:
+    s = torch.cuda.current_stream() if stream is None else stream
+    return ctypes.c_void_p(s.cuda_stream)
+
+
+def _m(x: torch.Tensor) -> int:
+    if x.dim() != 2 or x.shape[1] != HIDDEN or x.dtype != torch.bfloat16:
+        raise FgmError(f"expected bf16 [M, {HIDDEN}] activations, got {tuple(x.shape)} {x.dtype}")
+    return int(x.shape[0])
+
+
+def workspace_bytes(M: int = MAX_M, V: int = 0) -> int:
+    return int(lib().fgm_workspace_bytes(int(M), int(V)))
+
+
+class Workspace:
+    """Device scratch for the library's calls (one per concurrent stream)."""
+
+    def __init__(self, device=None, M: int = MAX_M, V: int = 0):
+        self.nbytes = workspace_bytes(M, V)
+        self.buf = torch.empty(self.nbytes + 256, dtype=torch.uint8, device=device or "cuda")
+        off = (-self.buf.data_ptr()) % 256
+        self.t = self.buf[off:off + self.nbytes]
+        _check(lib().fgm_workspace_init(_ptr(self.t), self.nbytes, _stream(None)))
+
+    @property
+    def ptr(self):
+        return _ptr(self.t)
+
+    def status(self, clear: bool = True) -> int:
+        out = ctypes.c_int32(0)
+        _check(lib().fgm_read_status(self.ptr, self.nbytes, int(clear), ctypes.byref(out), _stream(None)))
+        return int(out.value)
+
+
+@dataclass
+class Layer:
+    """One layer's device tensors (see ``fgm_layer`` in include/fgm.h)."""
+    router_w: torch.Tensor
+    router_b: torch.Tensor | None
+    gate_q: torch.Tensor
+    gate_s: torch.Tensor
+    up_q: torch.Tensor
+    up_s: torch.Tensor
+    down_q: torch.Tensor
+    down_s: torch.Tensor
+
+    @classmethod
+    def from_dict(cls, p: dict) -> "Layer":
+        return cls(**{k: p[k] for k in ("router_w", "router_b", "gate_q", "gate_s", "up_q", "up_s",
+                                        "down_q", "down_s")})
+
+    def struct(self) -> fgm_layer:
+        shapes = {"router_w": ((EXPERTS, HIDDEN), torch.bfloat16),
+                  "gate_q": ((N_EXPERTS, FFN, HIDDEN), torch.uint8),
+                  "up_q": ((N_EXPERTS, FFN, HIDDEN), torch.uint8),
+                  "down_q": ((N_EXPERTS, HIDDEN, FFN), torch.uint8),
+                  "gate_s": ((N_EXPERTS, FFN), torch.float32),
+                  "up_s": ((N_EXPERTS, FFN), torch.float32),
+                  "down_s": ((N_EXPERTS, HIDDEN), torch.float32)}
+        for name, (shape, dt) in shapes.items():
+            t = getattr(self, name)
+            if tuple(t.shape) != shape or t.dtype != dt:
+                raise FgmError(f"{name}: expected {shape} {dt}, got {tuple(t.shape)} {t.dtype}")
+        if self.router_b is not None and (tuple(self.router_b.shape) != (EXPERTS,)
+                                          or self.router_b.dtype != torch.float32):
+            raise FgmError("router_b: expected float32 [128]")
+        return fgm_layer(*[(_ptr(getattr(self, n)) or ctypes.c_void_p(0)).value for n in
+                           ("router_w", "router_b", "gate_q", "gate_s", "up_q", "up_s", "down_q",
+                            "down_s")])
+
+
+def _layers_array(layers) -> ctypes.Array:
+    structs = [(l if isinstance(l, Layer) else Layer.from_dict(l)).struct() for l in layers]
+    arr = (fgm_layer * len(structs))(*structs)
+    return arr
+
+
+def _ws(ws: Workspace | None, device) -> Workspace:
+    return ws if ws is not None else Workspace(device)
+
+
+# ---------------------------------------------------------------- entry points
+def moe_layer_fwd(layer, x: torch.Tensor, y: torch.Tensor | None = None,
+                  topk_ids: torch.Tensor | None = None, topk_w: torch.Tensor | None = None,
+                  ws: Workspace | None = None, stream=None) -> torch.Tensor:
+    """One MoE layer (no norm, no residual) on bf16 x[M, 2816]; returns bf16 y."""
+    M = _m(x)
+    y = torch.empty_like(x) if y is None else y
+    ws = _ws(ws, x.device)
+    L = (layer if isinstance(layer, Layer) else Layer.from_dict(layer)).struct()
+    _check(lib().fgm_moe_layer_fwd(ctypes.byref(L), _ptr(x), _ptr(y), M, _ptr(topk_ids), _ptr(topk_w),
+                                   ws.ptr, ws.nbytes, _stream(stream)))
+    return y
+
+
+def moe_stack_fwd(layers, x: torch.Tensor, y: torch.Tensor | None = None,
+                  ids_trace: torch.Tensor | None = None, ws: Workspace | None = None,
+                  stream=None) -> torch.Tensor:
+    """The stack h <- h + layer(RMSNorm(h)) over ``layers``; returns bf16 h."""
+    M = _m(x)
+    y = torch.empty_like(x) if y is None else y
+    ws = _ws(ws, x.device)
+    arr = _layers_array(layers)
+    _check(lib().fgm_moe_stack_fwd(arr, len(arr), _ptr(x), _ptr(y), M, _ptr(ids_trace), ws.ptr,
+                                   ws.nbytes, _stream(stream)))
+    return y
+
+
+def lm_head_argmax(emb: torch.Tensor, h: torch.Tensor, argmax: torch.Tensor | None = None,
+                   maxlogit: torch.Tensor | None = None, ws: Workspace | None = None,
+                   stream=None) -> torch.Tensor:
+    """argmax_v emb[v] . h[t] for each of the M rows of bf16 h; returns int32 [M]."""
+    M = _m(h)
+    V = int(emb.shape[0])
+    argmax = torch.empty(M, dtype=torch.int32, device=h.device) if argmax is None else argmax
+    ws = _ws(ws, h.device)
+    _check(lib().fgm_lm_head_argmax(_ptr(emb), V, _ptr(h), M, _ptr(argmax), _ptr(maxlogit), ws.ptr,
+                                    ws.nbytes, _stream(stream)))
+    return argmax
+
+
+def spec_verify(target: torch.Tensor, draft: torch.Tensor, out: torch.Tensor | None = None,
+                stream=None) -> torch.Tensor:
+    """Greedy acceptance; returns int32 [2] = {accepted drafts, next token}."""
+    M = int(target.shape[0])
+    out = torch.empty(2, dtype=torch.int32, device=target.device) if out is None else out
+    _check(lib().fgm_spec_verify(_ptr(target), _ptr(draft) if M > 1 else None, M, _ptr(out),
+                                 _stream(stream)))
+    return out
+
+
+def verify_step(layers, emb: torch.Tensor, x: torch.Tensor, draft: torch.Tensor | None,
+                out: torch.Tensor | None = None, argmax: torch.Tensor | None = None,
+                ws: Workspace | None = None, stream=None, _arr=None) -> torch.Tensor:
+    """Stack + final RMSNorm + lm_head argmax + greedy acceptance; returns int32
+    [2] = {accepted drafts, next token} on the device."""
+    M = _m(x)
+    out = torch.empty(2, dtype=torch.int32, device=x.device) if out is None else out
+    ws = _ws(ws, x.device)
+    arr = _layers_array(layers) if _arr is None else _arr
+    _check(lib().fgm_verify_step(arr, len(arr), _ptr(emb), int(emb.shape[0]), _ptr(x),
+                                 _ptr(draft) if M > 1 else None, M, _ptr(argmax), _ptr(out), ws.ptr,
+                                 ws.nbytes, _stream(stream)))
+    return out
+
+
+def verify_step_host(layers, emb: torch.Tensor, x_host: torch.Tensor, draft_host: torch.Tensor | None,
+                     out_host: torch.Tensor | None = None, ws: Workspace | None = None,
+                     stream=None, _arr=None) -> torch.Tensor:
+    """verify_step with host (ideally pinned) x/draft/out; synchronises."""
+    if x_host.is_cuda:
+        raise FgmError("x_host must be a host tensor")
+    M = int(x_host.shape[0])
+    out_host = torch.empty(2, dtype=torch.int32) if out_host is None else out_host
+    ws = _ws(ws, emb.device)
+    arr = _layers_array(layers) if _arr is None else _arr
+    dp = ctypes.c_void_p(draft_host.data_ptr()) if (draft_host is not None and M > 1) else None
+    _check(lib().fgm_verify_step_host(arr, len(arr), _ptr(emb), int(emb.shape[0]),
+                                      ctypes.c_void_p(x_host.data_ptr()), dp, M,
+                                      ctypes.c_void_p(out_host.data_ptr()), ws.ptr, ws.nbytes,
+                                      _stream(stream)))
+    return out_host
+
+
+def layers_array(layers):
+    """Pre-marshalled layer table, reusable across calls (pass as ``_arr``)."""
+    return _layers_array(layers)

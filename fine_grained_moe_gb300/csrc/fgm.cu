@@ -1,0 +1,401 @@
+// C ABI of the library (declared in include/fgm.h): argument validation,
+// workspace carving and launch sequencing. Every stage of the step runs in
+// the CUDA kernels of basic_kernels.cuh / fused_step.cuh.
+#include <stdarg.h>
+#include <stdio.h>
+#include <string.h>
+
+#include "basic_kernels.cuh"
+
+namespace fgm {
+namespace {
+
+thread_local char g_err[512] = "";
+
+int fail(int code, const char *fmt, ...)
+{
+    va_list ap;
+    va_start(ap, fmt);
+    vsnprintf(g_err, sizeof g_err, fmt, ap);
+    va_end(ap);
+    return code;
+}
+
+#define FGM_CUDA(call)                                                                         \
+    do {                                                                                       \
+        cudaError_t e_ = (call);                                                               \
+        if (e_ != cudaSuccess)                                                                 \
+            return fail(FGM_ERR_CUDA, "%s failed: %s", #call, cudaGetErrorString(e_));         \
+    } while (0)
+
+#define FGM_CHECK_LAUNCH()                                                                     \
+    do {                                                                                       \
+        cudaError_t e_ = cudaGetLastError();                                                   \
+        if (e_ != cudaSuccess)                                                                 \
+            return fail(FGM_ERR_CUDA, "kernel launch failed: %s (%s:%d)", cudaGetErrorString(e_), \
+                        __FILE__, __LINE__);                                                   \
+    } while (0)
+
+constexpr int kMaxDevices = 64;
+
+struct DeviceInfo {
+    bool ready = false;
+    bool ok = false;
+    int sms = 0;
+};
+DeviceInfo g_dev[kMaxDevices];
+
+// Checks (once per device) that the current device is an sm_103 GPU and
+// raises the dynamic shared-memory limit of the kernels that need it.
+int device_ready(int *sms)
+{
+    int dev = 0;
+    FGM_CUDA(cudaGetDevice(&dev));
+    if (dev < 0 || dev >= kMaxDevices)
+        return fail(FGM_ERR_DEVICE, "device index %d out of range", dev);
+    DeviceInfo &d = g_dev[dev];
+    if (!d.ready) {
+        int major = 0, minor = 0;
+        FGM_CUDA(cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev));
+        FGM_CUDA(cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev));
+        FGM_CUDA(cudaDeviceGetAttribute(&d.sms, cudaDevAttrMultiProcessorCount, dev));
+        d.ok = (major == 10 && minor == 3);
+        if (d.ok) {
+#define FGM_SMEM(k, bytes) FGM_CUDA(cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes))
+            FGM_SMEM(k_gateup_basic<1>, 1 * kH * 4);
+            FGM_SMEM(k_gateup_basic<2>, 2 * kH * 4);
+            FGM_SMEM(k_gateup_basic<3>, 3 * kH * 4);
+            FGM_SMEM(k_gateup_basic<4>, 4 * kH * 4);
+            FGM_SMEM(k_gateup_basic<5>, 5 * kH * 4);
+            FGM_SMEM(k_gateup_basic<6>, 6 * kH * 4);
+            FGM_SMEM(k_gateup_basic<7>, 7 * kH * 4);
+            FGM_SMEM(k_gateup_basic<8>, 8 * kH * 4);
+            FGM_SMEM(k_lmhead_basic<1>, 1 * kH * 4);
+            FGM_SMEM(k_lmhead_basic<2>, 2 * kH * 4);
+            FGM_SMEM(k_lmhead_basic<3>, 3 * kH * 4);
+            FGM_SMEM(k_lmhead_basic<4>, 4 * kH * 4);
+            FGM_SMEM(k_lmhead_basic<5>, 5 * kH * 4);
+            FGM_SMEM(k_lmhead_basic<6>, 6 * kH * 4);
+            FGM_SMEM(k_lmhead_basic<7>, 7 * kH * 4);
+            FGM_SMEM(k_lmhead_basic<8>, 8 * kH * 4);
+#undef FGM_SMEM
+        }
+        d.ready = true;
+    }
+    if (!d.ok)
+        return fail(FGM_ERR_DEVICE, "device %d is not an sm_103 GPU; this library is built for sm_103a", dev);
+    if (sms)
+        *sms = d.sms;
+    return FGM_OK;
+}
+
+bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+int check_layer(const fgm_layer *L, int index)
+{
+    if (!L)
+        return fail(FGM_ERR_INVALID_ARG, "layer %d: null layer struct", index);
+    const void *ptrs[] = {L->router_w, L->gate_q, L->gate_s, L->up_q, L->up_s, L->down_q, L->down_s};
+    const char *names[] = {"router_w", "gate_q", "gate_s", "up_q", "up_s", "down_q", "down_s"};
+    for (int i = 0; i < 7; ++i) {
+        if (!ptrs[i])
+            return fail(FGM_ERR_INVALID_ARG, "layer %d: %s is NULL", index, names[i]);
+        if (!aligned16(ptrs[i]))
+            return fail(FGM_ERR_INVALID_ARG, "layer %d: %s is not 16-byte aligned", index, names[i]);
+    }
+    if (L->router_b && (reinterpret_cast<uintptr_t>(L->router_b) & 3u))
+        return fail(FGM_ERR_INVALID_ARG, "layer %d: router_b is not 4-byte aligned", index);
+    return FGM_OK;
+}
+
+int check_ws(void *ws, size_t ws_bytes, int M, int64_t V)
+{
+    if (!ws)
+        return fail(FGM_ERR_WORKSPACE, "workspace is NULL");
+    if (reinterpret_cast<uintptr_t>(ws) & 255u)
+        return fail(FGM_ERR_WORKSPACE, "workspace is not 256-byte aligned");
+    const size_t need = fgm_workspace_bytes(M, V);
+    if (ws_bytes < need)
+        return fail(FGM_ERR_WORKSPACE, "workspace has %zu bytes, %zu needed", ws_bytes, need);
+    return FGM_OK;
+}
+
+int check_m(int M)
+{
+    if (M < 1 || M > kMaxM)
+        return fail(FGM_ERR_INVALID_ARG, "M = %d outside [1, %d]", M, kMaxM);
+    return FGM_OK;
+}
+
+#define FGM_TRY(expr)              \
+    do {                           \
+        int rc_ = (expr);          \
+        if (rc_ != FGM_OK)         \
+            return rc_;            \
+    } while (0)
+
+template <int M>
+int launch_layer_experts(const fgm_layer *L, const Ws &w, float *out, cudaStream_t st)
+{
+    k_gateup_basic<M><<<dim3(kF / 32, kMaxSlots), 256, M * kH * 4, st>>>(
+        L->gate_q, L->gate_s, L->up_q, L->up_s, w.xn, w.meta, w.comb, w.act);
+    FGM_CHECK_LAUNCH();
+    k_down_basic<M><<<dim3(kH / 32, kMaxSlots), 256, 0, st>>>(L->down_q, L->down_s, w.act, w.meta, out);
+    FGM_CHECK_LAUNCH();
+    return FGM_OK;
+}
+
+int launch_experts(int M, const fgm_layer *L, const Ws &w, float *out, cudaStream_t st)
+{
+    switch (M) {
+    case 1: return launch_layer_experts<1>(L, w, out, st);
+    case 2: return launch_layer_experts<2>(L, w, out, st);
+    case 3: return launch_layer_experts<3>(L, w, out, st);
+    case 4: return launch_layer_experts<4>(L, w, out, st);
+    case 5: return launch_layer_experts<5>(L, w, out, st);
+    case 6: return launch_layer_experts<6>(L, w, out, st);
+    case 7: return launch_layer_experts<7>(L, w, out, st);
+    default: return launch_layer_experts<8>(L, w, out, st);
+    }
+}
+
+// Router + dedup + experts of one layer reading w.xn, adding into `out`.
+int run_layer(int M, const fgm_layer *L, const Ws &w, float *out, int32_t *ids_out, float *w_out,
+              cudaStream_t st)
+{
+    k_router_logits<<<kE, 256, 0, st>>>(w.xn, M, L->router_w, L->router_b, w.logits);
+    FGM_CHECK_LAUNCH();
+    k_topk_dedup<<<1, 256, 0, st>>>(w.logits, M, w.meta, w.comb, ids_out, w_out, w.status);
+    FGM_CHECK_LAUNCH();
+    return launch_experts(M, L, w, out, st);
+}
+
+int lmhead_grid(int sms) { return sms * 4 < kMaxParts ? sms * 4 : kMaxParts; }
+
+template <int M>
+int launch_lmhead_t(const uint16_t *emb, int64_t V, const uint16_t *hb, const Ws &w, int G, cudaStream_t st)
+{
+    k_lmhead_basic<M><<<G, 256, M * kH * 4, st>>>(emb, V, hb, w.part_val, w.part_idx);
+    FGM_CHECK_LAUNCH();
+    return FGM_OK;
+}
+
+int launch_lmhead(int M, const uint16_t *emb, int64_t V, const uint16_t *hb, const Ws &w, int G,
+                  cudaStream_t st)
+{
+    switch (M) {
+    case 1: return launch_lmhead_t<1>(emb, V, hb, w, G, st);
+    case 2: return launch_lmhead_t<2>(emb, V, hb, w, G, st);
+    case 3: return launch_lmhead_t<3>(emb, V, hb, w, G, st);
+    case 4: return launch_lmhead_t<4>(emb, V, hb, w, G, st);
+    case 5: return launch_lmhead_t<5>(emb, V, hb, w, G, st);
+    case 6: return launch_lmhead_t<6>(emb, V, hb, w, G, st);
+    case 7: return launch_lmhead_t<7>(emb, V, hb, w, G, st);
+    default: return launch_lmhead_t<8>(emb, V, hb, w, G, st);
+    }
+}
+
+int check_layers(const fgm_layer *layers, int n_layers)
+{
+    if (!layers)
+        return fail(FGM_ERR_INVALID_ARG, "layers is NULL");
+    if (n_layers < 1 || n_layers > FGM_MAX_LAYERS)
+        return fail(FGM_ERR_INVALID_ARG, "n_layers = %d outside [1, %d]", n_layers, FGM_MAX_LAYERS);
+    for (int l = 0; l < n_layers; ++l)
+        FGM_TRY(check_layer(&layers[l], l));
+    return FGM_OK;
+}
+
+int check_vocab(const uint16_t *emb, int64_t V)
+{
+    if (!emb || !aligned16(emb))
+        return fail(FGM_ERR_INVALID_ARG, "emb is NULL or not 16-byte aligned");
+    if (V < 1 || V > 0x7FFFFFFFLL)
+        return fail(FGM_ERR_INVALID_ARG, "V = %lld outside [1, 2^31)", (long long)V);
+    return FGM_OK;
+}
+
+// The stack on w.h (already holding the input), layer by layer.
+int run_stack(const fgm_layer *layers, int n_layers, int M, const Ws &w, int32_t *ids_trace,
+              cudaStream_t st)
+{
+    for (int l = 0; l < n_layers; ++l) {
+        k_rmsnorm<<<M, 256, 0, st>>>(w.h, w.xn, nullptr);
+        FGM_CHECK_LAUNCH();
+        FGM_TRY(run_layer(M, &layers[l], w, w.h, ids_trace ? ids_trace + (size_t)l * M * kK : nullptr,
+                          nullptr, st));
+    }
+    return FGM_OK;
+}
+
+int verify_step_impl(const fgm_layer *layers, int n_layers, const uint16_t *emb, int64_t V,
+                     const uint16_t *x, const int32_t *draft, int M, int32_t *argmax, int32_t *out,
+                     void *ws, cudaStream_t st, int sms)
+{
+    Ws w = ws_carve(ws);
+    k_bf16_to_f32<<<8, 256, 0, st>>>(x, M * kH, w.h);
+    FGM_CHECK_LAUNCH();
+    FGM_TRY(run_stack(layers, n_layers, M, w, nullptr, st));
+    k_rmsnorm<<<M, 256, 0, st>>>(w.h, nullptr, w.hb);
+    FGM_CHECK_LAUNCH();
+    const int G = lmhead_grid(sms);
+    FGM_TRY(launch_lmhead(M, emb, V, w.hb, w, G, st));
+    k_argmax_final<<<1, 256, 0, st>>>(w.part_val, w.part_idx, G, M, argmax ? argmax : w.argmax, nullptr,
+                                      draft, out, w.status);
+    FGM_CHECK_LAUNCH();
+    return FGM_OK;
+}
+
+}  // namespace
+}  // namespace fgm
+
+using namespace fgm;
+
+extern "C" {
+
+size_t fgm_workspace_bytes(int M, int64_t V)
+{
+    (void)V;
+    if (M < 1 || M > kMaxM)
+        return 0;
+    return ws_offsets().total;
+}
+
+const char *fgm_last_error(void) { return g_err; }
+
+int fgm_version(void) { return 100; }
+
+int fgm_moe_layer_fwd(const fgm_layer *layer, const uint16_t *x, uint16_t *y, int M,
+                      int32_t *topk_ids, float *topk_w, void *ws, size_t ws_bytes, void *stream)
+{
+    int sms = 0;
+    FGM_TRY(check_m(M));
+    FGM_TRY(check_layer(layer, 0));
+    if (!x || !y || !aligned16(x) || !aligned16(y))
+        return fail(FGM_ERR_INVALID_ARG, "x/y NULL or not 16-byte aligned");
+    if (x == y)
+        return fail(FGM_ERR_INVALID_ARG, "y may not alias x");
+    FGM_TRY(check_ws(ws, ws_bytes, M, 0));
+    FGM_TRY(device_ready(&sms));
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    Ws w = ws_carve(ws);
+    k_layer_prep<<<16, 256, 0, st>>>(x, M, w.xn, w.acc);
+    FGM_CHECK_LAUNCH();
+    FGM_TRY(run_layer(M, layer, w, w.acc, topk_ids, topk_w, st));
+    k_f32_to_bf16<<<16, 256, 0, st>>>(w.acc, M * kH, y);
+    FGM_CHECK_LAUNCH();
+    return FGM_OK;
+}
+
+int fgm_moe_stack_fwd(const fgm_layer *layers, int n_layers, const uint16_t *x, uint16_t *y, int M,
+                      int32_t *ids_trace, void *ws, size_t ws_bytes, void *stream)
+{
+    int sms = 0;
+    FGM_TRY(check_m(M));
+    FGM_TRY(check_layers(layers, n_layers));
+    if (!x || !y || !aligned16(x) || !aligned16(y))
+        return fail(FGM_ERR_INVALID_ARG, "x/y NULL or not 16-byte aligned");
+    FGM_TRY(check_ws(ws, ws_bytes, M, 0));
+    FGM_TRY(device_ready(&sms));
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    Ws w = ws_carve(ws);
+    k_bf16_to_f32<<<8, 256, 0, st>>>(x, M * kH, w.h);
+    FGM_CHECK_LAUNCH();
+    FGM_TRY(run_stack(layers, n_layers, M, w, ids_trace, st));
+    k_f32_to_bf16<<<16, 256, 0, st>>>(w.h, M * kH, y);
+    FGM_CHECK_LAUNCH();
+    return FGM_OK;
+}
+
+int fgm_lm_head_argmax(const uint16_t *emb, int64_t V, const uint16_t *h, int M, int32_t *argmax,
+                       float *maxlogit, void *ws, size_t ws_bytes, void *stream)
+{
+    int sms = 0;
+    FGM_TRY(check_m(M));
+    FGM_TRY(check_vocab(emb, V));
+    if (!h || !aligned16(h) || !argmax)
+        return fail(FGM_ERR_INVALID_ARG, "h/argmax NULL or h not 16-byte aligned");
+    FGM_TRY(check_ws(ws, ws_bytes, M, V));
+    FGM_TRY(device_ready(&sms));
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    Ws w = ws_carve(ws);
+    const int G = lmhead_grid(sms);
+    FGM_TRY(launch_lmhead(M, emb, V, h, w, G, st));
+    k_argmax_final<<<1, 256, 0, st>>>(w.part_val, w.part_idx, G, M, argmax, maxlogit, nullptr, nullptr,
+                                      w.status);
+    FGM_CHECK_LAUNCH();
+    return FGM_OK;
+}
+
+int fgm_spec_verify(const int32_t *target, const int32_t *draft, int M, int32_t *out, void *stream)
+{
+    FGM_TRY(check_m(M));
+    if (!target || !out || (M > 1 && !draft))
+        return fail(FGM_ERR_INVALID_ARG, "target/out NULL, or draft NULL with M > 1");
+    FGM_TRY(device_ready(nullptr));
+    k_spec_verify<<<1, 32, 0, static_cast<cudaStream_t>(stream)>>>(target, draft, M, out);
+    FGM_CHECK_LAUNCH();
+    return FGM_OK;
+}
+
+int fgm_verify_step(const fgm_layer *layers, int n_layers, const uint16_t *emb, int64_t V,
+                    const uint16_t *x, const int32_t *draft, int M, int32_t *argmax, int32_t *out,
+                    void *ws, size_t ws_bytes, void *stream)
+{
+    int sms = 0;
+    FGM_TRY(check_m(M));
+    FGM_TRY(check_layers(layers, n_layers));
+    FGM_TRY(check_vocab(emb, V));
+    if (!x || !aligned16(x) || !out || (M > 1 && !draft))
+        return fail(FGM_ERR_INVALID_ARG, "x/out NULL, x misaligned, or draft NULL with M > 1");
+    FGM_TRY(check_ws(ws, ws_bytes, M, V));
+    FGM_TRY(device_ready(&sms));
+    return verify_step_impl(layers, n_layers, emb, V, x, draft, M, argmax, out, ws,
+                            static_cast<cudaStream_t>(stream), sms);
+}
+
+int fgm_verify_step_host(const fgm_layer *layers, int n_layers, const uint16_t *emb, int64_t V,
+                         const uint16_t *x_host, const int32_t *draft_host, int M, int32_t *out_host,
+                         void *ws, size_t ws_bytes, void *stream)
+{
+    int sms = 0;
+    FGM_TRY(check_m(M));
+    FGM_TRY(check_layers(layers, n_layers));
+    FGM_TRY(check_vocab(emb, V));
+    if (!x_host || !out_host || (M > 1 && !draft_host))
+        return fail(FGM_ERR_INVALID_ARG, "x_host/out_host NULL, or draft_host NULL with M > 1");
+    FGM_TRY(check_ws(ws, ws_bytes, M, V));
+    FGM_TRY(device_ready(&sms));
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    Ws w = ws_carve(ws);
+    FGM_CUDA(cudaMemcpyAsync(w.io_x, x_host, sizeof(uint16_t) * M * kH, cudaMemcpyHostToDevice, st));
+    if (M > 1)
+        FGM_CUDA(cudaMemcpyAsync(w.io_draft, draft_host, sizeof(int32_t) * (M - 1), cudaMemcpyHostToDevice, st));
+    FGM_TRY(verify_step_impl(layers, n_layers, emb, V, w.io_x, w.io_draft, M, nullptr, w.io_out, ws, st, sms));
+    FGM_CUDA(cudaMemcpyAsync(out_host, w.io_out, sizeof(int32_t) * 2, cudaMemcpyDeviceToHost, st));
+    FGM_CUDA(cudaStreamSynchronize(st));
+    return FGM_OK;
+}
+
+int fgm_workspace_init(void *ws, size_t ws_bytes, void *stream)
+{
+    FGM_TRY(check_ws(ws, ws_bytes, 1, 0));
+    FGM_CUDA(cudaMemsetAsync(ws, 0, ws_offsets().total, static_cast<cudaStream_t>(stream)));
+    return FGM_OK;
+}
+
+int fgm_read_status(void *ws, size_t ws_bytes, int clear, int32_t *status, void *stream)
+{
+    FGM_TRY(check_ws(ws, ws_bytes, 1, 0));
+    if (!status)
+        return fail(FGM_ERR_INVALID_ARG, "status is NULL");
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    Ws w = ws_carve(ws);
+    FGM_CUDA(cudaMemcpyAsync(status, w.status, sizeof(int32_t), cudaMemcpyDeviceToHost, st));
+    FGM_CUDA(cudaStreamSynchronize(st));
+    if (clear)
+        FGM_CUDA(cudaMemsetAsync(w.status, 0, sizeof(int32_t), st));
+    return FGM_OK;
+}
+
+}  // extern "C"

@@ -1,0 +1,176 @@
+/*
+ * fgm.h - C ABI of the GB300 batch-1 fine-grained MoE verify-step library.
+ *
+ * The library runs the memory-bound decode/verify step of speculative
+ * decoding on a Gemma-4-26B-A4B-shaped mixture of experts: hidden width 2816,
+ * 128 routed experts of FFN width 704 plus one always-on shared expert,
+ * top-8 routing, FP8-E4M3 expert weights with one fp32 scale per output row,
+ * and a tied 262,144-word bf16 lm_head. One call processes M = gamma + 1
+ * tokens (the real token and gamma drafted ones) in a single pass over the
+ * weights ("llm-decoding", us-homepage.pages.dev, §"Lever 2: fewer passes
+ * (native MTP)": the full model verifies the drafted tokens in one pass).
+ *
+ * Conventions for every entry point
+ *  - All tensor pointers are DEVICE pointers owned by the caller, unless an
+ *    entry point says otherwise. The library never frees them and keeps no
+ *    reference after the call returns.
+ *  - Row-major layouts; bf16 is passed as raw 16-bit patterns (uint16_t).
+ *  - Weight pointers and activation pointers must be 16-byte aligned.
+ *  - `ws` is caller-allocated device scratch of at least
+ *    fgm_workspace_bytes(M, V) bytes, 256-byte aligned; the library uses it
+ *    only during the call (calls that share a workspace must not overlap).
+ *  - `stream` is a cudaStream_t (NULL = legacy default stream). Calls are
+ *    asynchronous on that stream except where stated.
+ *  - Return value: FGM_OK (0) or a negative FGM_ERR_* code; arguments are
+ *    validated on the host before anything is launched, so an error return
+ *    means nothing was enqueued, except FGM_ERR_CUDA from a failed launch.
+ *    fgm_last_error() gives a message for the calling thread.
+ *  - Kernels never trap. Anomalies they detect (non-finite router logits,
+ *    a timed-out wait) set bits of a status word in the workspace, read
+ *    with fgm_read_status().
+ */
+#ifndef FGM_H
+#define FGM_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* Model shape ("llm-decoding", §"The exact architecture"). */
+#define FGM_HIDDEN 2816     /* hidden width */
+#define FGM_FFN 704         /* expert FFN width */
+#define FGM_EXPERTS 128     /* routed experts */
+#define FGM_SHARED 1        /* always-on shared experts, stored after the routed ones */
+#define FGM_TOPK 8          /* routed experts per token */
+#define FGM_MAX_M 8         /* tokens per call: 1 real + up to 7 drafted */
+#define FGM_MAX_LAYERS 48   /* layers per stack call */
+#define FGM_RMS_EPS 1e-6f   /* RMSNorm epsilon of the stack */
+
+enum {
+    FGM_OK = 0,
+    FGM_ERR_INVALID_ARG = -1, /* null/misaligned pointer, M or V out of range */
+    FGM_ERR_WORKSPACE = -2,   /* workspace missing, misaligned or too small */
+    FGM_ERR_CUDA = -3,        /* a CUDA runtime call failed; see fgm_last_error() */
+    FGM_ERR_DEVICE = -4,      /* the current device is not a supported GPU (sm_103) */
+};
+
+/* Status bits written by kernels into the workspace (fgm_read_status). */
+enum {
+    FGM_STATUS_NONFINITE_LOGITS = 1, /* a router or lm_head logit was NaN; treated as -inf */
+    FGM_STATUS_WAIT_TIMEOUT = 2,     /* a grid-wide wait gave up; outputs are invalid */
+};
+
+/* One MoE layer's weights (all device pointers).
+ *  router_w  bf16 [128][2816]         router logits l = router_w . x + router_b
+ *  router_b  fp32 [128] or NULL       additive logit bias
+ *  gate_q    E4M3 [129][704][2816]    expert e's gate rows (e = 128: shared)
+ *  gate_s    fp32 [129][704]          per-row scales: W = e4m3(q) * s
+ *  up_q      E4M3 [129][704][2816]
+ *  up_s      fp32 [129][704]
+ *  down_q    E4M3 [129][2816][704]
+ *  down_s    fp32 [129][2816]
+ * Weights follow "llm-decoding" §"Where the 7.36 GB goes" (gate, up and down
+ * of 2816x704 per expert) and §"Lever 1" (8-bit weights, dequantised at
+ * higher precision). */
+typedef struct fgm_layer {
+    const uint16_t *router_w;
+    const float *router_b;
+    const uint8_t *gate_q;
+    const float *gate_s;
+    const uint8_t *up_q;
+    const float *up_s;
+    const uint8_t *down_q;
+    const float *down_s;
+} fgm_layer;
+
+/* Bytes of scratch an M-token call needs; V is the vocabulary size for the
+ * lm_head entry points (0 if unused). Never fails; 0 for M out of range. */
+size_t fgm_workspace_bytes(int M, int64_t V);
+
+/* Zeroes a workspace (status word and wait counters included). Call once
+ * after allocating it, before its first use by any other entry point. */
+int fgm_workspace_init(void *ws, size_t ws_bytes, void *stream);
+
+/* One MoE FFN layer (no norm, no residual) on M tokens:
+ *   y_t = sum_{i<8} w_{t,i} * expert_{id_{t,i}}(x_t) + expert_128(x_t),
+ *   expert_e(x) = s_d (Q_d (gelu_tanh(s_g (Q_g x)) * s_u (Q_u x))),
+ * with ids/w from the router: softmax over the 128 biased logits, top-8
+ * (ties to the lower index), renormalised to sum to 1. Accumulation is fp32.
+ * Source: "llm-decoding" §"The exact architecture" (top 8 of 128 + one shared).
+ *  x         bf16 [M][2816] input
+ *  y         bf16 [M][2816] output (may not alias x)
+ *  topk_ids  int32 [M][8] or NULL: chosen expert ids, descending weight
+ *  topk_w    fp32 [M][8] or NULL: their renormalised weights */
+int fgm_moe_layer_fwd(const fgm_layer *layer, const uint16_t *x, uint16_t *y, int M,
+                      int32_t *topk_ids, float *topk_w, void *ws, size_t ws_bytes, void *stream);
+
+/* n_layers stacked layers (attention omitted), each
+ *   h <- h + moe_layer(RMSNorm(h)),  RMSNorm(h) = h / sqrt(mean(h^2) + 1e-6),
+ * starting from h = x; the residual stream stays fp32 inside the call.
+ *  layers     HOST array of n_layers fgm_layer (1 <= n_layers <= 48)
+ *  x          bf16 [M][2816] input hidden states
+ *  y          bf16 [M][2816] output: the final residual stream h (no norm)
+ *  ids_trace  int32 [n_layers][M][8] or NULL: routing of every layer */
+int fgm_moe_stack_fwd(const fgm_layer *layers, int n_layers, const uint16_t *x, uint16_t *y,
+                      int M, int32_t *ids_trace, void *ws, size_t ws_bytes, void *stream);
+
+/* Tied lm_head fused with argmax: z_{t,v} = sum_j emb[v][j] * h[t][j]
+ * (fp32 accumulation), argmax over v with ties to the lower index.
+ * Source: "llm-decoding" §"The exact architecture" (262,144-word tied
+ * lm_head) and §"Where the 7.36 GB goes" (read once per step).
+ *  emb       bf16 [V][2816], 1 <= V < 2^31
+ *  h         bf16 [M][2816] final hidden states
+ *  argmax    int32 [M] output
+ *  maxlogit  fp32 [M] or NULL: the winning logit */
+int fgm_lm_head_argmax(const uint16_t *emb, int64_t V, const uint16_t *h, int M, int32_t *argmax,
+                       float *maxlogit, void *ws, size_t ws_bytes, void *stream);
+
+/* Greedy acceptance of gamma = M - 1 drafted tokens: a = largest j <= gamma
+ * with draft[0..j-1] == target[0..j-1]; out = {a, target[a]} (the accepted
+ * count and the token emitted after the accepted drafts). Source:
+ * "llm-decoding" §"Lever 2" (keep the tokens the model would have produced)
+ * and §"What we learned" (identical output to ordinary decoding).
+ *  target  int32 [M] argmax tokens at the M positions (device)
+ *  draft   int32 [M-1] drafted tokens d_1..d_gamma (device; unused if M == 1)
+ *  out     int32 [2] (device) */
+int fgm_spec_verify(const int32_t *target, const int32_t *draft, int M, int32_t *out,
+                    void *stream);
+
+/* One full verify step: the n_layers stack from x, a final unit RMSNorm
+ * rounded to bf16, the lm_head argmax, and greedy acceptance of the drafts.
+ *  layers   HOST array of n_layers fgm_layer
+ *  emb      bf16 [V][2816]
+ *  x        bf16 [M][2816]
+ *  draft    int32 [M-1] (device; may be NULL when M == 1)
+ *  argmax   int32 [M] output (device) or NULL
+ *  out      int32 [2] output {accepted, next} (device) */
+int fgm_verify_step(const fgm_layer *layers, int n_layers, const uint16_t *emb, int64_t V,
+                    const uint16_t *x, const int32_t *draft, int M, int32_t *argmax, int32_t *out,
+                    void *ws, size_t ws_bytes, void *stream);
+
+/* fgm_verify_step with HOST input and output buffers: copies x_host
+ * (bf16 [M][2816]) and draft_host (int32 [M-1]) into the workspace, runs the
+ * step, copies {accepted, next} into out_host (int32 [2]) and synchronises
+ * the stream before returning. Host buffers should be pinned for speed. */
+int fgm_verify_step_host(const fgm_layer *layers, int n_layers, const uint16_t *emb, int64_t V,
+                         const uint16_t *x_host, const int32_t *draft_host, int M,
+                         int32_t *out_host, void *ws, size_t ws_bytes, void *stream);
+
+/* Reads the status word of a workspace (synchronises the stream) and, if
+ * `clear`, resets it. */
+int fgm_read_status(void *ws, size_t ws_bytes, int clear, int32_t *status, void *stream);
+
+/* Message describing the last error returned on the calling thread. */
+const char *fgm_last_error(void);
+
+/* Library version, major * 10000 + minor * 100 + patch. */
+int fgm_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* FGM_H */

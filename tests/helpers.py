@@ -32,3 +32,29 @@ def dequant_torch(q: np.ndarray, s: np.ndarray) -> torch.Tensor:
     """Library decode of E4M3 codes (torch's float8 view), times the row scales, in fp64."""
     codes = torch.from_numpy(np.ascontiguousarray(q)).view(torch.float8_e4m3fn).to(torch.float64)
     return codes * torch.from_numpy(np.ascontiguousarray(s)).to(torch.float64).unsqueeze(-1)
+
+
+# ---------------------------------------------------------------- comparison rules
+# Tolerance stated for the step: hidden states and logits within a maximum
+# relative error of 1e-2 of the bf16-rounded oracle, read per token row as
+# max|gpu - bf16(oracle)| / max|bf16(oracle)|. Router ids and accepted lengths
+# must be bit-exact wherever the oracle's decision margin exceeds 1e-2.
+REL_TOL = 1e-2
+MARGIN = 1e-2
+
+
+def rowwise_rel_err(gpu_bf16: torch.Tensor, ref_f64: np.ndarray) -> np.ndarray:
+    g = gpu_bf16.detach().cpu().to(torch.float64).numpy()
+    r = oracle.bf16_to_f64(oracle.bf16_round(ref_f64))
+    return np.abs(g - r).max(axis=1) / np.abs(r).max(axis=1)
+
+
+def id_sets_agree(gpu_ids: np.ndarray, ref_ids: np.ndarray) -> bool:
+    return sorted(gpu_ids.tolist()) == sorted(ref_ids.tolist())
+
+
+def ids_valid_at_tie(gpu_ids: np.ndarray, logits: np.ndarray, k: int = 8) -> bool:
+    """A routing that differs from the oracle's is acceptable only if every
+    chosen expert's oracle logit is within MARGIN of the oracle's k-th logit."""
+    kth = np.sort(logits)[::-1][k - 1]
+    return len(set(gpu_ids.tolist())) == k and bool(np.all(logits[gpu_ids] >= kth - MARGIN))
