@@ -160,6 +160,80 @@ def cpu_oracle_step(layers, emb, x, draft_seed, log_prefix="[oracle]"):
     return compute, a, nxt, oracle.num_threads()
 
 
+# ---------------------------------------------------------------- phase trace
+TRACE_POINTS = ("layer start", "norm/router partials", "partials reduced", "activation terms",
+                "shared gate/up done", "barrier 1 passed", "routing known", "routed gate/up done",
+                "barrier 2 passed", "down done")
+NTP = len(TRACE_POINTS)
+TRACE_STAGES = 48
+
+
+def write_phase_trace(path, fgm, layers, emb, x, draft, ws, arr, dev):
+    """One traced verify step: per layer and phase, the time at which the last
+    CTA (and the median CTA) reached each phase boundary, relative to the
+    first CTA starting the layer, averaged over the layers; then CTA 0's ring
+    stages of two layers."""
+    import torch
+    G = torch.cuda.get_device_properties(dev).multi_processor_count
+    n = (N_LAYERS * NTP + 2) * G + N_LAYERS * TRACE_STAGES * 8
+    buf = torch.zeros(n, dtype=torch.int64, device=dev)
+    fgm.set_phase_trace(buf)
+    t0 = torch.cuda.Event(enable_timing=True)
+    t1 = torch.cuda.Event(enable_timing=True)
+    t0.record()
+    fgm.verify_step(layers, emb, x, draft, ws=ws, _arr=arr)
+    t1.record()
+    torch.cuda.synchronize()
+    fgm.set_phase_trace(None)
+    flat = buf.cpu().double()
+    tr = flat[:(N_LAYERS * NTP + 2) * G].view(-1, G)
+    det = flat[(N_LAYERS * NTP + 2) * G:].view(N_LAYERS, TRACE_STAGES, 8)
+    lines = [f"one traced verify step: {t0.elapsed_time(t1) * 1e3:.1f} us (CUDA events), G = {G} CTAs"]
+    last = [0.0] * NTP
+    med = [0.0] * NTP
+    period = 0.0
+    for l in range(N_LAYERS):
+        base = tr[l * NTP].min()
+        nxt = tr[(l + 1) * NTP].min() if l + 1 < N_LAYERS else tr[N_LAYERS * NTP].min()
+        period += float(nxt - base) / 1e3 / N_LAYERS
+        for k in range(NTP):
+            last[k] += float(tr[l * NTP + k].max() - base) / 1e3 / N_LAYERS
+            med[k] += float(tr[l * NTP + k].median() - base) / 1e3 / N_LAYERS
+    lines.append(f"mean layer period (first CTA to first CTA): {period:.2f} us")
+    lines.append("point                      last CTA (us)   median CTA (us)   from layer start")
+    for k in range(1, NTP):
+        lines.append(f"{TRACE_POINTS[k]:26s} {last[k]:12.2f} {med[k]:16.2f}")
+    tail = tr[N_LAYERS * NTP + 1].max() - tr[N_LAYERS * NTP].min()
+    lines.append(f"lm_head + accept (last CTA end - first CTA after layers): {float(tail) / 1e3:.2f} us")
+    for l in (1, N_LAYERS // 2):
+        base = float(det[l, 0, 7])
+        lines.append(f"CTA 0, layer {l}: stage  issue  landed  products  released  epilogue"
+                     f"  (SM cycles from its layer start)")
+        for k in range(TRACE_STAGES):
+            row = det[l, k]
+            if row[1] == 0:
+                break
+            vals = ["%8d" % int(float(v) - base) if v != 0 else "       -" for v in row[:5]]
+            lines.append(f"  {k:3d}  " + "  ".join(vals))
+    with open(path, "w") as f:
+        f.write("\n".join(lines) + "\n")
+    log("\n".join(lines[:NTP + 3]))
+
+
+# ---------------------------------------------------------------- replicas
+def reduce_over_ranks(total_ms, tokens, e2e_s, e2e_tokens, device):
+    """Whole-job numbers of N independent replicas: the slowest rank's time and
+    the tokens of all ranks (torch.distributed all_gather; NCCL on GPUs, gloo
+    in the CPU tests)."""
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([total_ms, tokens, e2e_s, e2e_tokens], dtype=torch.float64, device=device)
+    parts = [torch.zeros_like(t) for _ in range(dist.get_world_size())]
+    dist.all_gather(parts, t)
+    return (max(float(q[0]) for q in parts), sum(float(q[1]) for q in parts),
+            max(float(q[2]) for q in parts), sum(float(q[3]) for q in parts))
+
+
 # ---------------------------------------------------------------- our arm
 def run_ours(args, rank, world):
     import torch
@@ -171,6 +245,7 @@ def run_ours(args, rank, world):
     dev = torch.device("cuda", int(os.environ.get("LOCAL_RANK", 0)))
     torch.cuda.set_device(dev)
     fgm.lib()
+    fgm.select_path(fgm.PATH_FUSED if args.path == "fused" else fgm.PATH_STAGED)
     layers, emb, xs = make_workload(dev)
     arr = fgm.layers_array(layers)
     ws = fgm.Workspace(dev)
@@ -215,6 +290,9 @@ def run_ours(args, rank, world):
     tokens = int(acc[:, 0].sum()) + K
     bytes_total = sum(step_bytes[i % N_BATCHES] for i in range(K))
 
+    if args.phase_trace:
+        write_phase_trace(args.phase_trace, fgm, layers, emb, xs[0], drafts[0], ws, arr, dev)
+
     # end to end through the host-buffer entry point
     x_h = [x.cpu().pin_memory() for x in xs]
     d_h = [d.cpu().pin_memory() for d in drafts]
@@ -229,15 +307,10 @@ def run_ours(args, rank, world):
         e2e_tokens += int(o_h[0]) + 1
     e2e_s = time.perf_counter() - t0
 
-    # max over ranks
+    # max time and summed tokens over ranks (replicas)
     if world > 1:
-        t = torch.tensor([total_ms, tokens, e2e_s, e2e_tokens, bytes_total], dtype=torch.float64, device=dev)
-        parts = [torch.zeros_like(t) for _ in range(world)]
-        torch.distributed.all_gather(parts, t)
-        total_ms_max = max(float(p[0]) for p in parts)
-        tokens_all = sum(float(p[1]) for p in parts)
-        e2e_max = max(float(p[2]) for p in parts)
-        e2e_tok_all = sum(float(p[3]) for p in parts)
+        total_ms_max, tokens_all, e2e_max, e2e_tok_all = reduce_over_ranks(
+            total_ms, tokens, e2e_s, e2e_tokens, dev)
     else:
         total_ms_max, tokens_all, e2e_max, e2e_tok_all = total_ms, tokens, e2e_s, e2e_tokens
     if rank != 0:
@@ -271,8 +344,10 @@ def run_ours(args, rank, world):
         "accepted_per_step": round((tokens - K) / K, 3),
         "p50_ms": round(statistics.median(per_step), 4),
         "p99_ms": round(sorted(per_step)[min(K - 1, int(0.99 * K))], 4),
+        "path": args.path,
         "roofline": {
-            "kernel": "verify step (all launches of one step)",
+            "kernel": ("k_fused (one persistent launch per step)" if args.path == "fused"
+                       else "verify step (all launches of one step)"),
             "bound": "hbm",
             "achieved": round(achieved, 1),
             "peak": peak,
@@ -284,7 +359,7 @@ def run_ours(args, rank, world):
         },
         "e2e": {"value": round(e2e_tok_all / e2e_max, 2), "unit": "tokens/s",
                 "h2d_bytes_per_step": M * 2816 * 2 + GAMMA * 4, "d2h_bytes_per_step": 8},
-        "gpu_launches": K * (1 + N_LAYERS * 5 + 3),
+        "gpu_launches": K * (1 if args.path == "fused" else 1 + N_LAYERS * 5 + 3),
         "clocks": {"sm_mhz": clocks["sm_mhz"], "sm_max_mhz": clocks["sm_max_mhz"],
                    "reasons": clocks["reasons"]},
         "status": status,
@@ -296,6 +371,63 @@ def run_ours(args, rank, world):
                                 "sample": "one full verify step (30 layers + lm_head + accept) on batch 0; "
                                           "host weight copies untimed"}
     return line
+
+
+# ---------------------------------------------------------------- single-stage cases
+def run_case(args):
+    """One stage alone, for profiling: `layer` = one MoE layer at M = 5 with the
+    Zipf(1.1) bias (four weight copies and eight inputs rotate, so L2 never
+    serves a repeated expert); `lm_head` = the 262,144-word lm_head argmax at
+    M = 5. Prints a JSON line with the stage's HBM GB/s."""
+    import torch
+
+    import fine_grained_moe_gb300 as fgm
+    import synth
+    from fine_grained_moe_gb300 import traffic
+
+    dev = torch.device("cuda", 0)
+    torch.cuda.set_device(dev)
+    fgm.lib()
+    fgm.select_path(fgm.PATH_FUSED if args.path == "fused" else fgm.PATH_STAGED)
+    ws = fgm.Workspace(dev)
+    xs = [synth.hidden_states(HIDDEN_SEED0 + b, M, device=dev) for b in range(N_BATCHES)]
+    K, W = args.steps, args.warmup
+    if args.case == "layer":
+        copies = [synth.layer(1 + c, device=dev, s=S_ZIPF) for c in range(4)]
+        ids = torch.empty((M, 8), dtype=torch.int32, device=dev)
+        calls, nbytes = [], []
+        for i in range(max(K, W)):
+            p, x = copies[i % 4], xs[i % N_BATCHES]
+            fgm.moe_layer_fwd(p, x, topk_ids=ids, ws=ws)
+            u = len(torch.unique(ids.cpu()))
+            nbytes.append(traffic.step_bytes([u], with_lm_head=False))
+            calls.append((p, x))
+        run = lambda i: fgm.moe_layer_fwd(calls[i][0], calls[i][1], ws=ws)
+        unit_bytes = nbytes
+        name = "one MoE layer, M=5, Zipf s=1.1 (4 weight copies rotate)"
+    else:
+        emb = synth.embedding(EMB_SEED, device=dev)
+        am = torch.empty(M, dtype=torch.int32, device=dev)
+        run = lambda i: fgm.lm_head_argmax(emb, xs[i % N_BATCHES], argmax=am, ws=ws)
+        unit_bytes = [traffic.lm_head_bytes()] * max(K, W)
+        name = "lm_head argmax, 262144 x 2816 bf16, M=5"
+    for i in range(W):
+        run(i)
+    torch.cuda.synchronize()
+    stream = torch.cuda.current_stream()
+    ev = [torch.cuda.Event(enable_timing=True) for _ in range(K + 1)]
+    ev[0].record(stream)
+    for i in range(K):
+        run(i)
+        ev[i + 1].record(stream)
+    torch.cuda.synchronize()
+    times = [ev[i].elapsed_time(ev[i + 1]) for i in range(K)]
+    gbs = sum(unit_bytes[:K]) / (sum(times) * 1e-3) / 1e9
+    peak, kind = measured_peaks()
+    return {"case": args.case, "workload": name, "path": args.path, "steps": K, "warmup": W,
+            "ms_per_call": round(statistics.mean(times), 4), "hbm_gbs": round(gbs, 1),
+            "frac_of_peak": round(gbs / peak, 4), "peak": peak, "peak_kind": kind,
+            "status": ws.status()}
 
 
 # ---------------------------------------------------------------- reference arm
@@ -366,6 +498,12 @@ def main():
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=("ours", "reference"), default="ours")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--path", choices=("fused", "staged"), default="fused",
+                    help="persistent kernel (default) or one launch per stage")
+    ap.add_argument("--phase-trace", metavar="PATH", default=None,
+                    help="after timing, run one traced step and write a per-phase summary to PATH")
+    ap.add_argument("--case", choices=("verify", "layer", "lm_head"), default="verify",
+                    help="verify: the headline step; layer / lm_head: one stage alone (profiling)")
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")
@@ -376,7 +514,12 @@ def main():
         torch.cuda.set_device(int(os.environ.get("LOCAL_RANK", 0)))
         torch.distributed.init_process_group("nccl")
     try:
-        line = run_reference(args, rank, world) if args.impl == "reference" else run_ours(args, rank, world)
+        if args.impl == "reference":
+            line = run_reference(args, rank, world)
+        elif args.case != "verify":
+            line = run_case(args)
+        else:
+            line = run_ours(args, rank, world)
     finally:
         if world > 1 and args.impl == "ours":
             import torch

@@ -30,6 +30,8 @@ MAX_LAYERS = 48
 
 STATUS_NONFINITE_LOGITS = 1
 STATUS_WAIT_TIMEOUT = 2
+PATH_FUSED = 0    # one persistent cooperative kernel per call (TMA ring + mma.sync tiles)
+PATH_STAGED = 1   # one launch per stage, fp32 CUDA-core arithmetic
 
 _PKG = os.path.dirname(os.path.abspath(__file__))
 LIB_PATH = os.path.join(_PKG, "libfgm.so")
@@ -65,6 +67,11 @@ def lib() -> ctypes.CDLL:
             "fgm_verify_step": (ci, [LP, ci, vp, i64, vp, vp, ci, vp, vp, vp, sz, vp]),
             "fgm_verify_step_host": (ci, [LP, ci, vp, i64, vp, vp, ci, vp, vp, sz, vp]),
             "fgm_read_status": (ci, [vp, sz, ci, vp, vp]),
+            "fgm_select_path": (ci, [ci]),
+            "fgm_set_phase_trace": (ci, [vp, sz]),
+            "fgm_debug_stall_next_launch": (ci, []),
+            "fgm_read_wait_report": (ci, [vp, sz, vp, vp]),
+            "fgm_set_wait_limit_ns": (ctypes.c_longlong, [ctypes.c_longlong]),
             "fgm_last_error": (ctypes.c_char_p, []),
             "fgm_version": (ci, []),
         }
@@ -103,6 +110,33 @@ def _m(x: torch.Tensor) -> int:
     return int(x.shape[0])
 
 
+def select_path(path: int) -> int:
+    """Selects the execution path (PATH_FUSED or PATH_STAGED); returns the previous one."""
+    return int(lib().fgm_select_path(int(path)))
+
+
+def set_wait_limit_ns(ns: int) -> int:
+    """Bound on every wait inside the persistent kernel (ns < 0 only queries)."""
+    return int(lib().fgm_set_wait_limit_ns(int(ns)))
+
+
+def set_phase_trace(buf: torch.Tensor | None) -> None:
+    """Profiling aid: record per-CTA phase timestamps of later persistent-kernel
+    launches into an int64 CUDA tensor (None stops)."""
+    if buf is None:
+        _check(lib().fgm_set_phase_trace(None, 0))
+    else:
+        if buf.dtype != torch.int64:
+            raise FgmError("trace buffer must be int64")
+        _check(lib().fgm_set_phase_trace(_ptr(buf), buf.numel()))
+
+
+def debug_stall_next_launch() -> None:
+    """Test hook: the next persistent-kernel launch waits on a barrier that can
+    never complete, so its wait limit must run out."""
+    _check(lib().fgm_debug_stall_next_launch())
+
+
 def workspace_bytes(M: int = MAX_M, V: int = 0) -> int:
     return int(lib().fgm_workspace_bytes(int(M), int(V)))
 
@@ -120,6 +154,12 @@ class Workspace:
     @property
     def ptr(self):
         return _ptr(self.t)
+
+    def wait_report(self) -> list[int]:
+        """{site, block, warp, index} of the first wait that ran out (see fgm.h)."""
+        out = (ctypes.c_int32 * 4)()
+        _check(lib().fgm_read_wait_report(self.ptr, self.nbytes, out, _stream(None)))
+        return list(out)
 
     def status(self, clear: bool = True) -> int:
         out = ctypes.c_int32(0)

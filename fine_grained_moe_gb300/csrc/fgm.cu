@@ -6,6 +6,7 @@
 #include <string.h>
 
 #include "basic_kernels.cuh"
+#include "fused_step.cuh"
 
 namespace fgm {
 namespace {
@@ -42,7 +43,14 @@ struct DeviceInfo {
     bool ready = false;
     bool ok = false;
     int sms = 0;
+    int fused_grid = 0;   // CTAs of the persistent kernel (one per SM), 0 if it cannot be co-resident
 };
+
+int g_path = FGM_PATH_FUSED;
+long long g_timeout_ns = 2000000000LL;
+long long *g_trace = nullptr;
+int g_debug_stall = 0;
+size_t g_trace_n = 0;
 DeviceInfo g_dev[kMaxDevices];
 
 // Checks (once per device) that the current device is an sm_103 GPU and
@@ -79,6 +87,12 @@ int device_ready(int *sms)
             FGM_SMEM(k_lmhead_basic<7>, 7 * kH * 4);
             FGM_SMEM(k_lmhead_basic<8>, 8 * kH * 4);
 #undef FGM_SMEM
+            FGM_CUDA(cudaFuncSetAttribute(fused::k_fused, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                          (int)sizeof(fused::Smem)));
+            int per_sm = 0;
+            FGM_CUDA(cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, fused::k_fused, fused::kThreads,
+                                                                   sizeof(fused::Smem)));
+            d.fused_grid = (per_sm >= 1 && d.sms >= fused::kMinCtas) ? d.sms : 0;
         }
         d.ready = true;
     }
@@ -87,6 +101,44 @@ int device_ready(int *sms)
     if (sms)
         *sms = d.sms;
     return FGM_OK;
+}
+
+int fused_grid()
+{
+    int dev = 0;
+    FGM_CUDA(cudaGetDevice(&dev));
+    const int G = g_dev[dev].fused_grid;
+    if (G <= 0)
+        return fail(FGM_ERR_DEVICE, "the persistent kernel cannot be resident on this device");
+    return G;
+}
+
+// Launches the persistent kernel (cooperative: all CTAs co-resident).
+int launch_fused(fused::Params &prm, cudaStream_t st)
+{
+    const int G = fused_grid();
+    if (G < 0)
+        return G;
+    prm.timeout_ns = g_timeout_ns;
+    const int n_l = prm.mode == fused::kModeLayer ? 1 : prm.mode == fused::kModeLmHead ? 0 : prm.n_layers;
+    const size_t need = (size_t)(n_l * fused::kTracePoints + 2) * G + (size_t)n_l * fused::kTraceStages * fused::kTraceDetail;
+    prm.trace = (g_trace && g_trace_n >= need) ? g_trace : nullptr;
+    prm.debug_stall = g_debug_stall;
+    g_debug_stall = 0;
+    void *args[] = {&prm};
+    FGM_CUDA(cudaLaunchCooperativeKernel(reinterpret_cast<const void *>(fused::k_fused), dim3(G),
+                                         dim3(fused::kThreads), args, sizeof(fused::Smem), st));
+    return FGM_OK;
+}
+
+fused::Params fused_params(int mode, int M, const Ws &w)
+{
+    fused::Params prm;
+    memset(&prm, 0, sizeof prm);
+    prm.mode = mode;
+    prm.M = M;
+    prm.ws = w;
+    return prm;
 }
 
 bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
@@ -233,6 +285,19 @@ int verify_step_impl(const fgm_layer *layers, int n_layers, const uint16_t *emb,
                      void *ws, cudaStream_t st, int sms)
 {
     Ws w = ws_carve(ws);
+    if (g_path == FGM_PATH_FUSED) {
+        fused::Params prm = fused_params(fused::kModeVerify, M, w);
+        for (int l = 0; l < n_layers; ++l)
+            prm.layers[l] = layers[l];
+        prm.n_layers = n_layers;
+        prm.x = x;
+        prm.emb = emb;
+        prm.V = V;
+        prm.draft = draft;
+        prm.argmax = argmax;
+        prm.out = out;
+        return launch_fused(prm, st);
+    }
     k_bf16_to_f32<<<8, 256, 0, st>>>(x, M * kH, w.h);
     FGM_CHECK_LAUNCH();
     FGM_TRY(run_stack(layers, n_layers, M, w, nullptr, st));
@@ -279,6 +344,16 @@ int fgm_moe_layer_fwd(const fgm_layer *layer, const uint16_t *x, uint16_t *y, in
     FGM_TRY(device_ready(&sms));
     cudaStream_t st = static_cast<cudaStream_t>(stream);
     Ws w = ws_carve(ws);
+    if (g_path == FGM_PATH_FUSED) {
+        fused::Params prm = fused_params(fused::kModeLayer, M, w);
+        prm.layers[0] = *layer;
+        prm.n_layers = 1;
+        prm.x = x;
+        prm.y = y;
+        prm.ids = topk_ids;
+        prm.wts = topk_w;
+        return launch_fused(prm, st);
+    }
     k_layer_prep<<<16, 256, 0, st>>>(x, M, w.xn, w.acc);
     FGM_CHECK_LAUNCH();
     FGM_TRY(run_layer(M, layer, w, w.acc, topk_ids, topk_w, st));
@@ -299,6 +374,16 @@ int fgm_moe_stack_fwd(const fgm_layer *layers, int n_layers, const uint16_t *x, 
     FGM_TRY(device_ready(&sms));
     cudaStream_t st = static_cast<cudaStream_t>(stream);
     Ws w = ws_carve(ws);
+    if (g_path == FGM_PATH_FUSED) {
+        fused::Params prm = fused_params(fused::kModeStack, M, w);
+        for (int l = 0; l < n_layers; ++l)
+            prm.layers[l] = layers[l];
+        prm.n_layers = n_layers;
+        prm.x = x;
+        prm.y = y;
+        prm.ids = ids_trace;
+        return launch_fused(prm, st);
+    }
     k_bf16_to_f32<<<8, 256, 0, st>>>(x, M * kH, w.h);
     FGM_CHECK_LAUNCH();
     FGM_TRY(run_stack(layers, n_layers, M, w, ids_trace, st));
@@ -319,6 +404,15 @@ int fgm_lm_head_argmax(const uint16_t *emb, int64_t V, const uint16_t *h, int M,
     FGM_TRY(device_ready(&sms));
     cudaStream_t st = static_cast<cudaStream_t>(stream);
     Ws w = ws_carve(ws);
+    if (g_path == FGM_PATH_FUSED) {
+        fused::Params prm = fused_params(fused::kModeLmHead, M, w);
+        prm.x = h;
+        prm.emb = emb;
+        prm.V = V;
+        prm.argmax = argmax;
+        prm.maxlogit = maxlogit;
+        return launch_fused(prm, st);
+    }
     const int G = lmhead_grid(sms);
     FGM_TRY(launch_lmhead(M, emb, V, h, w, G, st));
     k_argmax_final<<<1, 256, 0, st>>>(w.part_val, w.part_idx, G, M, argmax, maxlogit, nullptr, nullptr,
@@ -373,6 +467,47 @@ int fgm_verify_step_host(const fgm_layer *layers, int n_layers, const uint16_t *
         FGM_CUDA(cudaMemcpyAsync(w.io_draft, draft_host, sizeof(int32_t) * (M - 1), cudaMemcpyHostToDevice, st));
     FGM_TRY(verify_step_impl(layers, n_layers, emb, V, w.io_x, w.io_draft, M, nullptr, w.io_out, ws, st, sms));
     FGM_CUDA(cudaMemcpyAsync(out_host, w.io_out, sizeof(int32_t) * 2, cudaMemcpyDeviceToHost, st));
+    FGM_CUDA(cudaStreamSynchronize(st));
+    return FGM_OK;
+}
+
+int fgm_select_path(int path)
+{
+    const int prev = g_path;
+    if (path == FGM_PATH_FUSED || path == FGM_PATH_STAGED)
+        g_path = path;
+    return prev;
+}
+
+int fgm_debug_stall_next_launch(void)
+{
+    g_debug_stall = 1;
+    return FGM_OK;
+}
+
+int fgm_set_phase_trace(long long *buf, size_t n)
+{
+    g_trace = buf;
+    g_trace_n = buf ? n : 0;
+    return FGM_OK;
+}
+
+long long fgm_set_wait_limit_ns(long long ns)
+{
+    const long long prev = g_timeout_ns;
+    if (ns >= 0)
+        g_timeout_ns = ns;
+    return prev;
+}
+
+int fgm_read_wait_report(void *ws, size_t ws_bytes, int32_t *report, void *stream)
+{
+    FGM_TRY(check_ws(ws, ws_bytes, 1, 0));
+    if (!report)
+        return fail(FGM_ERR_INVALID_ARG, "report is NULL");
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    Ws w = ws_carve(ws);
+    FGM_CUDA(cudaMemcpyAsync(report, w.status + 1, 4 * sizeof(int32_t), cudaMemcpyDeviceToHost, st));
     FGM_CUDA(cudaStreamSynchronize(st));
     return FGM_OK;
 }

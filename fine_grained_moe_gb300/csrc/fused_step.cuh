@@ -1,0 +1,1357 @@
+// Persistent verify-step kernel: one cooperative launch runs every layer of
+// the MoE stack (and, for the verify step, the lm_head argmax and greedy
+// accept) with grid-wide barriers between the phases of a layer.
+//
+// CTA layout: one CTA per SM; 11 MMA warps and 1 producer warp.
+//  * The producer warp streams weight rows from HBM into a 3-slot shared
+//    memory ring with cp.async.bulk (TMA bulk copies) completing on mbarriers.
+//    Weight loads never depend on activations, so the producer runs ahead of
+//    the consumers across grid barriers; it only waits for the routing of a
+//    layer before fetching that layer's routed experts.
+//  * MMA warps split K: warp w owns a fixed 256-byte (gate/up, lm_head) or
+//    64-byte (down) slice of every row and keeps the activations of that
+//    slice in registers as mma B fragments. Each weight tile is 16 rows; the
+//    products run on the tensor cores (mma.sync m16n8k32 E4M3 for experts,
+//    m16n8k16 bf16 for the lm_head) with the M <= 8 tokens as the n = 8
+//    dimension. The 11 partials of a stage meet in shared memory; after a
+//    barrier of the MMA warps, 32 threads per tile sum them and apply the
+//    epilogue (row scales, gated GELU and router weight for gate/up; row
+//    scales and fp32 atomic accumulation into the residual for down; a
+//    running argmax per token for the lm_head).
+//  * Experts read E4M3 weights as they are stored; the fp32 activations are
+//    written as a sum of 3 E4M3 terms (each the rounding residual of the
+//    previous one times 16) under a power-of-two scale per warp and token,
+//    so products are exact and each activation carries <= 2^-12 relative
+//    error (twice finer than an f16 rounding).
+//
+// Phases of layer l (every CTA):
+//  A  RMSNorm of h (stack) -> activation terms; CTA e < 128 computes router
+//     logit e; the shared expert's gate/up rows (split over all CTAs).
+//  -- grid barrier
+//  B  softmax/top-8/renormalise + distinct-expert list (every CTA, same
+//     result); routed gate/up rows split evenly over CTAs by row pairs.
+//  -- grid barrier
+//  C  down rows of every distinct expert and the shared one, split evenly;
+//     results (already weighted by the router) are added into the fp32
+//     residual h with atomics.
+//  -- grid barrier
+// Verify step: final RMSNorm -> bf16, lm_head rows split over CTAs with a
+// running argmax per token, then the last CTA to finish reduces the per-CTA
+// winners and applies the greedy accept rule (no waiting involved).
+#pragma once
+
+#include "common.cuh"
+
+namespace fgm {
+namespace fused {
+
+constexpr int kMW = 11;                       // MMA warps (K-slices)
+constexpr int kProdWarp = kMW;                // producer warp index
+constexpr int kConsumers = kMW * 32;          // 352
+constexpr int kThreads = kConsumers + 32;     // 384
+constexpr int kStages = 4;                    // ring slots
+constexpr int kRowStride = 2880;              // smem stride of a 2816-byte row (conflict-free 16-byte reads)
+constexpr int kSlotBytes = 16 * kRowStride;   // 46080
+constexpr int kDownTiles = 4;                 // 16-row down tiles per ring slot (64 x 704 bytes)
+constexpr int kTerms = 3;                     // E4M3 terms per activation
+constexpr int kSharedSlot = kMaxSlots - 1;
+constexpr int kMinCtas = 128;                 // the persistent kernel needs at least this many SMs
+constexpr int kMaxGuRows = (kMaxSlots - 1) * kF / kMinCtas + 2;   // routed row pairs per CTA
+constexpr int kMaxDownRows = kMaxSlots * kH / kMinCtas + 2;       // down rows per CTA
+
+enum Mode { kModeLayer = 0, kModeStack = 1, kModeVerify = 2, kModeLmHead = 3 };
+enum TileKind { kTileGateUp = 0, kTileDown = 1, kTileLmHead = 2 };
+
+struct Params {
+    fgm_layer layers[FGM_MAX_LAYERS];
+    int n_layers;
+    int M;
+    int mode;
+    const uint16_t *x;      // bf16 [M][2816] input (lm_head mode: the hidden states)
+    uint16_t *y;            // bf16 [M][2816] output (layer / stack)
+    const uint16_t *emb;    // bf16 [V][2816] (verify, lm_head)
+    int64_t V;
+    const int32_t *draft;   // [M-1] (verify)
+    int32_t *argmax;        // [M] (verify, lm_head)
+    float *maxlogit;        // [M] (lm_head, optional)
+    int32_t *out;           // [2] (verify)
+    int32_t *ids;           // layer: [M][8]; stack/verify: [L][M][8] trace; optional
+    float *wts;             // layer: [M][8]; optional
+    Ws ws;
+    long long timeout_ns;
+    long long *trace;       // optional: %globaltimer stamps (see kTracePoints)
+    int debug_stall;        // test hook: add one grid barrier that can never complete
+};
+
+// Profiling aid (Params::trace): per layer kTracePoints phase stamps for every
+// CTA, [(l * kTracePoints + k) * G + cta], then two end stamps per CTA, then
+// for CTA 0 only a per-stage timeline [l][kTraceStages][8] of SM clock64
+// values = {producer issue, data landed, products done, slot released,
+// epilogue done, -, -, layer start}.
+constexpr int kTracePoints = 10;
+constexpr int kTraceStages = 48;
+constexpr int kTraceDetail = 8;
+
+struct __align__(128) Smem {
+    uint8_t ring[kStages][kSlotBytes];
+    float4 red[kMW][kDownTiles][32];   // per-warp K-slice partials of up to 4 tiles
+    float part[kMW][8];
+    float part2[kMW][8];
+    float best_v[kMW][8];       // lm_head winners per reducing warp and token
+    int32_t best_i[kMW][8];
+    float comb[2][kMaxSlots][8];
+    int32_t experts[2][kMaxSlots];
+    int32_t n_unique[2];
+    int32_t tk_ids[8][8];
+    float tk_w[8][8];
+    int32_t mark[kE];
+    int32_t slot_of[kE];
+    float sc_g[kMaxGuRows + 8]; // gate/up row scales of this CTA's routed rows, then (from
+    float sc_u[kMaxGuRows + 8]; // kMaxGuRows) its shared-expert rows
+    float sc_d[kMaxDownRows];   // down row scales of this CTA's down rows of the layer
+    unsigned long long full[kStages];
+    unsigned long long empty[kStages];
+    unsigned long long route;
+    int abort;
+    int last;
+};
+
+// ---------------------------------------------------------------- primitives
+
+__device__ __forceinline__ uint32_t su32(const void *p) { return static_cast<uint32_t>(__cvta_generic_to_shared(p)); }
+
+__device__ __forceinline__ long long gtime()
+{
+    long long t;
+    asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+    return t;
+}
+
+__device__ __forceinline__ void mbar_init(unsigned long long *b, int count)
+{
+    asm volatile("mbarrier.init.shared.b64 [%0], %1;" ::"r"(su32(b)), "r"(count));
+}
+
+__device__ __forceinline__ void mbar_expect_tx(unsigned long long *b, uint32_t bytes)
+{
+    asm volatile("mbarrier.arrive.expect_tx.shared.b64 _, [%0], %1;" ::"r"(su32(b)), "r"(bytes) : "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive(unsigned long long *b)
+{
+    asm volatile("mbarrier.arrive.shared.b64 _, [%0];" ::"r"(su32(b)) : "memory");
+}
+
+__device__ __forceinline__ bool mbar_try(unsigned long long *b, uint32_t parity)
+{
+    uint32_t ok;
+    asm volatile(
+        "{\n.reg .pred p;\nmbarrier.try_wait.parity.shared.b64 p, [%1], %2;\nselp.u32 %0, 1, 0, p;\n}\n"
+        : "=r"(ok)
+        : "r"(su32(b)), "r"(parity)
+        : "memory");
+    return ok != 0;
+}
+
+// Bounded wait: gives up when the CTA's abort flag is raised or the kernel's
+// deadline passes (then raises the abort flag and the status bit).
+// On timeout the first wait to give up records where: status[1] = site, status[2] =
+// block, status[3] = warp, status[4] = the stage/post index it waited for.
+__device__ __forceinline__ bool mbar_wait(unsigned long long *b, uint32_t parity, Smem &s,
+                                          long long deadline, int32_t *status, int site = 0, int index = 0)
+{
+    for (int it = 0;; ++it) {
+        if (mbar_try(b, parity))
+            return true;
+        if ((it & 15) == 15) {
+            if (*reinterpret_cast<volatile int *>(&s.abort))
+                return false;
+            if (gtime() > deadline) {
+                *reinterpret_cast<volatile int *>(&s.abort) = 1;
+                if (atomicOr(status, FGM_STATUS_WAIT_TIMEOUT) == 0) {
+                    status[1] = site;
+                    status[2] = blockIdx.x;
+                    status[3] = threadIdx.x >> 5;
+                    status[4] = index;
+                }
+                return false;
+            }
+        }
+    }
+}
+
+// 16-byte shared-memory load as volatile asm: it keeps its place ahead of the
+// (volatile) mma instructions that consume it, so all of a stage's loads are
+// in flight before the first product instead of one chunk at a time.
+__device__ __forceinline__ uint4 lds128(const void *p)
+{
+    uint4 v;
+    asm volatile("ld.shared.v4.u32 {%0,%1,%2,%3}, [%4];"
+                 : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+                 : "r"(static_cast<uint32_t>(__cvta_generic_to_shared(p))));
+    return v;
+}
+
+// Starts an asynchronous HBM -> L2 copy (no completion tracking).
+__device__ __forceinline__ void prefetch_l2(const void *src, uint32_t bytes)
+{
+    asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(src), "r"(bytes) : "memory");
+}
+
+__device__ __forceinline__ void bulk_g2s(void *dst, const void *src, uint32_t bytes, unsigned long long *bar)
+{
+    asm volatile(
+        "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(su32(dst)),
+        "l"(src), "r"(bytes), "r"(su32(bar))
+        : "memory");
+}
+
+// Named barrier of the MMA warps (the producer never joins).
+__device__ __forceinline__ void consumer_sync() { asm volatile("bar.sync 1, %0;" ::"n"(kConsumers) : "memory"); }
+
+__device__ __forceinline__ float4 ldcg4(const float *p) { return __ldcg(reinterpret_cast<const float4 *>(p)); }
+
+__device__ __forceinline__ void mma_e4m3(float (&c)[4], const uint32_t (&a)[4], uint32_t b0, uint32_t b1)
+{
+    asm volatile(
+        "mma.sync.aligned.m16n8k32.row.col.f32.e4m3.e4m3.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, "
+        "{%0,%1,%2,%3};\n"
+        : "+f"(c[0]), "+f"(c[1]), "+f"(c[2]), "+f"(c[3])
+        : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
+}
+
+__device__ __forceinline__ void mma_bf16(float (&c)[4], const uint32_t (&a)[4], uint32_t b0, uint32_t b1)
+{
+    asm volatile(
+        "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, "
+        "{%0,%1,%2,%3};\n"
+        : "+f"(c[0]), "+f"(c[1]), "+f"(c[2]), "+f"(c[3])
+        : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
+}
+
+// Power-of-two scale S with max|v| * S < 256 (S = 1 for an all-zero slice).
+__device__ __forceinline__ float term_scale(float amax)
+{
+    if (!(amax > 0.0f) || !isfinite(amax))
+        return 1.0f;
+    int e = static_cast<int>((__float_as_uint(amax) >> 23) & 0xFF) - 126;  // amax in [2^(e-1), 2^e)
+    e = max(e, -118);                                                      // subnormal maxima: S <= 2^126
+    return exp2f(static_cast<float>(8 - e));
+}
+
+// Writes 16 values as kTerms E4M3 terms: term t holds the E4M3 rounding of
+// y_t, with y_0 = v * S and y_{t+1} = (y_t - term_t) * 16 (exact in fp32),
+// so sum_t term_t / (S * 16^t) = v up to 2^-(4 kTerms) relative. b[t][j] packs
+// elements 4j..4j+3 (element 4j in the low byte).
+__device__ __forceinline__ void split_terms16(const float (&v)[16], float S, uint32_t (&b)[kTerms][4])
+{
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+        float y[4];
+#pragma unroll
+        for (int i = 0; i < 4; ++i)
+            y[i] = v[4 * j + i] * S;
+#pragma unroll
+        for (int t = 0; t < kTerms; ++t) {
+            const __nv_fp8x2_storage_t lo = __nv_cvt_float2_to_fp8x2(make_float2(y[0], y[1]), __NV_SATFINITE, __NV_E4M3);
+            const __nv_fp8x2_storage_t hi = __nv_cvt_float2_to_fp8x2(make_float2(y[2], y[3]), __NV_SATFINITE, __NV_E4M3);
+            b[t][j] = static_cast<uint32_t>(lo) | (static_cast<uint32_t>(hi) << 16);
+            if (t + 1 < kTerms) {
+                const float2 dl = __half22float2(__half2(__nv_cvt_fp8x2_to_halfraw2(lo, __NV_E4M3)));
+                const float2 dh = __half22float2(__half2(__nv_cvt_fp8x2_to_halfraw2(hi, __NV_E4M3)));
+                y[0] = (y[0] - dl.x) * 16.0f;
+                y[1] = (y[1] - dl.y) * 16.0f;
+                y[2] = (y[2] - dh.x) * 16.0f;
+                y[3] = (y[3] - dh.y) * 16.0f;
+            }
+        }
+    }
+}
+
+struct Terms16 {
+    uint32_t w[kTerms][4];
+};
+
+// Out-of-line form of split_terms16 (one copy of the code for all callers).
+__device__ __noinline__ Terms16 split16(float4 a, float4 b, float4 c, float4 d, float S)
+{
+    const float v[16] = {a.x, a.y, a.z, a.w, b.x, b.y, b.z, b.w, c.x, c.y, c.z, c.w, d.x, d.y, d.z, d.w};
+    Terms16 t;
+    split_terms16(v, S, t.w);
+    return t;
+}
+
+__device__ __forceinline__ void split16_into(const float (&v)[16], float S, uint32_t (&b)[kTerms][4])
+{
+    const Terms16 t = split16(make_float4(v[0], v[1], v[2], v[3]), make_float4(v[4], v[5], v[6], v[7]),
+                              make_float4(v[8], v[9], v[10], v[11]), make_float4(v[12], v[13], v[14], v[15]), S);
+#pragma unroll
+    for (int k = 0; k < kTerms; ++k)
+#pragma unroll
+        for (int j = 0; j < 4; ++j)
+            b[k][j] = t.w[k][j];
+}
+
+// Max over the 4 lanes that share a token (lane = 4 g + q).
+__device__ __forceinline__ float quad_max(float v)
+{
+    v = fmaxf(v, __shfl_xor_sync(0xFFFFFFFFu, v, 1));
+    return fmaxf(v, __shfl_xor_sync(0xFFFFFFFFu, v, 2));
+}
+
+__device__ __forceinline__ float quad_sum(float v)
+{
+    v += __shfl_xor_sync(0xFFFFFFFFu, v, 1);
+    return v + __shfl_xor_sync(0xFFFFFFFFu, v, 2);
+}
+
+// Term weights for the two token columns (2q, 2q+1) a thread's accumulator
+// holds: inv[t][0/1] = 1 / (S_col * 16^t). S of token g lives in lanes 4g..4g+3.
+__device__ __forceinline__ void column_inv(float S, int q, float (&inv)[kTerms][2])
+{
+    const float s0 = __shfl_sync(0xFFFFFFFFu, S, 8 * q);
+    const float s1 = __shfl_sync(0xFFFFFFFFu, S, 8 * q + 4);
+    float f = 1.0f;
+#pragma unroll
+    for (int t = 0; t < kTerms; ++t) {
+        inv[t][0] = f / s0;
+        inv[t][1] = f / s1;
+        f *= 0.0625f;
+    }
+}
+
+// ---------------------------------------------------------------- work plans
+// Both the producer and the consumers walk the same sequence of ring stages.
+
+struct Range {
+    int begin, end;
+};
+
+__device__ __forceinline__ Range split(long long total, int part, int parts)
+{
+    return Range{static_cast<int>(total * part / parts), static_cast<int>(total * (part + 1) / parts)};
+}
+
+// Down-phase stages of one CTA: the CTA's row range of the (slot, row) space
+// cut at every 64-row boundary of a slot. CTAs visit their stages in a
+// rotated order so that CTAs working on different experts add into different
+// rows of the residual at any moment.
+struct DownStages {
+    int begin, end;   // CTA range in the flattened (slot, row) space
+    int k0, n, rot;   // first 64-row block, number of blocks, rotation
+    __device__ DownStages(int U, int cta, int G)
+    {
+        const Range r = split((long long)(U + 1) * kH, cta, G);
+        begin = r.begin;
+        end = r.end;
+        constexpr int kBlk = kDownTiles * 16;   // 64 rows
+        constexpr int kBlocksPerSlot = kH / kBlk;
+        const int first = (begin / kH) * kBlocksPerSlot + (begin % kH) / kBlk;
+        const int last = end > begin ? ((end - 1) / kH) * kBlocksPerSlot + ((end - 1) % kH) / kBlk : first - 1;
+        k0 = first;
+        n = last - first + 1;
+        rot = n > 0 ? (cta * 7) % n : 0;
+    }
+    // i-th stage in visiting order: absolute position and row count
+    __device__ void get(int i, int &pos, int &nv) const
+    {
+        constexpr int kBlk = kDownTiles * 16;
+        constexpr int kBlocksPerSlot = kH / kBlk;
+        const int k = k0 + (i + rot) % n;
+        const int start = (k / kBlocksPerSlot) * kH + (k % kBlocksPerSlot) * kBlk;
+        pos = max(begin, start);
+        nv = min(end, start + kBlk) - pos;
+    }
+};
+
+// Loads the 64 activation values (4 chunks x 16) a consumer thread owns for
+// token g in K-slice `warp` of a 2816-wide row: positions 256 w + 64 c + 16 q + i.
+__device__ __forceinline__ void load_slice_f32(const float *row, int warp, int q, float (&v)[4][16])
+{
+#pragma unroll
+    for (int c = 0; c < 4; ++c) {
+        const float *p = row + 256 * warp + 64 * c + 16 * q;
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+            const float4 f = ldcg4(p + 4 * k);
+            v[c][4 * k + 0] = f.x;
+            v[c][4 * k + 1] = f.y;
+            v[c][4 * k + 2] = f.z;
+            v[c][4 * k + 3] = f.w;
+        }
+    }
+}
+
+__device__ __forceinline__ void load_slice_bf16(const uint16_t *row, int warp, int q, float (&v)[4][16])
+{
+#pragma unroll
+    for (int c = 0; c < 4; ++c) {
+        const uint16_t *p = row + 256 * warp + 64 * c + 16 * q;
+        const uint4 a = *reinterpret_cast<const uint4 *>(p);
+        const uint4 b = *reinterpret_cast<const uint4 *>(p + 8);
+        const uint32_t w[8] = {a.x, a.y, a.z, a.w, b.x, b.y, b.z, b.w};
+#pragma unroll
+        for (int k = 0; k < 8; ++k) {
+            const float2 f = bf16x2_to_f32(w[k]);
+            v[c][2 * k] = f.x;
+            v[c][2 * k + 1] = f.y;
+        }
+    }
+}
+
+// Gate/up ring stage: 16 smem rows (8 gate + 8 up) of 2816 bytes; warp w
+// multiplies its 256-byte K-slice by the activation terms b and leaves the
+// 16 x 8 partial (terms combined) in `out`.
+// A-fragment words of one gate/up or lm_head stage for warp w: chunk c of
+// rows g and g + 8 of the slot (bytes 256 w + 64 c + 16 q).
+__device__ __forceinline__ void load_a_wide(const uint8_t *slot, int warp, int g, int q, uint4 (&ra)[4], uint4 (&rb)[4])
+{
+#pragma unroll
+    for (int c = 0; c < 4; ++c) {
+        ra[c] = lds128(slot + g * kRowStride + 256 * warp + 64 * c + 16 * q);
+        rb[c] = lds128(slot + (g + 8) * kRowStride + 256 * warp + 64 * c + 16 * q);
+    }
+}
+
+// Gate/up products of one 16-row tile over warp w's 256-byte K-slice; the
+// terms are combined with their weights into the 16 x 8 partial `out`.
+__device__ __forceinline__ void gu_products(const uint4 (&ra)[4], const uint4 (&rb)[4], const uint32_t (&b)[4][kTerms][4],
+                                            const float (&inv)[kTerms][2], float (&out)[4])
+{
+    // two accumulator sets (even / odd chunks) halve the dependent mma chains
+    float acc[2][kTerms][4];
+#pragma unroll
+    for (int h = 0; h < 2; ++h)
+#pragma unroll
+        for (int t = 0; t < kTerms; ++t)
+#pragma unroll
+            for (int e = 0; e < 4; ++e)
+                acc[h][t][e] = 0.0f;
+#pragma unroll
+    for (int c = 0; c < 4; ++c) {
+        const uint32_t a0[4] = {ra[c].x, rb[c].x, ra[c].y, rb[c].y};
+        const uint32_t a1[4] = {ra[c].z, rb[c].z, ra[c].w, rb[c].w};
+#pragma unroll
+        for (int t = 0; t < kTerms; ++t) {
+            mma_e4m3(acc[c & 1][t], a0, b[c][t][0], b[c][t][1]);
+            mma_e4m3(acc[c & 1][t], a1, b[c][t][2], b[c][t][3]);
+        }
+    }
+#pragma unroll
+    for (int e = 0; e < 4; ++e) {
+        float v = 0.0f;
+#pragma unroll
+        for (int t = 0; t < kTerms; ++t)
+            v += (acc[0][t][e] + acc[1][t][e]) * inv[t][e & 1];
+        out[e] = v;
+    }
+}
+
+// Sum of the 11 K-slice partials of lane ln of tile t:
+// (row ln/4, cols 2(ln%4), 2(ln%4)+1) in x, y and row ln/4 + 8 in z, w.
+__device__ __forceinline__ float4 red_sum4(const Smem &s, int t, int ln)
+{
+    float4 v = s.red[0][t][ln];
+#pragma unroll
+    for (int w = 1; w < kMW; ++w) {
+        const float4 f = s.red[w][t][ln];
+        v.x += f.x;
+        v.y += f.y;
+        v.z += f.z;
+        v.w += f.w;
+    }
+    return v;
+}
+
+__global__ void __launch_bounds__(kThreads, 1) k_fused(const __grid_constant__ Params p)
+{
+    extern __shared__ __align__(128) uint8_t smem_raw[];
+    Smem &s = *reinterpret_cast<Smem *>(smem_raw);
+    const int G = gridDim.x, cta = blockIdx.x;
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const int g = lane >> 2, q = lane & 3;
+    const int M = p.M;
+    const Ws &ws = p.ws;
+    int32_t *status = ws.status;
+    const long long deadline = gtime() + p.timeout_ns;
+    const bool is_mma = warp < kMW;
+
+    if (tid == 0) {
+        for (int i = 0; i < kStages; ++i) {
+            mbar_init(&s.full[i], 1);
+            mbar_init(&s.empty[i], kMW);
+        }
+        mbar_init(&s.route, 1);
+        s.abort = 0;
+        asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+    }
+    __syncthreads();
+
+    const int n_layers = p.mode == kModeLayer ? 1 : p.mode == kModeLmHead ? 0 : p.n_layers;
+
+    // ============================================================ producer
+    if (warp == kProdWarp) {
+        if (lane == 0) {
+            uint32_t stage = 0;
+            bool ok = true;
+            long long *pdetail = (p.trace && cta == 0)
+                                     ? p.trace + (size_t)(n_layers * kTracePoints + 2) * G : nullptr;
+            int p_layer = 0;
+            uint32_t p_stage0 = 0;
+            // Claims the next ring slot for `bytes` of copies; returns its base.
+            auto claim = [&](uint32_t bytes) -> uint8_t * {
+                const int slot = stage % kStages;
+                if (stage >= kStages && ok)
+                    ok = mbar_wait(&s.empty[slot], ((stage / kStages) - 1) & 1, s, deadline, status, 1, (int)stage);
+                if (!ok)
+                    return nullptr;
+                mbar_expect_tx(&s.full[slot], bytes);
+                if (pdetail && stage - p_stage0 < kTraceStages)
+                    pdetail[((size_t)p_layer * kTraceStages + (stage - p_stage0)) * kTraceDetail] = clock64();
+                return s.ring[slot];
+            };
+            auto gu_rows = [&](const fgm_layer &L, int e, int i, int nv) {
+                uint8_t *dst = claim(2u * nv * kH);
+                if (!dst)
+                    return;
+                const uint8_t *gsrc = L.gate_q + ((size_t)e * kF + i) * kH;
+                const uint8_t *usrc = L.up_q + ((size_t)e * kF + i) * kH;
+                for (int rr = 0; rr < nv; ++rr) {
+                    bulk_g2s(dst + rr * kRowStride, gsrc + (size_t)rr * kH, kH, &s.full[stage % kStages]);
+                    bulk_g2s(dst + (8 + rr) * kRowStride, usrc + (size_t)rr * kH, kH, &s.full[stage % kStages]);
+                }
+                ++stage;
+            };
+            // The stages of a layer after its routing is known: routed gate/up
+            // row pairs, then down rows (routed experts and the shared one).
+            struct LayerPlan {
+                int U, gb, ge, gpos, di;
+                DownStages ds;
+                __device__ LayerPlan(int U_, int cta_, int G_)
+                    : U(U_), gb(0), ge(0), gpos(0), di(0), ds(U_, cta_, G_)
+                {
+                    const Range rb = split((long long)U_ * kF, cta_, G_);
+                    gb = rb.begin;
+                    ge = rb.end;
+                    gpos = gb;
+                }
+                // next stage: kind 0 = gate/up (slot u, row i, nv pairs), 1 = down (slot si, row j, nv rows)
+                __device__ bool next(int &kind, int &slot, int &row, int &nv)
+                {
+                    if (gpos < ge) {
+                        kind = 0;
+                        slot = gpos / kF;
+                        row = gpos % kF;
+                        nv = min(min(8, kF - row), ge - gpos);
+                        gpos += nv;
+                        return true;
+                    }
+                    if (di < ds.n) {
+                        int pos;
+                        ds.get(di++, pos, nv);
+                        kind = 1;
+                        slot = pos / kH;
+                        row = pos % kH;
+                        return true;
+                    }
+                    return false;
+                }
+            };
+            const bool lm_phase = p.mode == kModeVerify || p.mode == kModeLmHead;
+            const Range rvoc = lm_phase ? split(p.V, cta, G) : Range{0, 0};
+            for (int l = 0; l < n_layers && ok; ++l) {
+                const fgm_layer &L = p.layers[l];
+                p_layer = l;
+                p_stage0 = stage;
+                // phase A: shared expert gate/up rows
+                const Range ra = split(kF, cta, G);
+                for (int i = ra.begin; i < ra.end && ok; i += 8)
+                    gu_rows(L, kShared, i, min(8, ra.end - i));
+                if (!ok)
+                    break;
+                ok = mbar_wait(&s.route, l & 1, s, deadline, status, 2, l);
+                if (!ok)
+                    break;
+                const int pb = l & 1;
+                const int U = s.n_unique[pb];
+                // phases B and C
+                LayerPlan plan(U, cta, G);
+                int kind, slot, row, nv;
+                while (ok && plan.next(kind, slot, row, nv)) {
+                    if (kind == 0) {
+                        gu_rows(L, s.experts[pb][slot], row, nv);
+                    } else {
+                        const int e = slot < U ? s.experts[pb][slot] : kShared;
+                        uint8_t *dst = claim(static_cast<uint32_t>(nv) * kF);
+                        if (!dst)
+                            break;
+                        bulk_g2s(dst, L.down_q + ((size_t)e * kH + row) * kF, static_cast<uint32_t>(nv) * kF,
+                                 &s.full[stage % kStages]);
+                        ++stage;
+                    }
+                }
+            }
+            if (ok && lm_phase) {
+                for (int v0 = rvoc.begin; v0 < rvoc.end && ok; v0 += 16) {
+                    const int nv = min(16, rvoc.end - v0);
+                    for (int half = 0; half < 2 && ok; ++half) {
+                        uint8_t *dst = claim(static_cast<uint32_t>(nv) * kH);
+                        if (!dst)
+                            break;
+                        const uint8_t *src = reinterpret_cast<const uint8_t *>(p.emb + (size_t)v0 * kH) + half * kH;
+                        for (int rr = 0; rr < nv; ++rr)
+                            bulk_g2s(dst + rr * kRowStride, src + (size_t)rr * 2 * kH, kH, &s.full[stage % kStages]);
+                        ++stage;
+                    }
+                }
+            }
+            // Every issued copy must land before the CTA may exit.
+            const uint32_t first = stage > kStages ? stage - kStages : 0;
+            for (uint32_t k = first; k < stage; ++k)
+                for (int it = 0; it < (1 << 20); ++it)
+                    if (mbar_try(&s.full[k % kStages], (k / kStages) & 1))
+                        break;
+        }
+        return;
+    }
+
+    // ============================================================ consumers
+    uint32_t stage = 0;   // ring stages consumed
+    unsigned bar_target = 0;
+    unsigned *bar_ctr = ws.sync;
+
+    // Grid-wide barrier of the consumer warps (the producer never joins: it only
+    // reads weights). Release-add then acquire-spin on one counter in the
+    // workspace; bounded by the kernel's deadline.
+    auto grid_barrier = [&]() {
+        consumer_sync();
+        if (tid == 0) {
+            bar_target += G;
+            asm volatile("red.release.gpu.global.add.u32 [%0], 1;" ::"l"(bar_ctr) : "memory");
+            if (!*reinterpret_cast<volatile int *>(&s.abort)) {
+                for (int it = 0;; ++it) {
+                    unsigned v;
+                    asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(bar_ctr) : "memory");
+                    if (v >= bar_target)
+                        break;
+                    if ((it & 63) == 63 && gtime() > deadline) {
+                        s.abort = 1;
+                        if (atomicOr(status, FGM_STATUS_WAIT_TIMEOUT) == 0) {
+                            status[1] = 6;
+                            status[2] = cta;
+                            status[3] = (int)v;
+                            status[4] = (int)bar_target;
+                        }
+                        break;
+                    }
+                }
+            }
+        }
+        consumer_sync();
+    };
+
+    long long *detail = (p.trace && cta == 0)
+                            ? p.trace + (size_t)(n_layers * kTracePoints + 2) * G : nullptr;
+    int cur_layer = 0;
+    uint32_t layer_stage0 = 0;
+    auto dstamp = [&](uint32_t k, uint32_t k0, int which) {
+        if (detail && k - k0 < kTraceStages)
+            detail[((size_t)cur_layer * kTraceStages + (k - k0)) * kTraceDetail + which] = clock64();
+    };
+    // MMA warps: wait for the next ring stage (false after an abort) and release it
+    auto stage_wait = [&]() -> bool {
+        const bool ok = mbar_wait(&s.full[stage % kStages], (stage / kStages) & 1, s, deadline, status, 3, (int)stage);
+        if (tid == 0)
+            dstamp(stage, layer_stage0, 1);
+        return ok;
+    };
+    auto stage_release = [&]() {
+        __syncwarp();
+        if (lane == 0)
+            mbar_arrive(&s.empty[stage % kStages]);
+        if (tid == 0)
+            dstamp(stage, layer_stage0, 3);
+        ++stage;
+    };
+    uint32_t bx[4][kTerms][4];   // activation terms of this warp's K-slice (token g)
+    float inv_x[kTerms][2];
+    int cur_pb = 0;               // routing buffer of the current layer
+    // lm_head: lanes 0..3 keep the running best of tokens 2 lane, 2 lane + 1
+    // over the tiles this warp reduces
+    float best_v[2] = {-INFINITY, -INFINITY};
+    int best_i[2] = {0x7FFFFFFF, 0x7FFFFFFF};
+
+    // Epilogue of one reduced 16 x 8 tile; lane holds rows r0 = lane / 4 (x, y)
+    // and r0 + 8 (z, w), columns n0 = 2 (lane % 4) and n0 + 1.
+    auto finish_tile = [&](const int4 &m, int tl, const float4 &f) {
+        const int r0 = lane >> 2, n0 = (lane & 3) * 2;
+        const int kind = m.x & 3;
+        if (kind == kTileGateUp) {
+            // m.x >> 2 = act slot, m.y = first row, m.z = row pairs | (k0 << 8), m.w = comb slot or -1;
+            // x, y: gate of row r0; z, w: up of row r0
+            const int aslot = m.x >> 2, i = m.y, nv = m.z & 0xFF, k0 = m.z >> 8;
+            if (r0 < nv) {
+                const float sg = s.sc_g[k0 + r0], su = s.sc_u[k0 + r0];
+                const float c0 = m.w >= 0 ? s.comb[cur_pb][m.w][n0] : 1.0f;
+                const float c1 = m.w >= 0 ? s.comb[cur_pb][m.w][n0 + 1] : 1.0f;
+                float *dst = ws.act + ((size_t)aslot * kMaxM + n0) * kF + i + r0;
+                if (n0 < M)
+                    __stcg(dst, gelu_tanh(sg * f.x) * (su * f.z) * c0);
+                if (n0 + 1 < M)
+                    __stcg(dst + kF, gelu_tanh(sg * f.y) * (su * f.w) * c1);
+            }
+        } else if (kind == kTileDown) {
+            // tile tl of a 64-row stage: m.y = first output row j of the stage, m.z = scale
+            // index of that row, m.w = valid rows of the stage
+            const int j = m.y + 16 * tl, k0 = m.z + 16 * tl, nv = m.w - 16 * tl;
+            if (r0 < nv) {
+                const float sd = s.sc_d[k0 + r0];
+                if (n0 < M)
+                    atomicAdd(ws.h + (size_t)n0 * kH + j + r0, f.x * sd);
+                if (n0 + 1 < M)
+                    atomicAdd(ws.h + (size_t)(n0 + 1) * kH + j + r0, f.y * sd);
+            }
+            if (r0 + 8 < nv) {
+                const float sd = s.sc_d[k0 + r0 + 8];
+                if (n0 < M)
+                    atomicAdd(ws.h + (size_t)n0 * kH + j + r0 + 8, f.z * sd);
+                if (n0 + 1 < M)
+                    atomicAdd(ws.h + (size_t)(n0 + 1) * kH + j + r0 + 8, f.w * sd);
+            }
+        } else {
+            // m.y = first vocabulary row v0, m.z = valid rows
+            const int v0 = m.y, nv = m.z;
+#pragma unroll
+            for (int c = 0; c < 2; ++c) {
+                const float za = c ? f.y : f.x, zb = c ? f.w : f.z;
+                const bool ca = r0 < nv && n0 + c < M && !isnan(za);
+                const bool cb = r0 + 8 < nv && n0 + c < M && !isnan(zb);
+                float bz = ca ? za : -INFINITY;
+                int bi = ca ? v0 + r0 : 0x7FFFFFFF;
+                if (cb && better(zb, v0 + r0 + 8, bz, bi)) {
+                    bz = zb;
+                    bi = v0 + r0 + 8;
+                }
+#pragma unroll
+                for (int o = 4; o < 32; o <<= 1) {
+                    const float oz = __shfl_xor_sync(0xFFFFFFFFu, bz, o);
+                    const int oi = __shfl_xor_sync(0xFFFFFFFFu, bi, o);
+                    if (better(oz, oi, bz, bi)) {
+                        bz = oz;
+                        bi = oi;
+                    }
+                }
+                if (better(bz, bi, best_v[c], best_i[c])) {
+                    best_v[c] = bz;
+                    best_i[c] = bi;
+                }
+            }
+        }
+    };
+
+    // The partials of a stage's nt tiles meet in shared memory; after a barrier
+    // the first 32 nt threads sum one tile each and apply its epilogue.
+    auto exchange = [&](const int4 &m, const float (&part)[kDownTiles][4], int nt) {
+#pragma unroll
+        for (int t = 0; t < kDownTiles; ++t)
+            if (t < nt)
+                s.red[warp][t][lane] = make_float4(part[t][0], part[t][1], part[t][2], part[t][3]);
+        consumer_sync();
+        if (tid < 32 * nt) {
+            const int t = tid >> 5;
+            finish_tile(m, t, red_sum4(s, t, lane));
+        }
+        consumer_sync();
+        if (tid == 0 && cta == 0)
+            dstamp(stage - 1, layer_stage0, 4);
+    };
+    auto exchange1 = [&](const int4 &m, float x, float y, float z, float w) {
+        float part[kDownTiles][4];
+        part[0][0] = x;
+        part[0][1] = y;
+        part[0][2] = z;
+        part[0][3] = w;
+        exchange(m, part, 1);
+    };
+
+    // One gate/up tile (rows i..i+nv-1 of one expert, written to act slot
+    // aslot): act[aslot][n][i + ii] = comb * gelu_tanh(s_g g) * (s_u u).
+    auto gu_tile = [&](int aslot, int comb_slot, int i, int nv, int k0) {
+        uint4 ra[4], rb[4];
+        const bool got = stage_wait();
+        float part[4] = {0.0f, 0.0f, 0.0f, 0.0f};
+        if (got) {
+            load_a_wide(s.ring[stage % kStages], warp, g, q, ra, rb);
+            gu_products(ra, rb, bx, inv_x, part);
+        }
+        stage_release();
+        if (tid == 0)
+            dstamp(stage - 1, layer_stage0, 2);
+        exchange1(make_int4(kTileGateUp | (aslot << 2), i, nv | (k0 << 8), comb_slot), part[0], part[1], part[2],
+                  part[3]);
+    };
+
+    for (int l = 0; l < n_layers; ++l) {
+        const fgm_layer &L = p.layers[l];
+        const int pb = l & 1;
+        auto stamp = [&](int k) {
+            if (p.trace && tid == 0)
+                p.trace[((size_t)l * kTracePoints + k) * G + cta] = gtime();
+        };
+        cur_layer = l;
+        cur_pb = pb;
+        layer_stage0 = stage;
+        if (detail && tid == 0)
+            detail[((size_t)l * kTraceStages) * kTraceDetail + 7] = clock64();
+        stamp(0);
+        if (l == 0 && p.debug_stall && tid == 0)
+            bar_target += 1;   // the next grid barrier can never complete
+        if (l == 0 && p.debug_stall)
+            grid_barrier();
+        // -------------------------------------------------------- phase A
+        const Range rsh = split(kF, cta, G);
+        {
+            const bool from_x = (p.mode == kModeLayer) || l == 0;
+            const bool norm = p.mode != kModeLayer;
+            const bool router_cta = cta < kE;
+            float v[4][16];
+            const uint16_t *wrow = L.router_w + (size_t)cta * kH + 256 * warp + 16 * q;
+            // router row of this CTA (its K-slice positions): fetch into L1
+            // while the activations load
+            if (router_cta) {
+#pragma unroll
+                for (int c = 0; c < 4; ++c)
+                    asm volatile("prefetch.global.L1 [%0];" ::"l"(wrow + 64 * c));
+            }
+            if (g < M) {
+                if (from_x)
+                    load_slice_bf16(p.x + (size_t)g * kH, warp, q, v);
+                else
+                    load_slice_f32(ws.h + (size_t)g * kH, warp, q, v);
+            } else {
+#pragma unroll
+                for (int c = 0; c < 4; ++c)
+#pragma unroll
+                    for (int i = 0; i < 16; ++i)
+                        v[c][i] = 0.0f;
+            }
+            // scales of this CTA's shared-expert gate/up rows (read after the
+            // consumer barrier below)
+            for (int i = tid; i < rsh.end - rsh.begin; i += kConsumers) {
+                s.sc_g[kMaxGuRows + i] = __ldg(L.gate_s + (size_t)kShared * kF + rsh.begin + i);
+                s.sc_u[kMaxGuRows + i] = __ldg(L.up_s + (size_t)kShared * kF + rsh.begin + i);
+            }
+            if (l == 0) {
+                // residual (stack) or accumulator (layer) initialisation, split over CTAs
+                for (int i = cta * kConsumers + tid; i < kMaxM * kH; i += G * kConsumers) {
+                    const int n = i / kH;
+                    float init = 0.0f;
+                    if (p.mode != kModeLayer && n < M)
+                        init = bf16_to_f32(p.x[i]);
+                    ws.h[i] = init;
+                }
+            }
+            {
+                // sum of squares and the router dot product on the un-normalised
+                // row; RMSNorm is a per-token scale, applied to the dot afterwards
+                float ss = 0.0f, dot = 0.0f;
+#pragma unroll
+                for (int c = 0; c < 4; ++c)
+#pragma unroll
+                    for (int i = 0; i < 16; ++i)
+                        ss += v[c][i] * v[c][i];
+                if (router_cta) {
+#pragma unroll
+                    for (int c = 0; c < 4; ++c) {
+                        const uint4 w0 = __ldg(reinterpret_cast<const uint4 *>(wrow + 64 * c));
+                        const uint4 w1 = __ldg(reinterpret_cast<const uint4 *>(wrow + 64 * c + 8));
+                        const uint32_t w8[8] = {w0.x, w0.y, w0.z, w0.w, w1.x, w1.y, w1.z, w1.w};
+#pragma unroll
+                        for (int k = 0; k < 8; ++k) {
+                            const float2 f = bf16x2_to_f32(w8[k]);
+                            dot += f.x * v[c][2 * k] + f.y * v[c][2 * k + 1];
+                        }
+                    }
+                }
+                ss = quad_sum(ss);
+                dot = quad_sum(dot);
+                if (q == 0) {
+                    s.part[warp][g] = ss;
+                    s.part2[warp][g] = dot;
+                }
+                stamp(1);
+            }
+            consumer_sync();
+            stamp(2);
+            {
+                float r = 1.0f;
+                if (norm) {
+                    float tot = 0.0f;
+#pragma unroll
+                    for (int w = 0; w < kMW; ++w)
+                        tot += s.part[w][g];
+                    r = 1.0f / sqrtf(tot / static_cast<float>(kH) + kEps);
+                }
+                if (router_cta && tid < M) {
+                    float z = 0.0f, tot = 0.0f;
+#pragma unroll
+                    for (int w = 0; w < kMW; ++w) {
+                        z += s.part2[w][tid];
+                        tot += s.part[w][tid];
+                    }
+                    const float rt = norm ? 1.0f / sqrtf(tot / static_cast<float>(kH) + kEps) : 1.0f;
+                    __stcg(ws.logits + tid * kE + cta, z * rt + (L.router_b ? L.router_b[cta] : 0.0f));
+                }
+                // activation terms for the gate/up products (this warp's K-slice, token g)
+                float amax = 0.0f;
+#pragma unroll
+                for (int c = 0; c < 4; ++c)
+#pragma unroll
+                    for (int i = 0; i < 16; ++i) {
+                        v[c][i] *= r;
+                        amax = fmaxf(amax, fabsf(v[c][i]));
+                    }
+                const float S = term_scale(quad_max(amax));
+#pragma unroll
+                for (int c = 0; c < 4; ++c)
+                    split16_into(v[c], S, bx[c]);
+                column_inv(S, q, inv_x);
+            }
+        }
+        stamp(3);
+        stamp(4);
+        grid_barrier();
+        stamp(5);
+        // -------------------------------------------------------- phase B
+        {
+            if (warp < M) {
+                float lv[4];
+#pragma unroll
+                for (int k = 0; k < 4; ++k)
+                    lv[k] = __ldcg(ws.logits + warp * kE + lane + 32 * k);
+                // top-8 by repeated warp argmax (ties to the lower index)
+                bool bad = false;
+#pragma unroll
+                for (int k = 0; k < 4; ++k)
+                    if (isnan(lv[k])) {
+                        lv[k] = -INFINITY;
+                        bad = true;
+                    }
+                if (__any_sync(0xFFFFFFFFu, bad) && lane == 0)
+                    atomicOr(status, FGM_STATUS_NONFINITE_LOGITS);
+                unsigned taken = 0;
+                float top0 = 0.0f, my_v = 0.0f;
+                int my_i = 0;
+#pragma unroll 1
+                for (int rr = 0; rr < kK; ++rr) {
+                    float bv = -INFINITY;
+                    int bi = 0x7FFFFFFF;
+#pragma unroll
+                    for (int k = 0; k < 4; ++k) {
+                        const int idx = lane + 32 * k;
+                        if (!(taken & (1u << k)) && better(lv[k], idx, bv, bi)) {
+                            bv = lv[k];
+                            bi = idx;
+                        }
+                    }
+#pragma unroll
+                    for (int o = 16; o > 0; o >>= 1) {
+                        const float ov = __shfl_xor_sync(0xFFFFFFFFu, bv, o);
+                        const int oi = __shfl_xor_sync(0xFFFFFFFFu, bi, o);
+                        if (better(ov, oi, bv, bi)) {
+                            bv = ov;
+                            bi = oi;
+                        }
+                    }
+                    if ((bi & 31) == lane)
+                        taken |= 1u << (bi >> 5);
+                    if (rr == 0)
+                        top0 = bv;
+                    if (rr == lane) {
+                        my_v = bv;
+                        my_i = bi;
+                    }
+                }
+                // lanes 0..7 hold the 8 picks; weights = exp(l - l_max) / sum
+                const float ex = lane < kK ? (top0 == -INFINITY ? 1.0f : expf(my_v - top0)) : 0.0f;
+                float z = ex;
+#pragma unroll
+                for (int o = 16; o > 0; o >>= 1)
+                    z += __shfl_xor_sync(0xFFFFFFFFu, z, o);
+                if (lane < kK) {
+                    s.tk_ids[warp][lane] = my_i;
+                    s.tk_w[warp][lane] = ex / z;
+                }
+            }
+            for (int i = tid; i < kE; i += kConsumers)
+                s.mark[i] = 0;
+            consumer_sync();
+            if (tid < M * kK)
+                s.mark[s.tk_ids[tid >> 3][tid & 7]] = 1;
+            consumer_sync();
+            if (warp == 0) {
+                int base = 0;
+#pragma unroll
+                for (int k = 0; k < kE / 32; ++k) {
+                    const int e = 32 * k + lane;
+                    const bool m = s.mark[e] != 0;
+                    const unsigned bal = __ballot_sync(0xFFFFFFFFu, m);
+                    const int pos = base + __popc(bal & ((1u << lane) - 1u));
+                    if (m) {
+                        s.experts[pb][pos] = e;
+                        s.slot_of[e] = pos;
+                    }
+                    base += __popc(bal);
+                }
+                if (lane == 0)
+                    s.n_unique[pb] = base;
+            }
+            for (int i = tid; i < kMaxSlots * 8; i += kConsumers)
+                s.comb[pb][i >> 3][i & 7] = 0.0f;
+            consumer_sync();
+            if (tid < M * kK) {
+                const int t = tid >> 3, rr = tid & 7;
+                s.comb[pb][s.slot_of[s.tk_ids[t][rr]]][t] = s.tk_w[t][rr];
+                if (cta == 0 && p.ids) {
+                    const size_t base = p.mode == kModeLayer ? 0 : (size_t)l * M * kK;
+                    p.ids[base + tid] = s.tk_ids[t][rr];
+                    if (p.mode == kModeLayer && p.wts)
+                        p.wts[tid] = s.tk_w[t][rr];
+                }
+            }
+            consumer_sync();
+            if (tid == 0)
+                mbar_arrive(&s.route);
+            stamp(6);
+            const int U = s.n_unique[pb];
+            const Range rg = split((long long)U * kF, cta, G);
+            // row scales of this CTA's routed gate/up rows and of its down rows;
+            // their latency overlaps the producer's first routed copies
+            for (int k = tid; k < rg.end - rg.begin; k += kConsumers) {
+                const int pos = rg.begin + k;
+                const size_t row = (size_t)s.experts[pb][pos / kF] * kF + pos % kF;
+                s.sc_g[k] = __ldg(L.gate_s + row);
+                s.sc_u[k] = __ldg(L.up_s + row);
+            }
+            {
+                const Range rd = split((long long)(U + 1) * kH, cta, G);
+                for (int k = tid; k < rd.end - rd.begin; k += kConsumers) {
+                    const int pos = rd.begin + k;
+                    const int si = pos / kH;
+                    const int e = si < U ? s.experts[pb][si] : kShared;
+                    s.sc_d[k] = __ldg(L.down_s + (size_t)e * kH + pos % kH);
+                }
+            }
+            consumer_sync();
+            // the shared expert's rows of this CTA first (their copies were issued
+            // before the routing was known), then its routed rows
+            const int n_sh = (rsh.end - rsh.begin + 7) / 8;
+            int pos = rg.begin;
+            for (int it = 0;; ++it) {
+                int aslot, i, nv, k0, cslot = -1;
+                if (it < n_sh) {
+                    i = rsh.begin + 8 * it;
+                    nv = min(8, rsh.end - i);
+                    aslot = kSharedSlot;
+                    k0 = kMaxGuRows + 8 * it;
+                } else {
+                    if (pos >= rg.end)
+                        break;
+                    const int u = pos / kF;
+                    i = pos % kF;
+                    nv = min(min(8, kF - i), rg.end - pos);
+                    aslot = u;
+                    cslot = u;
+                    k0 = pos - rg.begin;
+                    pos += nv;
+                }
+                gu_tile(aslot, cslot, i, nv, k0);
+            }
+        }
+        stamp(7);
+        grid_barrier();
+        stamp(8);
+        // -------------------------------------------------------- phase C
+        {
+            const int U = s.n_unique[pb];
+            const DownStages ds(U, cta, G);
+            // A CTA's rows span at most two slots (it owns fewer than 2816 rows):
+            // their activation terms (this warp's 64-wide K-slice, token g) are
+            // prepared once, up front.
+            const int si0 = ds.begin / kH;
+            uint32_t bd[2][kTerms][4];
+            float inv_d[2][kTerms][2];
+#pragma unroll
+            for (int h2 = 0; h2 < 2; ++h2) {
+                const int si = si0 + h2;
+                float v[16];
+                if (g < M && si <= U && (h2 == 0 || ds.end > (si0 + 1) * kH)) {
+                    const int aslot = si < U ? si : kSharedSlot;
+                    const float *ar = ws.act + ((size_t)aslot * kMaxM + g) * kF + 64 * warp + 16 * q;
+#pragma unroll
+                    for (int k = 0; k < 4; ++k) {
+                        const float4 f = ldcg4(ar + 4 * k);
+                        v[4 * k] = f.x;
+                        v[4 * k + 1] = f.y;
+                        v[4 * k + 2] = f.z;
+                        v[4 * k + 3] = f.w;
+                    }
+                } else {
+#pragma unroll
+                    for (int i = 0; i < 16; ++i)
+                        v[i] = 0.0f;
+                }
+                float amax = 0.0f;
+#pragma unroll
+                for (int i = 0; i < 16; ++i)
+                    amax = fmaxf(amax, fabsf(v[i]));
+                const float S = term_scale(quad_max(amax));
+                split16_into(v, S, bd[h2]);
+                column_inv(S, q, inv_d[h2]);
+            }
+            for (int di = 0; di < ds.n; ++di) {
+                int pos, nv;
+                ds.get(di, pos, nv);
+                const int si = pos / kH, j = pos % kH;
+                const int hs = si == si0 ? 0 : 1;
+                uint32_t bt[kTerms][4];
+                float it[kTerms][2];
+#pragma unroll
+                for (int tt = 0; tt < kTerms; ++tt) {
+#pragma unroll
+                    for (int k = 0; k < 4; ++k)
+                        bt[tt][k] = hs ? bd[1][tt][k] : bd[0][tt][k];
+                    it[tt][0] = hs ? inv_d[1][tt][0] : inv_d[0][tt][0];
+                    it[tt][1] = hs ? inv_d[1][tt][1] : inv_d[0][tt][1];
+                }
+                const bool got = stage_wait();
+                const uint8_t *slot = s.ring[stage % kStages];
+                float po[kDownTiles][4];
+#pragma unroll
+                for (int t0 = 0; t0 < kDownTiles; t0 += 2) {
+                    // two tiles x 3 terms = 6 independent accumulator chains
+                    float acc[2][kTerms][4];
+#pragma unroll
+                    for (int t = 0; t < 2; ++t)
+#pragma unroll
+                        for (int tt = 0; tt < kTerms; ++tt)
+#pragma unroll
+                            for (int e2 = 0; e2 < 4; ++e2)
+                                acc[t][tt][e2] = 0.0f;
+                    if (got) {
+                        uint4 ra[2], rb[2];
+#pragma unroll
+                        for (int t = 0; t < 2; ++t) {
+                            ra[t] = lds128(slot + (16 * (t0 + t) + g) * kF + 64 * warp + 16 * q);
+                            rb[t] = lds128(slot + (16 * (t0 + t) + g + 8) * kF + 64 * warp + 16 * q);
+                        }
+#pragma unroll
+                        for (int step = 0; step < 2; ++step)
+#pragma unroll
+                            for (int tt = 0; tt < kTerms; ++tt)
+#pragma unroll
+                                for (int t = 0; t < 2; ++t) {
+                                    const uint32_t a[4] = {step ? ra[t].z : ra[t].x, step ? rb[t].z : rb[t].x,
+                                                           step ? ra[t].w : ra[t].y, step ? rb[t].w : rb[t].y};
+                                    mma_e4m3(acc[t][tt], a, bt[tt][2 * step], bt[tt][2 * step + 1]);
+                                }
+                    }
+#pragma unroll
+                    for (int t = 0; t < 2; ++t)
+#pragma unroll
+                        for (int e2 = 0; e2 < 4; ++e2) {
+                            float o = 0.0f;
+#pragma unroll
+                            for (int tt = 0; tt < kTerms; ++tt)
+                                o += acc[t][tt][e2] * it[tt][e2 & 1];
+                            po[t0 + t][e2] = o;
+                        }
+                }
+                if (tid == 0)
+                    dstamp(stage, layer_stage0, 2);
+                stage_release();
+                exchange(make_int4(kTileDown, j, pos - ds.begin, nv), po, kDownTiles);
+            }
+        }
+        stamp(9);
+        grid_barrier();
+    }
+    if (p.trace && tid == 0)
+        p.trace[((size_t)n_layers * kTracePoints) * G + cta] = gtime();
+
+    // ------------------------------------------------------------ outputs
+    if (p.mode == kModeLayer || p.mode == kModeStack) {
+        for (int i = cta * kConsumers + tid; i < M * kH; i += G * kConsumers)
+            p.y[i] = f32_to_bf16(__ldcg(ws.h + i));
+    } else {
+        // lm_head input: bf16(RMSNorm(h)) after the stack, or the given bf16 rows.
+        // warp w's K-slice in each half (1408 elements) of a row: 128 w + 32 c + 8 q + [0, 8)
+        uint32_t bh[2][4][4];
+        if (p.mode == kModeVerify) {
+            float ss = 0.0f;
+            if (is_mma && g < M) {
+                float v[4][16];
+                load_slice_f32(ws.h + (size_t)g * kH, warp, q, v);
+#pragma unroll
+                for (int c = 0; c < 4; ++c)
+#pragma unroll
+                    for (int i = 0; i < 16; ++i)
+                        ss += v[c][i] * v[c][i];
+            }
+            ss = quad_sum(ss);
+            if (is_mma && q == 0)
+                s.part[warp][g] = ss;
+            consumer_sync();
+            if (is_mma) {
+                float tot = 0.0f;
+#pragma unroll
+                for (int w = 0; w < kMW; ++w)
+                    tot += s.part[w][g];
+                const float r = g < M ? 1.0f / sqrtf(tot / static_cast<float>(kH) + kEps) : 0.0f;
+#pragma unroll
+                for (int half = 0; half < 2; ++half)
+#pragma unroll
+                    for (int c = 0; c < 4; ++c) {
+                        float hv[8];
+                        if (g < M) {
+                            const float *hp = ws.h + (size_t)g * kH + 1408 * half + 128 * warp + 32 * c + 8 * q;
+                            const float4 f0 = ldcg4(hp), f1 = ldcg4(hp + 4);
+                            hv[0] = f0.x; hv[1] = f0.y; hv[2] = f0.z; hv[3] = f0.w;
+                            hv[4] = f1.x; hv[5] = f1.y; hv[6] = f1.z; hv[7] = f1.w;
+                        } else {
+#pragma unroll
+                            for (int i = 0; i < 8; ++i)
+                                hv[i] = 0.0f;
+                        }
+#pragma unroll
+                        for (int k = 0; k < 4; ++k)
+                            bh[half][c][k] = static_cast<uint32_t>(f32_to_bf16(hv[2 * k] * r)) |
+                                             (static_cast<uint32_t>(f32_to_bf16(hv[2 * k + 1] * r)) << 16);
+                    }
+            }
+        } else if (is_mma) {
+#pragma unroll
+            for (int half = 0; half < 2; ++half)
+#pragma unroll
+                for (int c = 0; c < 4; ++c) {
+                    uint4 w4 = make_uint4(0u, 0u, 0u, 0u);
+                    if (g < M)
+                        w4 = *reinterpret_cast<const uint4 *>(p.x + (size_t)g * kH + 1408 * half + 128 * warp + 32 * c + 8 * q);
+                    bh[half][c][0] = w4.x;
+                    bh[half][c][1] = w4.y;
+                    bh[half][c][2] = w4.z;
+                    bh[half][c][3] = w4.w;
+                }
+        }
+        const Range rv = split(p.V, cta, G);
+        for (int v0 = rv.begin; v0 < rv.end; v0 += 16) {
+            const int nv = min(16, rv.end - v0);
+            float acc[2][4] = {{0.0f, 0.0f, 0.0f, 0.0f}, {0.0f, 0.0f, 0.0f, 0.0f}};
+#pragma unroll
+            for (int half = 0; half < 2; ++half) {
+                uint4 ra[4], rb[4];
+                const bool got = stage_wait();
+                if (got) {
+                    load_a_wide(s.ring[stage % kStages], warp, g, q, ra, rb);
+#pragma unroll
+                    for (int c = 0; c < 4; ++c) {
+                        const uint32_t a0[4] = {ra[c].x, rb[c].x, ra[c].y, rb[c].y};
+                        const uint32_t a1[4] = {ra[c].z, rb[c].z, ra[c].w, rb[c].w};
+                        mma_bf16(acc[c & 1], a0, bh[half][c][0], bh[half][c][1]);
+                        mma_bf16(acc[c & 1], a1, bh[half][c][2], bh[half][c][3]);
+                    }
+                }
+                stage_release();
+            }
+            exchange1(make_int4(kTileLmHead, v0, nv, 0), acc[0][0] + acc[1][0], acc[0][1] + acc[1][1],
+                      acc[0][2] + acc[1][2], acc[0][3] + acc[1][3]);
+        }
+        if (lane < 4) {
+#pragma unroll
+            for (int c = 0; c < 2; ++c) {
+                s.best_v[warp][2 * lane + c] = best_v[c];
+                s.best_i[warp][2 * lane + c] = best_i[c];
+            }
+        }
+        consumer_sync();
+        if (tid < kMaxM) {
+            float bv = s.best_v[0][tid];
+            int bi = s.best_i[0][tid];
+#pragma unroll
+            for (int w = 1; w < kMW; ++w)
+                if (better(s.best_v[w][tid], s.best_i[w][tid], bv, bi)) {
+                    bv = s.best_v[w][tid];
+                    bi = s.best_i[w][tid];
+                }
+            __stcg(ws.part_val + cta * kMaxM + tid, bv);
+            __stcg(ws.part_idx + cta * kMaxM + tid, bi);
+        }
+    }
+    if (p.trace && tid == 0)
+        p.trace[((size_t)n_layers * kTracePoints + 1) * G + cta] = gtime();
+
+    // ------------------------------------------------------------ exit
+    // The last CTA to get here reduces the lm_head winners (lm_head modes)
+    // and returns the barrier counters to zero for the next launch: every
+    // CTA has passed its last grid barrier by then.
+    consumer_sync();
+    if (tid == 0) {
+        __threadfence();
+        const unsigned done = atomicAdd(bar_ctr + 1, 1u);
+        s.last = done == static_cast<unsigned>(G - 1);
+    }
+    consumer_sync();
+    if (!s.last)
+        return;
+    __threadfence();
+    if (p.mode == kModeVerify || p.mode == kModeLmHead) {
+        __shared__ int32_t arg[kMaxM];
+        if (warp < M) {
+            float bv = -INFINITY;
+            int bi = 0x7FFFFFFF;
+            for (int c = lane; c < G; c += 32) {
+                const float vv = __ldcg(ws.part_val + c * kMaxM + warp);
+                const int ii = __ldcg(ws.part_idx + c * kMaxM + warp);
+                if (better(vv, ii, bv, bi)) {
+                    bv = vv;
+                    bi = ii;
+                }
+            }
+#pragma unroll
+            for (int o = 16; o > 0; o >>= 1) {
+                const float ov = __shfl_xor_sync(0xFFFFFFFFu, bv, o);
+                const int oi = __shfl_xor_sync(0xFFFFFFFFu, bi, o);
+                if (better(ov, oi, bv, bi)) {
+                    bv = ov;
+                    bi = oi;
+                }
+            }
+            if (lane == 0) {
+                if (bi == 0x7FFFFFFF) {
+                    bi = 0;
+                    atomicOr(status, FGM_STATUS_NONFINITE_LOGITS);
+                }
+                arg[warp] = bi;
+                if (p.argmax)
+                    p.argmax[warp] = bi;
+                if (p.maxlogit)
+                    p.maxlogit[warp] = bv;
+            }
+        }
+        consumer_sync();
+        if (tid == 0 && p.mode == kModeVerify) {
+            int a = 0;
+            while (a < M - 1 && p.draft[a] == arg[a])
+                ++a;
+            p.out[0] = a;
+            p.out[1] = arg[a];
+        }
+    }
+    if (tid == 0) {
+        bar_ctr[1] = 0;
+        atomicExch(bar_ctr, 0u);
+    }
+}
+
+}  // namespace fused
+}  // namespace fgm

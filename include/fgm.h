@@ -57,6 +57,13 @@ enum {
     FGM_ERR_DEVICE = -4,      /* the current device is not a supported GPU (sm_103) */
 };
 
+/* Execution paths (fgm_select_path). */
+enum {
+    FGM_PATH_FUSED = 0,  /* default: one persistent cooperative kernel per call; weight rows stream
+                            through a TMA-bulk shared-memory ring into FP8/bf16 mma.sync tiles */
+    FGM_PATH_STAGED = 1, /* one launch per stage with fp32 CUDA-core arithmetic (comparison path) */
+};
+
 /* Status bits written by kernels into the workspace (fgm_read_status). */
 enum {
     FGM_STATUS_NONFINITE_LOGITS = 1, /* a router or lm_head logit was NaN; treated as -inf */
@@ -159,9 +166,45 @@ int fgm_verify_step_host(const fgm_layer *layers, int n_layers, const uint16_t *
                          const uint16_t *x_host, const int32_t *draft_host, int M,
                          int32_t *out_host, void *ws, size_t ws_bytes, void *stream);
 
+/* Selects the execution path of subsequent calls in this process; returns the
+ * previous one. An unknown value leaves the path unchanged. Both paths compute
+ * the same step; they differ in kernel design only. */
+int fgm_select_path(int path);
+
+/* Upper bound, in ns of GPU time, on every wait inside the persistent kernel
+ * (grid barriers, ring slots). When a wait runs out the kernel raises
+ * FGM_STATUS_WAIT_TIMEOUT, skips its remaining work and exits; its outputs are
+ * then invalid. Default 2 s; ns < 0 only queries. Returns the previous value. */
+long long fgm_set_wait_limit_ns(long long ns);
+
+/* Profiling aid: when buf (DEVICE, n int64 entries) is non-NULL, each later
+ * persistent-kernel launch records %globaltimer stamps (ns). Per CTA at the
+ * phase boundaries of layer l: entry [(l * 10 + k) * G + cta] with k = 0 layer
+ * start, 1 norm/router partials ready, 2 after their reduction, 3 activation
+ * terms ready, 4 shared gate/up done, 5 after barrier 1, 6 routing known,
+ * 7 routed gate/up done, 8 after barrier 2, 9 down done; then [(L*10) * G + cta]
+ * after the last layer and [(L*10 + 1) * G + cta] at the end (G = CTAs, one
+ * per SM). Then, for CTA 0 only, [L][48][8] SM clock64 values per ring stage
+ * of each layer: producer issue, data landed, products done, slot released,
+ * epilogue done, two unused, and (stage 0 only) the layer start. A buffer
+ * shorter than (L*10 + 2) * G + L*48*8 entries disables recording. NULL stops. */
+int fgm_set_phase_trace(long long *buf, size_t n);
+
+/* Test hook for failure detection: the next persistent-kernel launch adds one
+ * grid barrier that can never complete, so its bounded wait must run out,
+ * raise FGM_STATUS_WAIT_TIMEOUT and let the kernel exit (outputs invalid). */
+int fgm_debug_stall_next_launch(void);
+
 /* Reads the status word of a workspace (synchronises the stream) and, if
  * `clear`, resets it. */
 int fgm_read_status(void *ws, size_t ws_bytes, int clear, int32_t *status, void *stream);
+
+/* After FGM_STATUS_WAIT_TIMEOUT: where the first wait gave up, as 4 int32
+ * (HOST report): {site, block, warp, index}; site 1 = ring slot free
+ * (producer), 2 = routing known (producer), 3 = ring data landed, 4 = all
+ * partials of a tile posted, 5 = reduction buffer free, 6 = grid barrier
+ * (then warp = counter value, index = target). Synchronises the stream. */
+int fgm_read_wait_report(void *ws, size_t ws_bytes, int32_t *report, void *stream);
 
 /* Message describing the last error returned on the calling thread. */
 const char *fgm_last_error(void);

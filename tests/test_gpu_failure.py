@@ -1,0 +1,43 @@
+"""Failure detection on the GPU without a fault. Every wait inside the
+persistent kernel has a time limit. A test hook makes the next launch wait on
+a grid barrier that no CTA can complete (a flag that nothing sets); the wait
+must run out within the limit, the kernel must raise the timeout status bit
+and exit, and the same context and workspace must then give correct results.
+"""
+
+import time
+
+import pytest
+import torch
+
+import synth
+
+pytestmark = pytest.mark.gpu
+
+
+def test_unreachable_barrier_times_out_then_recovers():
+    import fine_grained_moe_gb300 as m
+    prev_path = m.select_path(m.PATH_FUSED)
+    prev_limit = m.set_wait_limit_ns(50_000_000)   # 50 ms
+    try:
+        ws = m.Workspace("cuda")
+        p = synth.layer(0, device="cuda", s=1.1)
+        x = synth.hidden_states(5, 3, device="cuda")
+        ref = m.moe_layer_fwd(p, x, ws=ws)
+        torch.cuda.synchronize()
+        assert ws.status() == 0
+        m.debug_stall_next_launch()
+        t0 = time.perf_counter()
+        m.moe_layer_fwd(p, x, ws=ws)
+        torch.cuda.synchronize()
+        elapsed = time.perf_counter() - t0
+        assert ws.status() & m.STATUS_WAIT_TIMEOUT
+        assert elapsed < 5.0
+        again = m.moe_layer_fwd(p, x, ws=ws)
+        torch.cuda.synchronize()
+        assert ws.status() == 0
+        diff = (again.double() - ref.double()).abs().max().item()
+        assert diff <= 1e-2 * ref.double().abs().max().item()
+    finally:
+        m.set_wait_limit_ns(prev_limit)
+        m.select_path(prev_path)

@@ -22,10 +22,11 @@ M = 5
 N_LAYERS = 30
 
 
-@pytest.fixture(scope="module")
-def setup():
+@pytest.fixture(scope="module", params=[0, 1], ids=["fused", "staged"])
+def setup(request):
     import fine_grained_moe_gb300 as fgm
     fgm.lib()
+    prev = fgm.select_path(request.param)
     layers = [synth.layer(l + 1, device="cuda", s=1.1) for l in range(N_LAYERS)]
     emb = synth.embedding(32, device="cuda")
     x = synth.hidden_states(31, M, device="cuda")
@@ -41,8 +42,9 @@ def setup():
     hn_bits = oracle.bf16_round(oracle.rmsnorm(h))
     am, mx, mg = oracle.lm_head(bf16_bits(emb), oracle.bf16_to_f64(hn_bits))
     draft = synth.drafts(33, am)
-    return dict(fgm=fgm, layers=layers, emb=emb, x=x, h_ref=h, traj=traj, host=host, am=am, mg=mg,
-                draft=draft, ws=fgm.Workspace("cuda"))
+    yield dict(fgm=fgm, layers=layers, emb=emb, x=x, h_ref=h, traj=traj, host=host, am=am, mg=mg,
+               draft=draft, ws=fgm.Workspace("cuda"))
+    fgm.select_path(prev)
 
 
 def test_stack_30_layers(setup):
