@@ -61,6 +61,7 @@ def lib() -> ctypes.CDLL:
             "fgm_workspace_bytes": (sz, [ci, i64]),
             "fgm_workspace_init": (ci, [vp, sz, vp]),
             "fgm_moe_layer_fwd": (ci, [LP, vp, vp, ci, vp, vp, vp, sz, vp]),
+            "fgm_moe_layer_fwd_noalloc": (ci, [LP, vp, vp, ci, vp, vp, vp]),
             "fgm_moe_stack_fwd": (ci, [LP, ci, vp, vp, ci, vp, vp, sz, vp]),
             "fgm_lm_head_argmax": (ci, [vp, i64, vp, ci, vp, vp, vp, sz, vp]),
             "fgm_spec_verify": (ci, [vp, vp, ci, vp, vp]),
@@ -225,6 +226,21 @@ def moe_layer_fwd(layer, x: torch.Tensor, y: torch.Tensor | None = None,
     L = (layer if isinstance(layer, Layer) else Layer.from_dict(layer)).struct()
     _check(lib().fgm_moe_layer_fwd(ctypes.byref(L), _ptr(x), _ptr(y), M, _ptr(topk_ids), _ptr(topk_w),
                                    ws.ptr, ws.nbytes, _stream(stream)))
+    return y
+
+
+def moe_layer_fwd_noalloc(layer, x: torch.Tensor, y: torch.Tensor,
+                          topk_ids: torch.Tensor | None = None, topk_w: torch.Tensor | None = None,
+                          stream=None) -> torch.Tensor:
+    """moe_layer_fwd on the library's built-in device scratch instead of a
+    Workspace, for callers that must not allocate while they run (``y`` is
+    therefore required). At most 8 tokens. Calls whose GPU work overlaps on
+    one device race on that scratch; make the first call on a device before
+    any stream capture starts, since it looks the scratch up."""
+    M = _m(x)
+    L = (layer if isinstance(layer, Layer) else Layer.from_dict(layer)).struct()
+    _check(lib().fgm_moe_layer_fwd_noalloc(ctypes.byref(L), _ptr(x), _ptr(y), M, _ptr(topk_ids),
+                                           _ptr(topk_w), _stream(stream)))
     return y
 
 

@@ -5,6 +5,8 @@
 #include <stdio.h>
 #include <string.h>
 
+#include <mutex>
+
 #include "basic_kernels.cuh"
 #include "fused_step.cuh"
 
@@ -534,3 +536,75 @@ int fgm_read_status(void *ws, size_t ws_bytes, int clear, int32_t *status, void 
 }
 
 }  // extern "C"
+
+// ---------------------------------------------------------------- allocation-free layer call
+//
+// fgm_moe_layer_fwd_noalloc runs fgm_moe_layer_fwd on scratch that the library
+// owns: a module-scope device array reserved when the CUDA module is loaded,
+// so the call itself never allocates. Its capacity is one full workspace
+// (M <= FGM_MAX_M = 8, V = 0); the array is shared by every caller on a device.
+
+namespace {
+
+constexpr size_t kNoAllocScratchBytes = size_t(2) << 20;  // >= fgm_workspace_bytes(8, 0)
+
+}  // namespace
+
+static __device__ __align__(256) unsigned char g_noalloc_scratch[kNoAllocScratchBytes];
+
+namespace {
+
+void *g_noalloc_base[kMaxDevices];  // device address of g_noalloc_scratch, per device
+std::mutex g_noalloc_mu;
+
+// Resolves (once per device, with that device current) the address of the
+// module-scope scratch. Nothing is allocated; the CUDA runtime may load the
+// module on this first query.
+int noalloc_scratch(void **base)
+{
+    int dev = 0;
+    FGM_CUDA(cudaGetDevice(&dev));
+    if (dev < 0 || dev >= kMaxDevices)
+        return fail(FGM_ERR_DEVICE, "device index %d out of range", dev);
+    std::lock_guard<std::mutex> lock(g_noalloc_mu);
+    if (!g_noalloc_base[dev]) {
+        if (ws_offsets().total > kNoAllocScratchBytes)
+            return fail(FGM_ERR_WORKSPACE, "built-in scratch of %zu bytes is below the %zu a layer call needs",
+                        kNoAllocScratchBytes, ws_offsets().total);
+        void *p = nullptr;
+        const cudaError_t e = cudaGetSymbolAddress(&p, g_noalloc_scratch);
+        if (e != cudaSuccess || !p)
+            return fail(FGM_ERR_CUDA, "cudaGetSymbolAddress(built-in scratch) failed: %s",
+                        cudaGetErrorString(e));
+        if (reinterpret_cast<uintptr_t>(p) & 255u)
+            return fail(FGM_ERR_WORKSPACE, "built-in scratch is not 256-byte aligned");
+        g_noalloc_base[dev] = p;
+    }
+    *base = g_noalloc_base[dev];
+    return FGM_OK;
+}
+
+}  // namespace
+
+extern "C" int fgm_moe_layer_fwd_noalloc(const fgm_layer *layer, const uint16_t *x, uint16_t *y, int M,
+                                         int32_t *topk_ids, float *topk_w, void *stream)
+{
+    if (M < 1 || M > kMaxM)
+        return fail(FGM_ERR_INVALID_ARG,
+                    "M = %d outside [1, %d]: the built-in scratch of fgm_moe_layer_fwd_noalloc holds at most "
+                    "%d tokens", M, kMaxM, kMaxM);
+    FGM_TRY(check_layer(layer, 0));
+    if (!x || !y || !aligned16(x) || !aligned16(y))
+        return fail(FGM_ERR_INVALID_ARG, "x/y NULL or not 16-byte aligned");
+    if (x == y)
+        return fail(FGM_ERR_INVALID_ARG, "y may not alias x");
+    FGM_TRY(device_ready(nullptr));
+    void *base = nullptr;
+    FGM_TRY(noalloc_scratch(&base));
+    // The status word and the grid-barrier counters must start at zero; the
+    // kernels initialise every other region they read.
+    const WsOffsets o = ws_offsets();
+    FGM_CUDA(cudaMemsetAsync(static_cast<char *>(base) + o.status, 0, o.total - o.status,
+                             static_cast<cudaStream_t>(stream)));
+    return fgm_moe_layer_fwd(layer, x, y, M, topk_ids, topk_w, base, o.total, stream);
+}

@@ -114,6 +114,32 @@ int fgm_workspace_init(void *ws, size_t ws_bytes, void *stream);
 int fgm_moe_layer_fwd(const fgm_layer *layer, const uint16_t *x, uint16_t *y, int M,
                       int32_t *topk_ids, float *topk_w, void *ws, size_t ws_bytes, void *stream);
 
+/* fgm_moe_layer_fwd without a caller workspace, for callers that may not
+ * allocate device memory while they run: a serving loop whose memory pool is
+ * already handed out to weights and caches, a host framework that owns every
+ * allocation and forbids them inside its per-step hook, or latency-critical
+ * code where a cudaMalloc/cudaFree could stall on a device-wide
+ * synchronisation. The operation is the same as fgm_moe_layer_fwd (same
+ * arguments, same results); the pages describe no such variant, it is an
+ * interface convenience only.
+ *  - Scratch: a fixed device array inside the library (2 MiB, enough for
+ *    M <= FGM_MAX_M = 8 tokens), reserved when the library's CUDA module is
+ *    loaded. The call allocates nothing; M outside [1, 8] returns
+ *    FGM_ERR_INVALID_ARG with a message naming the limit.
+ *  - Set-up: the first call on each device, with that device current, looks
+ *    up the array's device address (the CUDA runtime may load the module
+ *    then). Make that first call before any stream capture begins.
+ *  - Each call clears the array's status word and barrier counters on
+ *    `stream` before it launches.
+ *  - One array per device serves every caller on it: calls on that device
+ *    whose GPU work overlaps (other streams, other threads) race on the
+ *    scratch and give wrong results. Order them on one stream, or use
+ *    fgm_moe_layer_fwd with one workspace per stream.
+ *  - The status word cannot be read back (it lives in the library's array);
+ *    use fgm_moe_layer_fwd when the status must be checked. */
+int fgm_moe_layer_fwd_noalloc(const fgm_layer *layer, const uint16_t *x, uint16_t *y, int M,
+                              int32_t *topk_ids, float *topk_w, void *stream);
+
 /* n_layers stacked layers (attention omitted), each
  *   h <- h + moe_layer(RMSNorm(h)),  RMSNorm(h) = h / sqrt(mean(h^2) + 1e-6),
  * starting from h = x; the residual stream stays fp32 inside the call.
