@@ -94,7 +94,7 @@ constexpr int kTraceDetail = 8;
 
 struct __align__(128) Smem {
     uint8_t ring[kStages][kSlotBytes];
-    float4 red[kMW][kDownTiles][32];   // per-warp K-slice partials of up to 4 tiles
+    float4 red[2][kMW][2][32];   // per-warp K-slice partials of up to 2 tiles, double-buffered
     float part[kMW][8];
     float part2[kMW][8];
     float best_v[kMW][8];       // lm_head winners per reducing warp and token
@@ -449,12 +449,12 @@ __device__ __forceinline__ void gu_products(const uint4 (&ra)[4], const uint4 (&
 
 // Sum of the 11 K-slice partials of lane ln of tile t:
 // (row ln/4, cols 2(ln%4), 2(ln%4)+1) in x, y and row ln/4 + 8 in z, w.
-__device__ __forceinline__ float4 red_sum4(const Smem &s, int t, int ln)
+__device__ __forceinline__ float4 red_sum4(const Smem &s, int b, int t, int ln)
 {
-    float4 v = s.red[0][t][ln];
+    float4 v = s.red[b][0][t][ln];
 #pragma unroll
     for (int w = 1; w < kMW; ++w) {
-        const float4 f = s.red[w][t][ln];
+        const float4 f = s.red[b][w][t][ln];
         v.x += f.x;
         v.y += f.y;
         v.z += f.z;
@@ -585,8 +585,12 @@ __global__ void __launch_bounds__(kThreads, 1) k_fused(const __grid_constant__ P
                         uint8_t *dst = claim(static_cast<uint32_t>(nv) * kF);
                         if (!dst)
                             break;
-                        bulk_g2s(dst, L.down_q + ((size_t)e * kH + row) * kF, static_cast<uint32_t>(nv) * kF,
-                                 &s.full[stage % kStages]);
+                        // 4-row (2816-byte) pieces: many mid-sized copies keep more
+                        // requests in flight than one 45 KB copy
+                        const uint8_t *src = L.down_q + ((size_t)e * kH + row) * kF;
+                        for (int r4 = 0; r4 < nv; r4 += 4)
+                            bulk_g2s(dst + r4 * kF, src + (size_t)r4 * kF,
+                                     static_cast<uint32_t>(min(4, nv - r4)) * kF, &s.full[stage % kStages]);
                         ++stage;
                     }
                 }
@@ -749,29 +753,38 @@ __global__ void __launch_bounds__(kThreads, 1) k_fused(const __grid_constant__ P
         }
     };
 
-    // The partials of a stage's nt tiles meet in shared memory; after a barrier
-    // the first 32 nt threads sum one tile each and apply its epilogue.
-    auto exchange = [&](const int4 &m, const float (&part)[kDownTiles][4], int nt) {
+    // The partials of nt <= 2 tiles meet in shared memory buffer rbuf; after
+    // one barrier, nt reducer warps (rotating over the posts) sum one tile each
+    // and apply its epilogue while the other warps go on to their next
+    // products. The buffers alternate: a buffer is written again only after the
+    // next post's barrier, which its reducers reach after they are done. Every
+    // read of an epilogue's results is preceded by a barrier (the next post's
+    // or a grid barrier's).
+    int rbuf = 0;
+    int rot = 0;   // first reducer warp of the next post
+    auto post = [&](const int4 &m, const float (&part)[2][4], int nt, int t_off) {
 #pragma unroll
-        for (int t = 0; t < kDownTiles; ++t)
+        for (int t = 0; t < 2; ++t)
             if (t < nt)
-                s.red[warp][t][lane] = make_float4(part[t][0], part[t][1], part[t][2], part[t][3]);
+                s.red[rbuf][warp][t][lane] = make_float4(part[t][0], part[t][1], part[t][2], part[t][3]);
         consumer_sync();
-        if (tid < 32 * nt) {
-            const int t = tid >> 5;
-            finish_tile(m, t, red_sum4(s, t, lane));
-        }
-        consumer_sync();
+        int t = warp - rot;
+        if (t < 0)
+            t += kMW;
+        if (t < nt)
+            finish_tile(m, t_off + t, red_sum4(s, rbuf, t, lane));
+        rbuf ^= 1;
+        rot = rot + 1 == kMW ? 0 : rot + 1;
         if (tid == 0 && cta == 0)
             dstamp(stage - 1, layer_stage0, 4);
     };
     auto exchange1 = [&](const int4 &m, float x, float y, float z, float w) {
-        float part[kDownTiles][4];
+        float part[2][4];
         part[0][0] = x;
         part[0][1] = y;
         part[0][2] = z;
         part[0][3] = w;
-        exchange(m, part, 1);
+        post(m, part, 1, 0);
     };
 
     // One gate/up tile (rows i..i+nv-1 of one expert, written to act slot
@@ -823,6 +836,8 @@ __global__ void __launch_bounds__(kThreads, 1) k_fused(const __grid_constant__ P
                 for (int c = 0; c < 4; ++c)
                     asm volatile("prefetch.global.L1 [%0];" ::"l"(wrow + 64 * c));
             }
+            // router bias of this CTA's expert, fetched early (off the critical path)
+            const float rbias = (router_cta && tid < M && L.router_b) ? __ldg(L.router_b + cta) : 0.0f;
             if (g < M) {
                 if (from_x)
                     load_slice_bf16(p.x + (size_t)g * kH, warp, q, v);
@@ -900,7 +915,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_fused(const __grid_constant__ P
                         tot += s.part[w][tid];
                     }
                     const float rt = norm ? 1.0f / sqrtf(tot / static_cast<float>(kH) + kEps) : 1.0f;
-                    __stcg(ws.logits + tid * kE + cta, z * rt + (L.router_b ? L.router_b[cta] : 0.0f));
+                    __stcg(ws.logits + tid * kE + cta, z * rt + rbias);
                 }
                 // activation terms for the gate/up products (this warp's K-slice, token g)
                 float amax = 0.0f;
@@ -1126,9 +1141,9 @@ __global__ void __launch_bounds__(kThreads, 1) k_fused(const __grid_constant__ P
                 }
                 const bool got = stage_wait();
                 const uint8_t *slot = s.ring[stage % kStages];
-                float po[kDownTiles][4];
 #pragma unroll
                 for (int t0 = 0; t0 < kDownTiles; t0 += 2) {
+                    float po[2][4];
                     // two tiles x 3 terms = 6 independent accumulator chains
                     float acc[2][kTerms][4];
 #pragma unroll
@@ -1164,13 +1179,16 @@ __global__ void __launch_bounds__(kThreads, 1) k_fused(const __grid_constant__ P
 #pragma unroll
                             for (int tt = 0; tt < kTerms; ++tt)
                                 o += acc[t][tt][e2] * it[tt][e2 & 1];
-                            po[t0 + t][e2] = o;
+                            po[t][e2] = o;
                         }
+                    if (t0 + 2 == kDownTiles) {
+                        if (tid == 0)
+                            dstamp(stage, layer_stage0, 2);
+                        stage_release();
+                    }
+                    // tiles t0, t0 + 1 (rows beyond the stage's nv rows are skipped)
+                    post(make_int4(kTileDown, j, pos - ds.begin, nv), po, 2, t0);
                 }
-                if (tid == 0)
-                    dstamp(stage, layer_stage0, 2);
-                stage_release();
-                exchange(make_int4(kTileDown, j, pos - ds.begin, nv), po, kDownTiles);
             }
         }
         stamp(9);
