@@ -171,8 +171,8 @@ TRACE_STAGES = 48
 def write_phase_trace(path, fgm, layers, emb, x, draft, ws, arr, dev):
     """One traced verify step: per layer and phase, the time at which the last
     CTA (and the median CTA) reached each phase boundary, relative to the
-    first CTA starting the layer, averaged over the layers; then CTA 0's ring
-    stages of two layers."""
+    first CTA starting the layer, averaged over the layers; then the ring
+    stages of two layers as seen by CTA G/2."""
     import torch
     G = torch.cuda.get_device_properties(dev).multi_processor_count
     n = (N_LAYERS * NTP + 2) * G + N_LAYERS * TRACE_STAGES * 8
@@ -207,13 +207,13 @@ def write_phase_trace(path, fgm, layers, emb, x, draft, ws, arr, dev):
     lines.append(f"lm_head + accept (last CTA end - first CTA after layers): {float(tail) / 1e3:.2f} us")
     for l in (1, N_LAYERS // 2):
         base = float(det[l, 0, 7])
-        lines.append(f"CTA 0, layer {l}: stage  issue  landed  products  released  epilogue"
+        lines.append(f"CTA {G // 2}, layer {l}: stage  issue  wait-from  landed  products  released  posted"
                      f"  (SM cycles from its layer start)")
         for k in range(TRACE_STAGES):
             row = det[l, k]
             if row[1] == 0:
                 break
-            vals = ["%8d" % int(float(v) - base) if v != 0 else "       -" for v in row[:5]]
+            vals = ["%8d" % int(float(row[c]) - base) if row[c] != 0 else "       -" for c in (0, 5, 1, 2, 3, 4)]
             lines.append(f"  {k:3d}  " + "  ".join(vals))
     with open(path, "w") as f:
         f.write("\n".join(lines) + "\n")

@@ -62,6 +62,12 @@ constexpr int kMaxDownRows = kMaxSlots * kH / kMinCtas + 2;       // down rows p
 enum Mode { kModeLayer = 0, kModeStack = 1, kModeVerify = 2, kModeLmHead = 3 };
 enum TileKind { kTileGateUp = 0, kTileDown = 1, kTileLmHead = 2 };
 
+// Compile-time tile kind: each exchange site carries only its own epilogue.
+template <int K>
+struct KindTag {
+    static constexpr int value = K;
+};
+
 struct Params {
     fgm_layer layers[FGM_MAX_LAYERS];
     int n_layers;
@@ -85,9 +91,9 @@ struct Params {
 
 // Profiling aid (Params::trace): per layer kTracePoints phase stamps for every
 // CTA, [(l * kTracePoints + k) * G + cta], then two end stamps per CTA, then
-// for CTA 0 only a per-stage timeline [l][kTraceStages][8] of SM clock64
-// values = {producer issue, data landed, products done, slot released,
-// epilogue done, -, -, layer start}.
+// for CTA G/2 only a per-stage timeline [l][kTraceStages][8] of SM clock64
+// values = {producer issue, data landed, products done, slot released, last
+// exchange posted, consumer wait begun, -, layer start}.
 constexpr int kTracePoints = 10;
 constexpr int kTraceStages = 48;
 constexpr int kTraceDetail = 8;
@@ -353,11 +359,12 @@ struct DownStages {
         rot = n > 0 ? (cta * 7) % n : 0;
     }
     // i-th stage in visiting order: absolute position and row count
-    __device__ void get(int i, int &pos, int &nv) const
+    __device__ void get(int i, int &pos, int &nv) const { at(k0 + (i + rot) % n, pos, nv); }
+    // stage of 64-row block k
+    __device__ void at(int k, int &pos, int &nv) const
     {
         constexpr int kBlk = kDownTiles * 16;
         constexpr int kBlocksPerSlot = kH / kBlk;
-        const int k = k0 + (i + rot) % n;
         const int start = (k / kBlocksPerSlot) * kH + (k % kBlocksPerSlot) * kBlk;
         pos = max(begin, start);
         nv = min(end, start + kBlk) - pos;
@@ -447,6 +454,38 @@ __device__ __forceinline__ void gu_products(const uint4 (&ra)[4], const uint4 (&
     }
 }
 
+// Gate/up epilogue of one reduced tile, out of line (one copy of the code):
+// lane holds gate (x, y) and up (z, w) of row r0 = lane / 4 for tokens n0 =
+// 2 (lane % 4) and n0 + 1; writes act = comb * gelu_tanh(s_g g) * (s_u u) for
+// the tokens < M. dst points at act[aslot][n0][i + r0].
+__device__ __forceinline__ void gu_epilogue(float *dst, float4 f, float sg, float su, float c0, float c1, bool t0,
+                                         bool t1)
+{
+    if (t0)
+        __stcg(dst, gelu_tanh(sg * f.x) * (su * f.z) * c0);
+    if (t1)
+        __stcg(dst + kF, gelu_tanh(sg * f.y) * (su * f.w) * c1);
+}
+
+// Down epilogue of one reduced tile: adds s_d * partial into the
+// residual h for rows r0 (x, y) and r0 + 8 (z, w), tokens n0 and n0 + 1.
+__device__ __forceinline__ void down_epilogue(float *h0, float4 f, float sd0, float sd1, bool r0ok, bool r1ok, bool t0,
+                                           bool t1)
+{
+    if (r0ok) {
+        if (t0)
+            atomicAdd(h0, f.x * sd0);
+        if (t1)
+            atomicAdd(h0 + kH, f.y * sd0);
+    }
+    if (r1ok) {
+        if (t0)
+            atomicAdd(h0 + 8, f.z * sd1);
+        if (t1)
+            atomicAdd(h0 + kH + 8, f.w * sd1);
+    }
+}
+
 // Sum of the 11 K-slice partials of lane ln of tile t:
 // (row ln/4, cols 2(ln%4), 2(ln%4)+1) in x, y and row ln/4 + 8 in z, w.
 __device__ __forceinline__ float4 red_sum4(const Smem &s, int b, int t, int ln)
@@ -494,7 +533,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_fused(const __grid_constant__ P
         if (lane == 0) {
             uint32_t stage = 0;
             bool ok = true;
-            long long *pdetail = (p.trace && cta == 0)
+            long long *pdetail = (p.trace && cta == G / 2)
                                      ? p.trace + (size_t)(n_layers * kTracePoints + 2) * G : nullptr;
             int p_layer = 0;
             uint32_t p_stage0 = 0;
@@ -654,7 +693,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_fused(const __grid_constant__ P
         consumer_sync();
     };
 
-    long long *detail = (p.trace && cta == 0)
+    long long *detail = (p.trace && cta == G / 2)
                             ? p.trace + (size_t)(n_layers * kTracePoints + 2) * G : nullptr;
     int cur_layer = 0;
     uint32_t layer_stage0 = 0;
@@ -664,6 +703,8 @@ __global__ void __launch_bounds__(kThreads, 1) k_fused(const __grid_constant__ P
     };
     // MMA warps: wait for the next ring stage (false after an abort) and release it
     auto stage_wait = [&]() -> bool {
+        if (tid == 0)
+            dstamp(stage, layer_stage0, 5);
         const bool ok = mbar_wait(&s.full[stage % kStages], (stage / kStages) & 1, s, deadline, status, 3, (int)stage);
         if (tid == 0)
             dstamp(stage, layer_stage0, 1);
@@ -687,10 +728,10 @@ __global__ void __launch_bounds__(kThreads, 1) k_fused(const __grid_constant__ P
 
     // Epilogue of one reduced 16 x 8 tile; lane holds rows r0 = lane / 4 (x, y)
     // and r0 + 8 (z, w), columns n0 = 2 (lane % 4) and n0 + 1.
-    auto finish_tile = [&](const int4 &m, int tl, const float4 &f) {
+    auto finish_tile = [&](auto kind_tag, const int4 &m, int tl, const float4 &f) {
         const int r0 = lane >> 2, n0 = (lane & 3) * 2;
-        const int kind = m.x & 3;
-        if (kind == kTileGateUp) {
+        constexpr int kind = decltype(kind_tag)::value;
+        if constexpr (kind == kTileGateUp) {
             // m.x >> 2 = act slot, m.y = first row, m.z = row pairs | (k0 << 8), m.w = comb slot or -1;
             // x, y: gate of row r0; z, w: up of row r0
             const int aslot = m.x >> 2, i = m.y, nv = m.z & 0xFF, k0 = m.z >> 8;
@@ -698,29 +739,17 @@ __global__ void __launch_bounds__(kThreads, 1) k_fused(const __grid_constant__ P
                 const float sg = s.sc_g[k0 + r0], su = s.sc_u[k0 + r0];
                 const float c0 = m.w >= 0 ? s.comb[cur_pb][m.w][n0] : 1.0f;
                 const float c1 = m.w >= 0 ? s.comb[cur_pb][m.w][n0 + 1] : 1.0f;
-                float *dst = ws.act + ((size_t)aslot * kMaxM + n0) * kF + i + r0;
-                if (n0 < M)
-                    __stcg(dst, gelu_tanh(sg * f.x) * (su * f.z) * c0);
-                if (n0 + 1 < M)
-                    __stcg(dst + kF, gelu_tanh(sg * f.y) * (su * f.w) * c1);
+                gu_epilogue(ws.act + ((size_t)aslot * kMaxM + n0) * kF + i + r0, f, sg, su, c0, c1, n0 < M,
+                            n0 + 1 < M);
             }
-        } else if (kind == kTileDown) {
+        } else if constexpr (kind == kTileDown) {
             // tile tl of a 64-row stage: m.y = first output row j of the stage, m.z = scale
             // index of that row, m.w = valid rows of the stage
             const int j = m.y + 16 * tl, k0 = m.z + 16 * tl, nv = m.w - 16 * tl;
             if (r0 < nv) {
-                const float sd = s.sc_d[k0 + r0];
-                if (n0 < M)
-                    atomicAdd(ws.h + (size_t)n0 * kH + j + r0, f.x * sd);
-                if (n0 + 1 < M)
-                    atomicAdd(ws.h + (size_t)(n0 + 1) * kH + j + r0, f.y * sd);
-            }
-            if (r0 + 8 < nv) {
-                const float sd = s.sc_d[k0 + r0 + 8];
-                if (n0 < M)
-                    atomicAdd(ws.h + (size_t)n0 * kH + j + r0 + 8, f.z * sd);
-                if (n0 + 1 < M)
-                    atomicAdd(ws.h + (size_t)(n0 + 1) * kH + j + r0 + 8, f.w * sd);
+                const float sd0 = s.sc_d[k0 + r0];
+                const float sd1 = r0 + 8 < nv ? s.sc_d[k0 + r0 + 8] : 0.0f;
+                down_epilogue(ws.h + (size_t)n0 * kH + j + r0, f, sd0, sd1, true, r0 + 8 < nv, n0 < M, n0 + 1 < M);
             }
         } else {
             // m.y = first vocabulary row v0, m.z = valid rows
@@ -762,7 +791,8 @@ __global__ void __launch_bounds__(kThreads, 1) k_fused(const __grid_constant__ P
     // or a grid barrier's).
     int rbuf = 0;
     int rot = 0;   // first reducer warp of the next post
-    auto post = [&](const int4 &m, const float (&part)[2][4], int nt, int t_off) {
+    auto post = [&](auto kind_tag, const int4 &m0, const int4 &m1, const float (&part)[2][4], int nt, int t_off,
+                    bool last_of_stage) {
 #pragma unroll
         for (int t = 0; t < 2; ++t)
             if (t < nt)
@@ -772,27 +802,31 @@ __global__ void __launch_bounds__(kThreads, 1) k_fused(const __grid_constant__ P
         if (t < 0)
             t += kMW;
         if (t < nt)
-            finish_tile(m, t_off + t, red_sum4(s, rbuf, t, lane));
+            finish_tile(kind_tag, t ? m1 : m0, t_off + t, red_sum4(s, rbuf, t, lane));
         rbuf ^= 1;
         rot = rot + 1 == kMW ? 0 : rot + 1;
-        if (tid == 0 && cta == 0)
+        if (tid == 0 && last_of_stage)
             dstamp(stage - 1, layer_stage0, 4);
     };
-    auto exchange1 = [&](const int4 &m, float x, float y, float z, float w) {
+    auto exchange1 = [&](auto kind_tag, const int4 &m, float x, float y, float z, float w) {
         float part[2][4];
         part[0][0] = x;
         part[0][1] = y;
         part[0][2] = z;
         part[0][3] = w;
-        post(m, part, 1, 0);
+        post(kind_tag, m, m, part, 1, 0, true);
     };
 
     // One gate/up tile (rows i..i+nv-1 of one expert, written to act slot
     // aslot): act[aslot][n][i + ii] = comb * gelu_tanh(s_g g) * (s_u u).
-    auto gu_tile = [&](int aslot, int comb_slot, int i, int nv, int k0) {
+    // Products of the gate/up tile at the ring head into part (the caller
+    // posts tiles in pairs: one exchange barrier per two ring stages).
+    auto gu_tile = [&](float (&part)[4]) {
         uint4 ra[4], rb[4];
         const bool got = stage_wait();
-        float part[4] = {0.0f, 0.0f, 0.0f, 0.0f};
+#pragma unroll
+        for (int e = 0; e < 4; ++e)
+            part[e] = 0.0f;
         if (got) {
             load_a_wide(s.ring[stage % kStages], warp, g, q, ra, rb);
             gu_products(ra, rb, bx, inv_x, part);
@@ -800,8 +834,6 @@ __global__ void __launch_bounds__(kThreads, 1) k_fused(const __grid_constant__ P
         stage_release();
         if (tid == 0)
             dstamp(stage - 1, layer_stage0, 2);
-        exchange1(make_int4(kTileGateUp | (aslot << 2), i, nv | (k0 << 8), comb_slot), part[0], part[1], part[2],
-                  part[3]);
     };
 
     for (int l = 0; l < n_layers; ++l) {
@@ -1062,6 +1094,9 @@ __global__ void __launch_bounds__(kThreads, 1) k_fused(const __grid_constant__ P
             // before the routing was known), then its routed rows
             const int n_sh = (rsh.end - rsh.begin + 7) / 8;
             int pos = rg.begin;
+            float pend[2][4];
+            int4 pend_m = make_int4(0, 0, 0, 0);
+            bool have_pend = false;
             for (int it = 0;; ++it) {
                 int aslot, i, nv, k0, cslot = -1;
                 if (it < n_sh) {
@@ -1080,7 +1115,21 @@ __global__ void __launch_bounds__(kThreads, 1) k_fused(const __grid_constant__ P
                     k0 = pos - rg.begin;
                     pos += nv;
                 }
-                gu_tile(aslot, cslot, i, nv, k0);
+                const int4 m = make_int4(kTileGateUp | (aslot << 2), i, nv | (k0 << 8), cslot);
+                const bool last = !(it + 1 < n_sh || pos < rg.end);
+                if (!have_pend) {
+                    gu_tile(pend[0]);
+                    pend_m = m;
+                    have_pend = true;
+                    if (last) {
+                        post(KindTag<kTileGateUp>{}, m, m, pend, 1, 0, true);
+                        have_pend = false;
+                    }
+                } else {
+                    gu_tile(pend[1]);
+                    post(KindTag<kTileGateUp>{}, pend_m, m, pend, 2, 0, true);
+                    have_pend = false;
+                }
             }
         }
         stamp(7);
@@ -1124,9 +1173,11 @@ __global__ void __launch_bounds__(kThreads, 1) k_fused(const __grid_constant__ P
                 split16_into(v, S, bd[h2]);
                 column_inv(S, q, inv_d[h2]);
             }
+            int kk = ds.rot;   // visiting order without a division per stage
             for (int di = 0; di < ds.n; ++di) {
                 int pos, nv;
-                ds.get(di, pos, nv);
+                ds.at(ds.k0 + kk, pos, nv);
+                kk = kk + 1 == ds.n ? 0 : kk + 1;
                 const int si = pos / kH, j = pos % kH;
                 const int hs = si == si0 ? 0 : 1;
                 uint32_t bt[kTerms][4];
@@ -1187,7 +1238,8 @@ __global__ void __launch_bounds__(kThreads, 1) k_fused(const __grid_constant__ P
                         stage_release();
                     }
                     // tiles t0, t0 + 1 (rows beyond the stage's nv rows are skipped)
-                    post(make_int4(kTileDown, j, pos - ds.begin, nv), po, 2, t0);
+                    const int4 md = make_int4(kTileDown, j, pos - ds.begin, nv);
+                    post(KindTag<kTileDown>{}, md, md, po, 2, t0, t0 + 2 == kDownTiles);
                 }
             }
         }
@@ -1281,7 +1333,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_fused(const __grid_constant__ P
                 }
                 stage_release();
             }
-            exchange1(make_int4(kTileLmHead, v0, nv, 0), acc[0][0] + acc[1][0], acc[0][1] + acc[1][1],
+            exchange1(KindTag<kTileLmHead>{}, make_int4(kTileLmHead, v0, nv, 0), acc[0][0] + acc[1][0], acc[0][1] + acc[1][1],
                       acc[0][2] + acc[1][2], acc[0][3] + acc[1][3]);
         }
         if (lane < 4) {

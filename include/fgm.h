@@ -210,9 +210,10 @@ long long fgm_set_wait_limit_ns(long long ns);
  * terms ready, 4 shared gate/up done, 5 after barrier 1, 6 routing known,
  * 7 routed gate/up done, 8 after barrier 2, 9 down done; then [(L*10) * G + cta]
  * after the last layer and [(L*10 + 1) * G + cta] at the end (G = CTAs, one
- * per SM). Then, for CTA 0 only, [L][48][8] SM clock64 values per ring stage
- * of each layer: producer issue, data landed, products done, slot released,
- * epilogue done, two unused, and (stage 0 only) the layer start. A buffer
+ * per SM). Then, for CTA G/2 only, [L][48][8] SM clock64 values per ring stage
+ * of each layer: producer issue, data landed (consumer wait over), products
+ * done, slot released, last exchange of the stage posted, consumer wait
+ * begun, unused, and (stage 0 only) the layer start. A buffer
  * shorter than (L*10 + 2) * G + L*48*8 entries disables recording. NULL stops. */
 int fgm_set_phase_trace(long long *buf, size_t n);
 
