@@ -163,7 +163,8 @@ def cpu_oracle_step(layers, emb, x, draft_seed, log_prefix="[oracle]"):
 # ---------------------------------------------------------------- phase trace
 TRACE_POINTS = ("layer start", "norm/router partials", "partials reduced", "activation terms",
                 "shared gate/up done", "barrier 1 passed", "routing known", "routed gate/up done",
-                "barrier 2 passed", "down done")
+                "barrier 2 passed", "down done", "top-k done", "expert list done")
+TRACE_ORDER = (1, 2, 3, 4, 5, 10, 11, 6, 7, 8, 9)   # the points in the order a layer reaches them
 NTP = len(TRACE_POINTS)
 TRACE_STAGES = 48
 
@@ -201,7 +202,7 @@ def write_phase_trace(path, fgm, layers, emb, x, draft, ws, arr, dev):
             med[k] += float(tr[l * NTP + k].median() - base) / 1e3 / N_LAYERS
     lines.append(f"mean layer period (first CTA to first CTA): {period:.2f} us")
     lines.append("point                      last CTA (us)   median CTA (us)   from layer start")
-    for k in range(1, NTP):
+    for k in TRACE_ORDER:
         lines.append(f"{TRACE_POINTS[k]:26s} {last[k]:12.2f} {med[k]:16.2f}")
     tail = tr[N_LAYERS * NTP + 1].max() - tr[N_LAYERS * NTP].min()
     lines.append(f"lm_head + accept (last CTA end - first CTA after layers): {float(tail) / 1e3:.2f} us")

@@ -43,6 +43,8 @@ struct Ws {
     int32_t *io_out;   // [2]
     int32_t *status;   // [1] FGM_STATUS_* bits
     unsigned *sync;    // [64] grid-barrier counters
+    uint8_t *xterms;   // [8][3][2816] E4M3 terms of the gate/up input of the current layer
+    float *xscale;     // [8][11] their power-of-two scale per token and 256-wide K-slice
 };
 
 __host__ __device__ inline size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
@@ -50,7 +52,7 @@ __host__ __device__ inline size_t align_up(size_t x, size_t a) { return (x + a -
 // Byte offsets of every region; the same function serves host and device.
 struct WsOffsets {
     size_t h, xn, acc, logits, meta, comb, act, ids, wts, part_val, part_idx, hb, argmax, io_x,
-        io_draft, io_out, status, sync, total;
+        io_draft, io_out, status, sync, xterms, xscale, total;
 };
 
 inline WsOffsets ws_offsets()
@@ -80,6 +82,8 @@ inline WsOffsets ws_offsets()
     o.io_out = take(sizeof(int32_t) * 2);
     o.status = take(sizeof(int32_t) * 64);
     o.sync = take(sizeof(unsigned) * 64);
+    o.xterms = take(static_cast<size_t>(kMaxM) * 3 * kH);
+    o.xscale = take(sizeof(float) * kMaxM * 11);
     o.total = p;
     return o;
 }
@@ -107,6 +111,8 @@ inline Ws ws_carve(void *base)
     w.io_out = reinterpret_cast<int32_t *>(b + o.io_out);
     w.status = reinterpret_cast<int32_t *>(b + o.status);
     w.sync = reinterpret_cast<unsigned *>(b + o.sync);
+    w.xterms = reinterpret_cast<uint8_t *>(b + o.xterms);
+    w.xscale = reinterpret_cast<float *>(b + o.xscale);
     return w;
 }
 

@@ -89,11 +89,16 @@ int device_ready(int *sms)
             FGM_SMEM(k_lmhead_basic<7>, 7 * kH * 4);
             FGM_SMEM(k_lmhead_basic<8>, 8 * kH * 4);
 #undef FGM_SMEM
-            FGM_CUDA(cudaFuncSetAttribute(fused::k_fused, cudaFuncAttributeMaxDynamicSharedMemorySize,
+            FGM_CUDA(cudaFuncSetAttribute(fused::k_fused<2>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                           (int)sizeof(fused::Smem)));
-            int per_sm = 0;
-            FGM_CUDA(cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, fused::k_fused, fused::kThreads,
+            FGM_CUDA(cudaFuncSetAttribute(fused::k_fused<3>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                          (int)sizeof(fused::Smem)));
+            int per_sm = 0, per_sm3 = 0;
+            FGM_CUDA(cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, fused::k_fused<2>, fused::kThreads,
                                                                    sizeof(fused::Smem)));
+            FGM_CUDA(cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm3, fused::k_fused<3>, fused::kThreads,
+                                                                   sizeof(fused::Smem)));
+            per_sm = per_sm < per_sm3 ? per_sm : per_sm3;
             d.fused_grid = (per_sm >= 1 && d.sms >= fused::kMinCtas) ? d.sms : 0;
         }
         d.ready = true;
@@ -128,7 +133,10 @@ int launch_fused(fused::Params &prm, cudaStream_t st)
     prm.debug_stall = g_debug_stall;
     g_debug_stall = 0;
     void *args[] = {&prm};
-    FGM_CUDA(cudaLaunchCooperativeKernel(reinterpret_cast<const void *>(fused::k_fused), dim3(G),
+    // packed activation columns: 2 blocks of 8 hold M <= 5 tokens x 3 terms, 3 blocks M <= 8
+    const void *kern = prm.M <= 5 ? reinterpret_cast<const void *>(fused::k_fused<2>)
+                                  : reinterpret_cast<const void *>(fused::k_fused<3>);
+    FGM_CUDA(cudaLaunchCooperativeKernel(kern, dim3(G),
                                          dim3(fused::kThreads), args, sizeof(fused::Smem), st));
     return FGM_OK;
 }
@@ -604,7 +612,7 @@ extern "C" int fgm_moe_layer_fwd_noalloc(const fgm_layer *layer, const uint16_t 
     // The status word and the grid-barrier counters must start at zero; the
     // kernels initialise every other region they read.
     const WsOffsets o = ws_offsets();
-    FGM_CUDA(cudaMemsetAsync(static_cast<char *>(base) + o.status, 0, o.total - o.status,
+    FGM_CUDA(cudaMemsetAsync(static_cast<char *>(base) + o.status, 0, o.xterms - o.status,
                              static_cast<cudaStream_t>(stream)));
     return fgm_moe_layer_fwd(layer, x, y, M, topk_ids, topk_w, base, o.total, stream);
 }

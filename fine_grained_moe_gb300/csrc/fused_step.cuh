@@ -94,7 +94,7 @@ struct Params {
 // for CTA G/2 only a per-stage timeline [l][kTraceStages][8] of SM clock64
 // values = {producer issue, data landed, products done, slot released, last
 // exchange posted, consumer wait begun, -, layer start}.
-constexpr int kTracePoints = 10;
+constexpr int kTracePoints = 12;
 constexpr int kTraceStages = 48;
 constexpr int kTraceDetail = 8;
 
@@ -216,6 +216,17 @@ __device__ __forceinline__ void bulk_g2s(void *dst, const void *src, uint32_t by
 __device__ __forceinline__ void consumer_sync() { asm volatile("bar.sync 1, %0;" ::"n"(kConsumers) : "memory"); }
 
 __device__ __forceinline__ float4 ldcg4(const float *p) { return __ldcg(reinterpret_cast<const float4 *>(p)); }
+
+// 4-byte asynchronous global -> shared copy and the wait for all of a thread's copies.
+__device__ __forceinline__ void cp_async4(float *dst, const float *src)
+{
+    asm volatile("cp.async.ca.shared.global [%0], [%1], 4;" ::"r"(su32(dst)), "l"(src) : "memory");
+}
+
+__device__ __forceinline__ void cp_async_wait_all() { asm volatile("cp.async.wait_all;" ::: "memory"); }
+__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
+// all but the most recently committed group of this thread's copies have landed
+__device__ __forceinline__ void cp_async_wait_group1() { asm volatile("cp.async.wait_group 1;" ::: "memory"); }
 
 __device__ __forceinline__ void mma_e4m3(float (&c)[4], const uint32_t (&a)[4], uint32_t b0, uint32_t b1)
 {
@@ -420,6 +431,124 @@ __device__ __forceinline__ void load_a_wide(const uint8_t *slot, int warp, int g
     }
 }
 
+// Packed activation columns. An mma B fragment (k32 x n8) carries 8 columns
+// and each column is one (token, term) pair, so NB = 2 blocks hold the 15
+// columns of M <= 5 tokens x 3 terms and NB = 3 blocks the 24 of M <= 8.
+// Column c = 2 c' + e of block j holds
+//   block 0: token c', term e
+//   block 1: e = 0: token c', term 2
+//            e = 1: NB = 2: token 4, term c' (c' < 3; c' = 3 is empty)
+//                   NB = 3: token c' + 4, term 0
+//   block 2: token c' + 4, term 1 + e (NB = 3)
+// A thread's accumulator columns 2q, 2q + 1 of all blocks then cover every
+// term of token q and of its second token q2 (4, split over lanes q < 3, when
+// NB = 2; q + 4 when NB = 3). tok = -1 marks an empty column.
+template <int NB>
+__device__ __forceinline__ void column_of(int j, int c, int &tok, int &term)
+{
+    const int cc = c >> 1, e = c & 1;
+    if (j == 0) {
+        tok = cc;
+        term = e;
+    } else if (j == 1) {
+        if (e == 0) {
+            tok = cc;
+            term = 2;
+        } else if (NB == 2) {
+            tok = cc < 3 ? 4 : -1;
+            term = cc;
+        } else {
+            tok = cc + 4;
+            term = 0;
+        }
+    } else {
+        tok = cc + 4;
+        term = 1 + e;
+    }
+}
+
+// Term weights of a thread's columns: fa[t] = 16^-t / S(q), fb[t] = 16^-t / S(q2)
+// (NB = 3), fb[0] = 16^-q / S(4) (NB = 2); 0 for tokens >= M.
+template <int NB>
+__device__ __forceinline__ void column_weights(float sa, float sb, int q, int M, float (&fa)[3], float (&fb)[3])
+{
+    float f = 1.0f;
+#pragma unroll
+    for (int t = 0; t < 3; ++t) {
+        fa[t] = q < M ? f / sa : 0.0f;
+        fb[t] = (NB == 3 && q + 4 < M) ? f / sb : 0.0f;
+        f *= 0.0625f;
+    }
+    if (NB == 2)
+        fb[0] = (q < 3 && 4 < M) ? (q == 0 ? 1.0f : q == 1 ? 0.0625f : 0.00390625f) / sb : 0.0f;
+}
+
+// Combines the terms of a thread's packed accumulators into
+// {row r: token q, row r: token q2, row r + 8: token q, row r + 8: token q2}.
+template <int NB>
+__device__ __forceinline__ float4 combine_terms(const float (&acc)[NB][4], const float (&fa)[3], const float (&fb)[3])
+{
+    float4 r;
+    r.x = acc[0][0] * fa[0] + acc[0][1] * fa[1] + acc[1][0] * fa[2];
+    r.z = acc[0][2] * fa[0] + acc[0][3] * fa[1] + acc[1][2] * fa[2];
+    if constexpr (NB == 2) {
+        // token 4: this lane's column holds its term q; sum the quad's terms
+        r.y = quad_sum(acc[1][1] * fb[0]);
+        r.w = quad_sum(acc[1][3] * fb[0]);
+    } else {
+        r.y = acc[1][1] * fb[0] + acc[2][0] * fb[1] + acc[2][1] * fb[2];
+        r.w = acc[1][3] * fb[0] + acc[2][2] * fb[1] + acc[2][3] * fb[2];
+    }
+    return r;
+}
+
+// Gate/up products of one 16-row tile (rows 0..7 gate, 8..15 up) over warp w's
+// 256-byte K-slice with packed activation columns; returns the combined
+// partial {gate q, gate q2, up q, up q2} of row g.
+template <int NB>
+__device__ __forceinline__ float4 gu_products_packed(const uint4 (&ra)[4], const uint4 (&rb)[4],
+                                                     const uint32_t (&b)[4][NB][4], const float (&fa)[3],
+                                                     const float (&fb)[3])
+{
+    float acc[NB][4];
+#pragma unroll
+    for (int j = 0; j < NB; ++j)
+#pragma unroll
+        for (int e = 0; e < 4; ++e)
+            acc[j][e] = 0.0f;
+#pragma unroll
+    for (int c = 0; c < 4; ++c) {
+        const uint32_t a0[4] = {ra[c].x, rb[c].x, ra[c].y, rb[c].y};
+        const uint32_t a1[4] = {ra[c].z, rb[c].z, ra[c].w, rb[c].w};
+#pragma unroll
+        for (int j = 0; j < NB; ++j)
+            mma_e4m3(acc[j], a0, b[c][j][0], b[c][j][1]);
+#pragma unroll
+        for (int j = 0; j < NB; ++j)
+            mma_e4m3(acc[j], a1, b[c][j][2], b[c][j][3]);
+    }
+    return combine_terms<NB>(acc, fa, fb);
+}
+
+// E4M3 terms of 4 values (see split_terms16): w[t] packs term t of y[0..3].
+__device__ __forceinline__ void split_terms4(float (&y)[4], uint32_t (&w)[kTerms])
+{
+#pragma unroll
+    for (int t = 0; t < kTerms; ++t) {
+        const __nv_fp8x2_storage_t lo = __nv_cvt_float2_to_fp8x2(make_float2(y[0], y[1]), __NV_SATFINITE, __NV_E4M3);
+        const __nv_fp8x2_storage_t hi = __nv_cvt_float2_to_fp8x2(make_float2(y[2], y[3]), __NV_SATFINITE, __NV_E4M3);
+        w[t] = static_cast<uint32_t>(lo) | (static_cast<uint32_t>(hi) << 16);
+        if (t + 1 < kTerms) {
+            const float2 dl = __half22float2(__half2(__nv_cvt_fp8x2_to_halfraw2(lo, __NV_E4M3)));
+            const float2 dh = __half22float2(__half2(__nv_cvt_fp8x2_to_halfraw2(hi, __NV_E4M3)));
+            y[0] = (y[0] - dl.x) * 16.0f;
+            y[1] = (y[1] - dl.y) * 16.0f;
+            y[2] = (y[2] - dh.x) * 16.0f;
+            y[3] = (y[3] - dh.y) * 16.0f;
+        }
+    }
+}
+
 // Gate/up products of one 16-row tile over warp w's 256-byte K-slice; the
 // terms are combined with their weights into the 16 x 8 partial `out`.
 __device__ __forceinline__ void gu_products(const uint4 (&ra)[4], const uint4 (&rb)[4], const uint32_t (&b)[4][kTerms][4],
@@ -454,35 +583,32 @@ __device__ __forceinline__ void gu_products(const uint4 (&ra)[4], const uint4 (&
     }
 }
 
-// Gate/up epilogue of one reduced tile, out of line (one copy of the code):
-// lane holds gate (x, y) and up (z, w) of row r0 = lane / 4 for tokens n0 =
-// 2 (lane % 4) and n0 + 1; writes act = comb * gelu_tanh(s_g g) * (s_u u) for
-// the tokens < M. dst points at act[aslot][n0][i + r0].
-__device__ __forceinline__ void gu_epilogue(float *dst, float4 f, float sg, float su, float c0, float c1, bool t0,
-                                         bool t1)
+// Gate/up epilogue of one reduced tile: the lane holds gate (x, y) and up
+// (z, w) of one row for its tokens a and b; writes act = comb *
+// gelu_tanh(s_g g) * (s_u u) at dst_a / dst_b.
+__device__ __forceinline__ void gu_epilogue(float *dst_a, float *dst_b, float4 f, float sg, float su, float ca,
+                                            float cb, bool ta, bool tb)
 {
-    if (t0)
-        __stcg(dst, gelu_tanh(sg * f.x) * (su * f.z) * c0);
-    if (t1)
-        __stcg(dst + kF, gelu_tanh(sg * f.y) * (su * f.w) * c1);
+    if (ta)
+        __stcg(dst_a, gelu_tanh(sg * f.x) * (su * f.z) * ca);
+    if (tb)
+        __stcg(dst_b, gelu_tanh(sg * f.y) * (su * f.w) * cb);
 }
 
-// Down epilogue of one reduced tile: adds s_d * partial into the
-// residual h for rows r0 (x, y) and r0 + 8 (z, w), tokens n0 and n0 + 1.
-__device__ __forceinline__ void down_epilogue(float *h0, float4 f, float sd0, float sd1, bool r0ok, bool r1ok, bool t0,
-                                           bool t1)
+// Down epilogue of one reduced tile: adds s_d * partial into the residual
+// rows h_a (token a) and h_b (token b): x, y at row r, z, w at row r + 8.
+__device__ __forceinline__ void down_epilogue(float *h_a, float *h_b, float4 f, float sd0, float sd1, bool r1ok,
+                                              bool ta, bool tb)
 {
-    if (r0ok) {
-        if (t0)
-            atomicAdd(h0, f.x * sd0);
-        if (t1)
-            atomicAdd(h0 + kH, f.y * sd0);
+    if (ta) {
+        atomicAdd(h_a, f.x * sd0);
+        if (r1ok)
+            atomicAdd(h_a + 8, f.z * sd1);
     }
-    if (r1ok) {
-        if (t0)
-            atomicAdd(h0 + 8, f.z * sd1);
-        if (t1)
-            atomicAdd(h0 + kH + 8, f.w * sd1);
+    if (tb) {
+        atomicAdd(h_b, f.y * sd0);
+        if (r1ok)
+            atomicAdd(h_b + 8, f.w * sd1);
     }
 }
 
@@ -502,6 +628,7 @@ __device__ __forceinline__ float4 red_sum4(const Smem &s, int b, int t, int ln)
     return v;
 }
 
+template <int NB>
 __global__ void __launch_bounds__(kThreads, 1) k_fused(const __grid_constant__ Params p)
 {
     extern __shared__ __align__(128) uint8_t smem_raw[];
@@ -602,6 +729,12 @@ __global__ void __launch_bounds__(kThreads, 1) k_fused(const __grid_constant__ P
                 const fgm_layer &L = p.layers[l];
                 p_layer = l;
                 p_stage0 = stage;
+                // this layer's router row (and bias) into L2 ahead of phase A: the
+                // consumers are still in the previous layer's down rows
+                if (l > 0 && cta < kE)
+                    prefetch_l2(L.router_w + (size_t)cta * kH, kH * sizeof(uint16_t));
+                if (l > 0 && cta == kE - 1 && L.router_b)
+                    prefetch_l2(L.router_b, kE * sizeof(float));
                 // phase A: shared expert gate/up rows
                 const Range ra = split(kF, cta, G);
                 for (int i = ra.begin; i < ra.end && ok; i += 8)
@@ -718,38 +851,44 @@ __global__ void __launch_bounds__(kThreads, 1) k_fused(const __grid_constant__ P
             dstamp(stage, layer_stage0, 3);
         ++stage;
     };
-    uint32_t bx[4][kTerms][4];   // activation terms of this warp's K-slice (token g)
-    float inv_x[kTerms][2];
+    uint32_t bx[4][NB][4];   // packed activation columns of this warp's K-slice (gate/up)
+    float fa_x[3], fb_x[3];  // their term weights
     int cur_pb = 0;               // routing buffer of the current layer
     // lm_head: lanes 0..3 keep the running best of tokens 2 lane, 2 lane + 1
     // over the tiles this warp reduces
     float best_v[2] = {-INFINITY, -INFINITY};
     int best_i[2] = {0x7FFFFFFF, 0x7FFFFFFF};
 
-    // Epilogue of one reduced 16 x 8 tile; lane holds rows r0 = lane / 4 (x, y)
-    // and r0 + 8 (z, w), columns n0 = 2 (lane % 4) and n0 + 1.
+    // Epilogue of one reduced tile. Expert tiles (packed columns): the lane
+    // holds row r0 = lane / 4 in x, y and row r0 + 8 in z, w for its tokens
+    // qa = lane % 4 and qb. lm_head tiles: token columns n0 = 2 (lane % 4), n0 + 1.
     auto finish_tile = [&](auto kind_tag, const int4 &m, int tl, const float4 &f) {
         const int r0 = lane >> 2, n0 = (lane & 3) * 2;
         constexpr int kind = decltype(kind_tag)::value;
         if constexpr (kind == kTileGateUp) {
             // m.x >> 2 = act slot, m.y = first row, m.z = row pairs | (k0 << 8), m.w = comb slot or -1;
-            // x, y: gate of row r0; z, w: up of row r0
+            // x, y: gate of row r0; z, w: up of row r0 (the tile's rows 8.. are the up rows)
+            // lane: row r0, tokens qa = lane % 4 and qb (packed columns)
             const int aslot = m.x >> 2, i = m.y, nv = m.z & 0xFF, k0 = m.z >> 8;
+            const int qa = lane & 3, qb = NB == 2 ? 4 : qa + 4;
             if (r0 < nv) {
                 const float sg = s.sc_g[k0 + r0], su = s.sc_u[k0 + r0];
-                const float c0 = m.w >= 0 ? s.comb[cur_pb][m.w][n0] : 1.0f;
-                const float c1 = m.w >= 0 ? s.comb[cur_pb][m.w][n0 + 1] : 1.0f;
-                gu_epilogue(ws.act + ((size_t)aslot * kMaxM + n0) * kF + i + r0, f, sg, su, c0, c1, n0 < M,
-                            n0 + 1 < M);
+                const float ca = m.w >= 0 ? s.comb[cur_pb][m.w][qa] : 1.0f;
+                const float cb = m.w >= 0 ? s.comb[cur_pb][m.w][qb] : 1.0f;
+                float *base = ws.act + (size_t)aslot * kMaxM * kF + i + r0;
+                gu_epilogue(base + qa * kF, base + qb * kF, f, sg, su, ca, cb, qa < M,
+                            qb < M && (NB == 3 || qa == 0));
             }
         } else if constexpr (kind == kTileDown) {
             // tile tl of a 64-row stage: m.y = first output row j of the stage, m.z = scale
             // index of that row, m.w = valid rows of the stage
             const int j = m.y + 16 * tl, k0 = m.z + 16 * tl, nv = m.w - 16 * tl;
+            const int qa = lane & 3, qb = NB == 2 ? 4 : qa + 4;
             if (r0 < nv) {
                 const float sd0 = s.sc_d[k0 + r0];
                 const float sd1 = r0 + 8 < nv ? s.sc_d[k0 + r0 + 8] : 0.0f;
-                down_epilogue(ws.h + (size_t)n0 * kH + j + r0, f, sd0, sd1, true, r0 + 8 < nv, n0 < M, n0 + 1 < M);
+                down_epilogue(ws.h + (size_t)qa * kH + j + r0, ws.h + (size_t)qb * kH + j + r0, f, sd0, sd1,
+                              r0 + 8 < nv, qa < M, qb < M && (NB == 3 || qa == 0));
             }
         } else {
             // m.y = first vocabulary row v0, m.z = valid rows
@@ -829,7 +968,11 @@ __global__ void __launch_bounds__(kThreads, 1) k_fused(const __grid_constant__ P
             part[e] = 0.0f;
         if (got) {
             load_a_wide(s.ring[stage % kStages], warp, g, q, ra, rb);
-            gu_products(ra, rb, bx, inv_x, part);
+            const float4 f = gu_products_packed<NB>(ra, rb, bx, fa_x, fb_x);
+            part[0] = f.x;
+            part[1] = f.y;
+            part[2] = f.z;
+            part[3] = f.w;
         }
         stage_release();
         if (tid == 0)
@@ -885,9 +1028,10 @@ __global__ void __launch_bounds__(kThreads, 1) k_fused(const __grid_constant__ P
             // scales of this CTA's shared-expert gate/up rows (read after the
             // consumer barrier below)
             for (int i = tid; i < rsh.end - rsh.begin; i += kConsumers) {
-                s.sc_g[kMaxGuRows + i] = __ldg(L.gate_s + (size_t)kShared * kF + rsh.begin + i);
-                s.sc_u[kMaxGuRows + i] = __ldg(L.up_s + (size_t)kShared * kF + rsh.begin + i);
+                cp_async4(&s.sc_g[kMaxGuRows + i], L.gate_s + (size_t)kShared * kF + rsh.begin + i);
+                cp_async4(&s.sc_u[kMaxGuRows + i], L.up_s + (size_t)kShared * kF + rsh.begin + i);
             }
+            cp_async_commit();
             if (l == 0) {
                 // residual (stack) or accumulator (layer) initialisation, split over CTAs
                 for (int i = cta * kConsumers + tid; i < kMaxM * kH; i += G * kConsumers) {
@@ -931,14 +1075,6 @@ __global__ void __launch_bounds__(kThreads, 1) k_fused(const __grid_constant__ P
             consumer_sync();
             stamp(2);
             {
-                float r = 1.0f;
-                if (norm) {
-                    float tot = 0.0f;
-#pragma unroll
-                    for (int w = 0; w < kMW; ++w)
-                        tot += s.part[w][g];
-                    r = 1.0f / sqrtf(tot / static_cast<float>(kH) + kEps);
-                }
                 if (router_cta && tid < M) {
                     float z = 0.0f, tot = 0.0f;
 #pragma unroll
@@ -949,20 +1085,60 @@ __global__ void __launch_bounds__(kThreads, 1) k_fused(const __grid_constant__ P
                     const float rt = norm ? 1.0f / sqrtf(tot / static_cast<float>(kH) + kEps) : 1.0f;
                     __stcg(ws.logits + tid * kE + cta, z * rt + rbias);
                 }
-                // activation terms for the gate/up products (this warp's K-slice, token g)
-                float amax = 0.0f;
+                // Activation terms of the gate/up products, computed once per grid:
+                // unit (token t, 256-wide K-slice w) is split by warp w' of CTA
+                // G - 1 - u / 11 (u = 11 t + w, w' = u % 11), 8 values a lane, into
+                // kTerms E4M3 terms under a power-of-two scale per unit.
+                const int u = (G - 1 - cta) * kMW + warp;
+                if (u < M * kMW) {
+                    const int t = u / kMW, w = u % kMW;
+                    const int k0 = 256 * w + 8 * lane;
+                    float xv[8];
+                    if (from_x) {
+                        const uint4 a = *reinterpret_cast<const uint4 *>(p.x + (size_t)t * kH + k0);
+                        const uint32_t wd[4] = {a.x, a.y, a.z, a.w};
 #pragma unroll
-                for (int c = 0; c < 4; ++c)
-#pragma unroll
-                    for (int i = 0; i < 16; ++i) {
-                        v[c][i] *= r;
-                        amax = fmaxf(amax, fabsf(v[c][i]));
+                        for (int k = 0; k < 4; ++k) {
+                            const float2 f = bf16x2_to_f32(wd[k]);
+                            xv[2 * k] = f.x;
+                            xv[2 * k + 1] = f.y;
+                        }
+                    } else {
+                        const float4 a = ldcg4(ws.h + (size_t)t * kH + k0);
+                        const float4 b = ldcg4(ws.h + (size_t)t * kH + k0 + 4);
+                        xv[0] = a.x; xv[1] = a.y; xv[2] = a.z; xv[3] = a.w;
+                        xv[4] = b.x; xv[5] = b.y; xv[6] = b.z; xv[7] = b.w;
                     }
-                const float S = term_scale(quad_max(amax));
+                    float r = 1.0f;
+                    if (norm) {
+                        float tot = 0.0f;
 #pragma unroll
-                for (int c = 0; c < 4; ++c)
-                    split16_into(v[c], S, bx[c]);
-                column_inv(S, q, inv_x);
+                        for (int w2 = 0; w2 < kMW; ++w2)
+                            tot += s.part[w2][t];
+                        r = 1.0f / sqrtf(tot / static_cast<float>(kH) + kEps);
+                    }
+                    float amax = 0.0f;
+#pragma unroll
+                    for (int i = 0; i < 8; ++i) {
+                        xv[i] *= r;
+                        amax = fmaxf(amax, fabsf(xv[i]));
+                    }
+#pragma unroll
+                    for (int o = 16; o > 0; o >>= 1)
+                        amax = fmaxf(amax, __shfl_xor_sync(0xFFFFFFFFu, amax, o));
+                    const float S = term_scale(amax);
+                    uint32_t w0[kTerms], w1[kTerms];
+                    float y0[4] = {xv[0] * S, xv[1] * S, xv[2] * S, xv[3] * S};
+                    float y1[4] = {xv[4] * S, xv[5] * S, xv[6] * S, xv[7] * S};
+                    split_terms4(y0, w0);
+                    split_terms4(y1, w1);
+#pragma unroll
+                    for (int tt = 0; tt < kTerms; ++tt)
+                        __stcg(reinterpret_cast<uint2 *>(ws.xterms + ((size_t)t * kTerms + tt) * kH + k0),
+                               make_uint2(w0[tt], w1[tt]));
+                    if (lane == 0)
+                        __stcg(ws.xscale + t * kMW + w, S);
+                }
             }
         }
         stamp(3);
@@ -971,11 +1147,13 @@ __global__ void __launch_bounds__(kThreads, 1) k_fused(const __grid_constant__ P
         stamp(5);
         // -------------------------------------------------------- phase B
         {
+            float lv[4];
             if (warp < M) {
-                float lv[4];
 #pragma unroll
                 for (int k = 0; k < 4; ++k)
                     lv[k] = __ldcg(ws.logits + warp * kE + lane + 32 * k);
+            }
+            if (warp < M) {
                 // top-8 by repeated warp argmax (ties to the lower index)
                 bool bad = false;
 #pragma unroll
@@ -986,39 +1164,46 @@ __global__ void __launch_bounds__(kThreads, 1) k_fused(const __grid_constant__ P
                     }
                 if (__any_sync(0xFFFFFFFFu, bad) && lane == 0)
                     atomicOr(status, FGM_STATUS_NONFINITE_LOGITS);
-                unsigned taken = 0;
-                float top0 = 0.0f, my_v = 0.0f;
+                // top-8 (larger logit first, ties to the lower index): each round
+                // takes the largest remaining key with one redux.sync max, then the
+                // lowest index holding it. Keys order floats as unsigned integers;
+                // 0 marks a taken logit (-inf maps to 0x007FFFFF, still above it).
+                uint32_t key[4];
+#pragma unroll
+                for (int k = 0; k < 4; ++k) {
+                    const uint32_t b = __float_as_uint(lv[k]);
+                    key[k] = (b & 0x80000000u) ? ~b : (b | 0x80000000u);
+                }
+                uint32_t top_key = 0, my_key = 0;
                 int my_i = 0;
-#pragma unroll 1
+#pragma unroll
                 for (int rr = 0; rr < kK; ++rr) {
-                    float bv = -INFINITY;
-                    int bi = 0x7FFFFFFF;
+                    const uint32_t lk = max(max(key[0], key[1]), max(key[2], key[3]));
+                    const uint32_t gk = __reduce_max_sync(0xFFFFFFFFu, lk);
+                    unsigned bal[4];
 #pragma unroll
-                    for (int k = 0; k < 4; ++k) {
-                        const int idx = lane + 32 * k;
-                        if (!(taken & (1u << k)) && better(lv[k], idx, bv, bi)) {
-                            bv = lv[k];
-                            bi = idx;
-                        }
-                    }
+                    for (int k = 0; k < 4; ++k)
+                        bal[k] = __ballot_sync(0xFFFFFFFFu, key[k] == gk);
+                    const int kw = bal[0] ? 0 : bal[1] ? 1 : bal[2] ? 2 : 3;
+                    const unsigned bw = kw == 0 ? bal[0] : kw == 1 ? bal[1] : kw == 2 ? bal[2] : bal[3];
+                    const int lw = __ffs(bw) - 1;
+                    if (lane == lw) {
 #pragma unroll
-                    for (int o = 16; o > 0; o >>= 1) {
-                        const float ov = __shfl_xor_sync(0xFFFFFFFFu, bv, o);
-                        const int oi = __shfl_xor_sync(0xFFFFFFFFu, bi, o);
-                        if (better(ov, oi, bv, bi)) {
-                            bv = ov;
-                            bi = oi;
-                        }
+                        for (int k = 0; k < 4; ++k)
+                            if (k == kw)
+                                key[k] = 0u;
                     }
-                    if ((bi & 31) == lane)
-                        taken |= 1u << (bi >> 5);
                     if (rr == 0)
-                        top0 = bv;
+                        top_key = gk;
                     if (rr == lane) {
-                        my_v = bv;
-                        my_i = bi;
+                        my_key = gk;
+                        my_i = lw + 32 * kw;
                     }
                 }
+                const auto key_value = [](uint32_t kk) {
+                    return __uint_as_float((kk & 0x80000000u) ? (kk & 0x7FFFFFFFu) : ~kk);
+                };
+                const float top0 = key_value(top_key), my_v = key_value(my_key);
                 // lanes 0..7 hold the 8 picks; weights = exp(l - l_max) / sum
                 const float ex = lane < kK ? (top0 == -INFINITY ? 1.0f : expf(my_v - top0)) : 0.0f;
                 float z = ex;
@@ -1030,6 +1215,34 @@ __global__ void __launch_bounds__(kThreads, 1) k_fused(const __grid_constant__ P
                     s.tk_w[warp][lane] = ex / z;
                 }
             }
+            // gate/up B fragments of this warp's K-slice: column g of each block
+            // (packed (token, term) columns), loaded once the top-k is done: their
+            // L2 traffic would slow the top-k down
+            {
+#pragma unroll
+                for (int j = 0; j < NB; ++j) {
+                    int tok, term;
+                    column_of<NB>(j, g, tok, term);
+                    const bool ok = tok >= 0 && tok < M;
+                    const uint8_t *src = ws.xterms + ((size_t)(ok ? tok : 0) * kTerms + term) * kH + 256 * warp + 16 * q;
+#pragma unroll
+                    for (int c = 0; c < 4; ++c) {
+                        uint4 w4 = make_uint4(0u, 0u, 0u, 0u);
+                        if (ok)
+                            w4 = __ldcg(reinterpret_cast<const uint4 *>(src + 64 * c));
+                        bx[c][j][0] = w4.x;
+                        bx[c][j][1] = w4.y;
+                        bx[c][j][2] = w4.z;
+                        bx[c][j][3] = w4.w;
+                    }
+                }
+                // the scales of this lane's tokens; the weights are formed after the
+                // top-k, so that nothing waits for these loads before then
+                const int qb = NB == 2 ? 4 : q + 4;
+                fa_x[0] = q < M ? __ldcg(ws.xscale + q * kMW + warp) : 1.0f;
+                fb_x[0] = qb < M ? __ldcg(ws.xscale + qb * kMW + warp) : 1.0f;
+            }
+            stamp(10);
             for (int i = tid; i < kE; i += kConsumers)
                 s.mark[i] = 0;
             consumer_sync();
@@ -1056,6 +1269,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_fused(const __grid_constant__ P
             for (int i = tid; i < kMaxSlots * 8; i += kConsumers)
                 s.comb[pb][i >> 3][i & 7] = 0.0f;
             consumer_sync();
+            stamp(11);
             if (tid < M * kK) {
                 const int t = tid >> 3, rr = tid & 7;
                 s.comb[pb][s.slot_of[s.tk_ids[t][rr]]][t] = s.tk_w[t][rr];
@@ -1072,13 +1286,15 @@ __global__ void __launch_bounds__(kThreads, 1) k_fused(const __grid_constant__ P
             stamp(6);
             const int U = s.n_unique[pb];
             const Range rg = split((long long)U * kF, cta, G);
-            // row scales of this CTA's routed gate/up rows and of its down rows;
-            // their latency overlaps the producer's first routed copies
+            // row scales of this CTA's routed gate/up rows and of its down rows,
+            // copied asynchronously (cp.async); each thread waits for its copies
+            // before the first routed tile, and the next exchange barrier makes
+            // them visible to the reducers
             for (int k = tid; k < rg.end - rg.begin; k += kConsumers) {
                 const int pos = rg.begin + k;
                 const size_t row = (size_t)s.experts[pb][pos / kF] * kF + pos % kF;
-                s.sc_g[k] = __ldg(L.gate_s + row);
-                s.sc_u[k] = __ldg(L.up_s + row);
+                cp_async4(&s.sc_g[k], L.gate_s + row);
+                cp_async4(&s.sc_u[k], L.up_s + row);
             }
             {
                 const Range rd = split((long long)(U + 1) * kH, cta, G);
@@ -1086,10 +1302,15 @@ __global__ void __launch_bounds__(kThreads, 1) k_fused(const __grid_constant__ P
                     const int pos = rd.begin + k;
                     const int si = pos / kH;
                     const int e = si < U ? s.experts[pb][si] : kShared;
-                    s.sc_d[k] = __ldg(L.down_s + (size_t)e * kH + pos % kH);
+                    cp_async4(&s.sc_d[k], L.down_s + (size_t)e * kH + pos % kH);
                 }
             }
-            consumer_sync();
+            cp_async_commit();
+            bool scales_ready = false;
+            {
+                const float sa = fa_x[0], sb = fb_x[0];
+                column_weights<NB>(sa, sb, q, M, fa_x, fb_x);
+            }
             // the shared expert's rows of this CTA first (their copies were issued
             // before the routing was known), then its routed rows
             const int n_sh = (rsh.end - rsh.begin + 7) / 8;
@@ -1099,6 +1320,12 @@ __global__ void __launch_bounds__(kThreads, 1) k_fused(const __grid_constant__ P
             bool have_pend = false;
             for (int it = 0;; ++it) {
                 int aslot, i, nv, k0, cslot = -1;
+                if (it == 0)
+                    cp_async_wait_group1();   // the shared-expert scales (phase A's copies)
+                if (!scales_ready && it >= n_sh) {
+                    cp_async_wait_all();
+                    scales_ready = true;
+                }
                 if (it < n_sh) {
                     i = rsh.begin + 8 * it;
                     nv = min(8, rsh.end - i);
@@ -1132,6 +1359,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_fused(const __grid_constant__ P
                 }
             }
         }
+        cp_async_wait_all();   // (CTAs without routed gate/up rows: the down scales)
         stamp(7);
         grid_barrier();
         stamp(8);
@@ -1143,35 +1371,69 @@ __global__ void __launch_bounds__(kThreads, 1) k_fused(const __grid_constant__ P
             // their activation terms (this warp's 64-wide K-slice, token g) are
             // prepared once, up front.
             const int si0 = ds.begin / kH;
-            uint32_t bd[2][kTerms][4];
-            float inv_d[2][kTerms][2];
+            uint32_t bd[2][NB][4];   // packed activation columns per slot
+            float fa_d[2][3], fb_d[2][3];
 #pragma unroll
             for (int h2 = 0; h2 < 2; ++h2) {
                 const int si = si0 + h2;
-                float v[16];
-                if (g < M && si <= U && (h2 == 0 || ds.end > (si0 + 1) * kH)) {
-                    const int aslot = si < U ? si : kSharedSlot;
-                    const float *ar = ws.act + ((size_t)aslot * kMaxM + g) * kF + 64 * warp + 16 * q;
+                const bool slot_ok = si <= U && (h2 == 0 || ds.end > (si0 + 1) * kH);   // same for the whole CTA
+                if (slot_ok) {
+                    // token g's 16 values of this K-slice, split into terms (lanes 4g..4g+3)
+                    float v[16];
+                    if (g < M) {
+                        const int aslot = si < U ? si : kSharedSlot;
+                        const float *ar = ws.act + ((size_t)aslot * kMaxM + g) * kF + 64 * warp + 16 * q;
 #pragma unroll
-                    for (int k = 0; k < 4; ++k) {
-                        const float4 f = ldcg4(ar + 4 * k);
-                        v[4 * k] = f.x;
-                        v[4 * k + 1] = f.y;
-                        v[4 * k + 2] = f.z;
-                        v[4 * k + 3] = f.w;
+                        for (int k = 0; k < 4; ++k) {
+                            const float4 f = ldcg4(ar + 4 * k);
+                            v[4 * k] = f.x;
+                            v[4 * k + 1] = f.y;
+                            v[4 * k + 2] = f.z;
+                            v[4 * k + 3] = f.w;
+                        }
+                    } else {
+#pragma unroll
+                        for (int i = 0; i < 16; ++i)
+                            v[i] = 0.0f;
                     }
-                } else {
+                    float amax = 0.0f;
 #pragma unroll
                     for (int i = 0; i < 16; ++i)
-                        v[i] = 0.0f;
-                }
-                float amax = 0.0f;
+                        amax = fmaxf(amax, fabsf(v[i]));
+                    const float S = term_scale(quad_max(amax));
+                    uint32_t T[kTerms][4];
+                    split16_into(v, S, T);
+                    // packed column g of block j: its (token, term) words from lane 4 token + q
 #pragma unroll
-                for (int i = 0; i < 16; ++i)
-                    amax = fmaxf(amax, fabsf(v[i]));
-                const float S = term_scale(quad_max(amax));
-                split16_into(v, S, bd[h2]);
-                column_inv(S, q, inv_d[h2]);
+                    for (int j = 0; j < NB; ++j) {
+                        int tok, term;
+                        column_of<NB>(j, g, tok, term);
+                        const bool ok = tok >= 0 && tok < M;
+                        const int src = 4 * (tok >= 0 ? tok : 0) + q;
+#pragma unroll
+                        for (int k = 0; k < 4; ++k) {
+                            const uint32_t w0 = __shfl_sync(0xFFFFFFFFu, T[0][k], src);
+                            const uint32_t w1 = __shfl_sync(0xFFFFFFFFu, T[1][k], src);
+                            const uint32_t w2 = __shfl_sync(0xFFFFFFFFu, T[2][k], src);
+                            bd[h2][j][k] = ok ? (term == 0 ? w0 : term == 1 ? w1 : w2) : 0u;
+                        }
+                    }
+                    const int qb = NB == 2 ? 4 : q + 4;
+                    const float sa = __shfl_sync(0xFFFFFFFFu, S, 4 * q);
+                    const float sb = __shfl_sync(0xFFFFFFFFu, S, 4 * qb);
+                    column_weights<NB>(sa, sb, q, M, fa_d[h2], fb_d[h2]);
+                } else {
+#pragma unroll
+                    for (int j = 0; j < NB; ++j)
+#pragma unroll
+                        for (int k = 0; k < 4; ++k)
+                            bd[h2][j][k] = 0u;
+#pragma unroll
+                    for (int t = 0; t < 3; ++t) {
+                        fa_d[h2][t] = 0.0f;
+                        fb_d[h2][t] = 0.0f;
+                    }
+                }
             }
             int kk = ds.rot;   // visiting order without a division per stage
             for (int di = 0; di < ds.n; ++di) {
@@ -1180,30 +1442,32 @@ __global__ void __launch_bounds__(kThreads, 1) k_fused(const __grid_constant__ P
                 kk = kk + 1 == ds.n ? 0 : kk + 1;
                 const int si = pos / kH, j = pos % kH;
                 const int hs = si == si0 ? 0 : 1;
-                uint32_t bt[kTerms][4];
-                float it[kTerms][2];
+                uint32_t bt[NB][4];
+                float fa[3], fb[3];
 #pragma unroll
-                for (int tt = 0; tt < kTerms; ++tt) {
+                for (int jj = 0; jj < NB; ++jj)
 #pragma unroll
                     for (int k = 0; k < 4; ++k)
-                        bt[tt][k] = hs ? bd[1][tt][k] : bd[0][tt][k];
-                    it[tt][0] = hs ? inv_d[1][tt][0] : inv_d[0][tt][0];
-                    it[tt][1] = hs ? inv_d[1][tt][1] : inv_d[0][tt][1];
+                        bt[jj][k] = hs ? bd[1][jj][k] : bd[0][jj][k];
+#pragma unroll
+                for (int t = 0; t < 3; ++t) {
+                    fa[t] = hs ? fa_d[1][t] : fa_d[0][t];
+                    fb[t] = hs ? fb_d[1][t] : fb_d[0][t];
                 }
                 const bool got = stage_wait();
                 const uint8_t *slot = s.ring[stage % kStages];
 #pragma unroll
                 for (int t0 = 0; t0 < kDownTiles; t0 += 2) {
                     float po[2][4];
-                    // two tiles x 3 terms = 6 independent accumulator chains
-                    float acc[2][kTerms][4];
+                    // two tiles x NB packed blocks: 2 NB independent accumulator chains
+                    float acc[2][NB][4];
 #pragma unroll
                     for (int t = 0; t < 2; ++t)
 #pragma unroll
-                        for (int tt = 0; tt < kTerms; ++tt)
+                        for (int jj = 0; jj < NB; ++jj)
 #pragma unroll
                             for (int e2 = 0; e2 < 4; ++e2)
-                                acc[t][tt][e2] = 0.0f;
+                                acc[t][jj][e2] = 0.0f;
                     if (got) {
                         uint4 ra[2], rb[2];
 #pragma unroll
@@ -1214,24 +1478,22 @@ __global__ void __launch_bounds__(kThreads, 1) k_fused(const __grid_constant__ P
 #pragma unroll
                         for (int step = 0; step < 2; ++step)
 #pragma unroll
-                            for (int tt = 0; tt < kTerms; ++tt)
+                            for (int t = 0; t < 2; ++t) {
+                                const uint32_t a[4] = {step ? ra[t].z : ra[t].x, step ? rb[t].z : rb[t].x,
+                                                       step ? ra[t].w : ra[t].y, step ? rb[t].w : rb[t].y};
 #pragma unroll
-                                for (int t = 0; t < 2; ++t) {
-                                    const uint32_t a[4] = {step ? ra[t].z : ra[t].x, step ? rb[t].z : rb[t].x,
-                                                           step ? ra[t].w : ra[t].y, step ? rb[t].w : rb[t].y};
-                                    mma_e4m3(acc[t][tt], a, bt[tt][2 * step], bt[tt][2 * step + 1]);
-                                }
+                                for (int jj = 0; jj < NB; ++jj)
+                                    mma_e4m3(acc[t][jj], a, bt[jj][2 * step], bt[jj][2 * step + 1]);
+                            }
                     }
 #pragma unroll
-                    for (int t = 0; t < 2; ++t)
-#pragma unroll
-                        for (int e2 = 0; e2 < 4; ++e2) {
-                            float o = 0.0f;
-#pragma unroll
-                            for (int tt = 0; tt < kTerms; ++tt)
-                                o += acc[t][tt][e2] * it[tt][e2 & 1];
-                            po[t][e2] = o;
-                        }
+                    for (int t = 0; t < 2; ++t) {
+                        const float4 f = combine_terms<NB>(acc[t], fa, fb);
+                        po[t][0] = f.x;
+                        po[t][1] = f.y;
+                        po[t][2] = f.z;
+                        po[t][3] = f.w;
+                    }
                     if (t0 + 2 == kDownTiles) {
                         if (tid == 0)
                             dstamp(stage, layer_stage0, 2);

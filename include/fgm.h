@@ -205,16 +205,17 @@ long long fgm_set_wait_limit_ns(long long ns);
 
 /* Profiling aid: when buf (DEVICE, n int64 entries) is non-NULL, each later
  * persistent-kernel launch records %globaltimer stamps (ns). Per CTA at the
- * phase boundaries of layer l: entry [(l * 10 + k) * G + cta] with k = 0 layer
+ * phase boundaries of layer l: entry [(l * 12 + k) * G + cta] with k = 0 layer
  * start, 1 norm/router partials ready, 2 after their reduction, 3 activation
- * terms ready, 4 shared gate/up done, 5 after barrier 1, 6 routing known,
- * 7 routed gate/up done, 8 after barrier 2, 9 down done; then [(L*10) * G + cta]
- * after the last layer and [(L*10 + 1) * G + cta] at the end (G = CTAs, one
+ * terms ready, 4 shared gate/up done, 5 after barrier 1, 10 top-k done,
+ * 11 expert list done, 6 routing known, 7 routed gate/up done, 8 after
+ * barrier 2, 9 down done; then [(L*12) * G + cta] after the last layer and
+ * [(L*12 + 1) * G + cta] at the end (G = CTAs, one
  * per SM). Then, for CTA G/2 only, [L][48][8] SM clock64 values per ring stage
  * of each layer: producer issue, data landed (consumer wait over), products
  * done, slot released, last exchange of the stage posted, consumer wait
  * begun, unused, and (stage 0 only) the layer start. A buffer
- * shorter than (L*10 + 2) * G + L*48*8 entries disables recording. NULL stops. */
+ * shorter than (L*12 + 2) * G + L*48*8 entries disables recording. NULL stops. */
 int fgm_set_phase_trace(long long *buf, size_t n);
 
 /* Test hook for failure detection: the next persistent-kernel launch adds one
