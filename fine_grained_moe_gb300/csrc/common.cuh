@@ -42,7 +42,7 @@ struct Ws {
     int32_t *io_draft; // [8]
     int32_t *io_out;   // [2]
     int32_t *status;   // [1] FGM_STATUS_* bits
-    unsigned *sync;    // [64] grid-barrier counters
+    unsigned *sync;    // [128] [0] grid barrier, [1] exit count, [2 + s] completed activation rows of slot s
     uint8_t *xterms;   // [8][3][2816] E4M3 terms of the gate/up input of the current layer
     float *xscale;     // [8][11] their power-of-two scale per token and 256-wide K-slice
 };
@@ -81,7 +81,7 @@ inline WsOffsets ws_offsets()
     o.io_draft = take(sizeof(int32_t) * kMaxM);
     o.io_out = take(sizeof(int32_t) * 2);
     o.status = take(sizeof(int32_t) * 64);
-    o.sync = take(sizeof(unsigned) * 64);
+    o.sync = take(sizeof(unsigned) * 128);
     o.xterms = take(static_cast<size_t>(kMaxM) * 3 * kH);
     o.xscale = take(sizeof(float) * kMaxM * 11);
     o.total = p;

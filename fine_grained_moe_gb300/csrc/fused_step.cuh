@@ -94,7 +94,7 @@ struct Params {
 // for CTA G/2 only a per-stage timeline [l][kTraceStages][8] of SM clock64
 // values = {producer issue, data landed, products done, slot released, last
 // exchange posted, consumer wait begun, -, layer start}.
-constexpr int kTracePoints = 12;
+constexpr int kTracePoints = 13;
 constexpr int kTraceStages = 48;
 constexpr int kTraceDetail = 8;
 
@@ -118,6 +118,7 @@ struct __align__(128) Smem {
     unsigned long long full[kStages];
     unsigned long long empty[kStages];
     unsigned long long route;
+    unsigned slot_gen[kMaxSlots];   // layers so far (this one included) in which slot s was used
     int abort;
     int last;
 };
@@ -649,6 +650,8 @@ __global__ void __launch_bounds__(kThreads, 1) k_fused(const __grid_constant__ P
         }
         mbar_init(&s.route, 1);
         s.abort = 0;
+        for (int i = 0; i < kMaxSlots; ++i)
+            s.slot_gen[i] = 0;
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     }
     __syncthreads();
@@ -1286,6 +1289,8 @@ __global__ void __launch_bounds__(kThreads, 1) k_fused(const __grid_constant__ P
             stamp(6);
             const int U = s.n_unique[pb];
             const Range rg = split((long long)U * kF, cta, G);
+            if (tid < U || tid == kSharedSlot)
+                ++s.slot_gen[tid];   // read in phase C, after the next barrier
             // row scales of this CTA's routed gate/up rows and of its down rows,
             // copied asynchronously (cp.async); each thread waits for its copies
             // before the first routed tile, and the next exchange barrier makes
@@ -1361,7 +1366,58 @@ __global__ void __launch_bounds__(kThreads, 1) k_fused(const __grid_constant__ P
         }
         cp_async_wait_all();   // (CTAs without routed gate/up rows: the down scales)
         stamp(7);
-        grid_barrier();
+        // Phase C reads only the activation rows of this CTA's (at most two)
+        // slots: each CTA publishes the rows it finished per slot (one release
+        // after its gate/up work), and waits for the row counters of the slots
+        // it reads (704 rows per use of the slot) instead of a grid barrier.
+        consumer_sync();
+        if (tid == 0) {
+            const int U = s.n_unique[pb];
+            const Range rg = split((long long)U * kF, cta, G);
+            __threadfence();
+            if (rsh.end > rsh.begin)
+                asm volatile("red.relaxed.gpu.global.add.u32 [%0], %1;" ::"l"(ws.sync + 2 + kSharedSlot),
+                             "r"(rsh.end - rsh.begin)
+                             : "memory");
+            if (rg.end > rg.begin) {
+                for (int u = rg.begin / kF; u <= (rg.end - 1) / kF; ++u) {
+                    const int rows = min(rg.end, (u + 1) * kF) - max(rg.begin, u * kF);
+                    asm volatile("red.relaxed.gpu.global.add.u32 [%0], %1;" ::"l"(ws.sync + 2 + u), "r"(rows)
+                                 : "memory");
+                }
+            }
+        }
+        stamp(12);
+        if (tid == 0 && !*reinterpret_cast<volatile int *>(&s.abort)) {
+            const int U = s.n_unique[pb];
+            const Range rd = split((long long)(U + 1) * kH, cta, G);
+            if (rd.end > rd.begin) {
+                for (int si = rd.begin / kH; si <= (rd.end - 1) / kH; ++si) {
+                    const int cs = si < U ? si : kSharedSlot;
+                    const unsigned target = static_cast<unsigned>(kF) * s.slot_gen[cs];
+                    const unsigned *cnt = ws.sync + 2 + cs;
+                    bool done = false;
+                    for (int it = 0; !done; ++it) {
+                        unsigned v;
+                        asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(cnt) : "memory");
+                        done = v >= target;
+                        if (!done && (it & 63) == 63 && gtime() > deadline) {
+                            s.abort = 1;
+                            if (atomicOr(status, FGM_STATUS_WAIT_TIMEOUT) == 0) {
+                                status[1] = 7;
+                                status[2] = cta;
+                                status[3] = (int)v;
+                                status[4] = (int)target;
+                            }
+                            break;
+                        }
+                    }
+                    if (!done)
+                        break;
+                }
+            }
+        }
+        consumer_sync();
         stamp(8);
         // -------------------------------------------------------- phase C
         {
@@ -1679,6 +1735,8 @@ __global__ void __launch_bounds__(kThreads, 1) k_fused(const __grid_constant__ P
             p.out[1] = arg[a];
         }
     }
+    if (tid < kMaxSlots)
+        bar_ctr[2 + tid] = 0;
     if (tid == 0) {
         bar_ctr[1] = 0;
         atomicExch(bar_ctr, 0u);
