@@ -56,7 +56,7 @@ constexpr int kDownTiles = 4;                 // 16-row down tiles per ring slot
 constexpr int kTerms = 3;                     // E4M3 terms per activation
 constexpr int kSharedSlot = kMaxSlots - 1;
 constexpr int kMinCtas = 128;                 // the persistent kernel needs at least this many SMs
-constexpr int kMaxGuRows = (kMaxSlots - 1) * kF / kMinCtas + 2;   // routed row pairs per CTA
+constexpr int kMaxGuRows = 8 * ((kMaxSlots * (kF / 8) + kMinCtas - 1) / kMinCtas);   // routed row pairs per CTA
 constexpr int kMaxDownRows = kMaxSlots * kH / kMinCtas + 2;       // down rows per CTA
 
 enum Mode { kModeLayer = 0, kModeStack = 1, kModeVerify = 2, kModeLmHead = 3 };
@@ -348,6 +348,24 @@ struct Range {
 __device__ __forceinline__ Range split(long long total, int part, int parts)
 {
     return Range{static_cast<int>(total * part / parts), static_cast<int>(total * (part + 1) / parts)};
+}
+
+// Gate/up rows of one CTA, in whole 8-row tiles (no stage is partly empty):
+// CTA c < 88 owns shared-expert tile c; the U * 88 routed tiles are dealt so
+// that every CTA's total (shared + routed) is floor or ceil of (U + 1) * 88 / G.
+__device__ __forceinline__ Range gu_shared_rows(int cta)
+{
+    constexpr int kTiles = kF / 8;
+    return cta < kTiles ? Range{8 * cta, 8 * cta + 8} : Range{kF, kF};
+}
+
+__device__ __forceinline__ Range gu_routed_rows(int U, int cta, int G)
+{
+    constexpr int kTiles = kF / 8;
+    const long long total = (long long)(U + 1) * kTiles;
+    const int b = static_cast<int>(total * cta / G) - min(cta, kTiles);
+    const int e = static_cast<int>(total * (cta + 1) / G) - min(cta + 1, kTiles);
+    return Range{8 * b, 8 * e};
 }
 
 // Down-phase stages of one CTA: the CTA's row range of the (slot, row) space
@@ -699,7 +717,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_fused(const __grid_constant__ P
                 __device__ LayerPlan(int U_, int cta_, int G_)
                     : U(U_), gb(0), ge(0), gpos(0), di(0), ds(U_, cta_, G_)
                 {
-                    const Range rb = split((long long)U_ * kF, cta_, G_);
+                    const Range rb = gu_routed_rows(U_, cta_, G_);
                     gb = rb.begin;
                     ge = rb.end;
                     gpos = gb;
@@ -739,7 +757,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_fused(const __grid_constant__ P
                 if (l > 0 && cta == kE - 1 && L.router_b)
                     prefetch_l2(L.router_b, kE * sizeof(float));
                 // phase A: shared expert gate/up rows
-                const Range ra = split(kF, cta, G);
+                const Range ra = gu_shared_rows(cta);
                 for (int i = ra.begin; i < ra.end && ok; i += 8)
                     gu_rows(L, kShared, i, min(8, ra.end - i));
                 if (!ok)
@@ -1000,7 +1018,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_fused(const __grid_constant__ P
         if (l == 0 && p.debug_stall)
             grid_barrier();
         // -------------------------------------------------------- phase A
-        const Range rsh = split(kF, cta, G);
+        const Range rsh = gu_shared_rows(cta);
         {
             const bool from_x = (p.mode == kModeLayer) || l == 0;
             const bool norm = p.mode != kModeLayer;
@@ -1288,7 +1306,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_fused(const __grid_constant__ P
                 mbar_arrive(&s.route);
             stamp(6);
             const int U = s.n_unique[pb];
-            const Range rg = split((long long)U * kF, cta, G);
+            const Range rg = gu_routed_rows(U, cta, G);
             if (tid < U || tid == kSharedSlot)
                 ++s.slot_gen[tid];   // read in phase C, after the next barrier
             // row scales of this CTA's routed gate/up rows and of its down rows,
@@ -1373,7 +1391,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_fused(const __grid_constant__ P
         consumer_sync();
         if (tid == 0) {
             const int U = s.n_unique[pb];
-            const Range rg = split((long long)U * kF, cta, G);
+            const Range rg = gu_routed_rows(U, cta, G);
             __threadfence();
             if (rsh.end > rsh.begin)
                 asm volatile("red.relaxed.gpu.global.add.u32 [%0], %1;" ::"l"(ws.sync + 2 + kSharedSlot),
