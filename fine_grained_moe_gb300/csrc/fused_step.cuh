@@ -1532,6 +1532,9 @@ __global__ void __launch_bounds__(kThreads, 1) k_fused(const __grid_constant__ P
                 const uint8_t *slot = s.ring[stage % kStages];
 #pragma unroll
                 for (int t0 = 0; t0 < kDownTiles; t0 += 2) {
+                    // a stage's rows beyond nv are skipped half by half (same for the
+                    // whole CTA): a partial stage costs about its rows
+                    const bool half_used = 16 * t0 < nv;
                     float po[2][4];
                     // two tiles x NB packed blocks: 2 NB independent accumulator chains
                     float acc[2][NB][4];
@@ -1542,7 +1545,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_fused(const __grid_constant__ P
 #pragma unroll
                             for (int e2 = 0; e2 < 4; ++e2)
                                 acc[t][jj][e2] = 0.0f;
-                    if (got) {
+                    if (got && half_used) {
                         uint4 ra[2], rb[2];
 #pragma unroll
                         for (int t = 0; t < 2; ++t) {
@@ -1574,8 +1577,10 @@ __global__ void __launch_bounds__(kThreads, 1) k_fused(const __grid_constant__ P
                         stage_release();
                     }
                     // tiles t0, t0 + 1 (rows beyond the stage's nv rows are skipped)
-                    const int4 md = make_int4(kTileDown, j, pos - ds.begin, nv);
-                    post(KindTag<kTileDown>{}, md, md, po, 2, t0, t0 + 2 == kDownTiles);
+                    if (half_used) {
+                        const int4 md = make_int4(kTileDown, j, pos - ds.begin, nv);
+                        post(KindTag<kTileDown>{}, md, md, po, 16 * (t0 + 1) < nv ? 2 : 1, t0, t0 + 2 == kDownTiles);
+                    }
                 }
             }
         }
