@@ -163,8 +163,8 @@ def cpu_oracle_step(layers, emb, x, draft_seed, log_prefix="[oracle]"):
 # ---------------------------------------------------------------- phase trace
 TRACE_POINTS = ("layer start", "norm/router partials", "partials reduced", "activation terms",
                 "shared gate/up done", "barrier 1 passed", "routing known", "routed gate/up done",
-                "barrier 2 passed", "down done", "top-k done", "expert list done", "rows published")
-TRACE_ORDER = (1, 2, 3, 4, 5, 10, 11, 6, 7, 12, 8, 9)   # the points in the order a layer reaches them
+                "barrier 2 passed", "down done", "top-k done", "expert list done")
+TRACE_ORDER = (1, 2, 3, 4, 5, 10, 11, 6, 7, 8, 9)   # the points in the order a layer reaches them
 NTP = len(TRACE_POINTS)
 TRACE_STAGES = 48
 

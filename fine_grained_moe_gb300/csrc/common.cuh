@@ -31,7 +31,8 @@ struct Ws {
     float *logits;     // [8][128] router logits (bias included)
     int32_t *meta;     // [0] = distinct routed experts U, [1 + s] = expert of slot s (slot U: shared)
     float *comb;       // [65][8] routing weight of slot s for token t (0 when not routed)
-    float *act;        // [65][8][704] weighted gated activations per slot and token
+    float *act;        // [2][65][8][704] weighted gated activations per slot and token (the staged
+                       // path uses buffer 0; the persistent kernel alternates by layer)
     int32_t *ids;      // [8][8] chosen experts of the last routed layer
     float *wts;        // [8][8] their weights
     float *part_val;   // [kMaxParts][8] lm_head per-CTA best logit
@@ -70,7 +71,7 @@ inline WsOffsets ws_offsets()
     o.logits = take(sizeof(float) * kMaxM * kE);
     o.meta = take(sizeof(int32_t) * (kMaxSlots + 8));
     o.comb = take(sizeof(float) * kMaxSlots * kMaxM);
-    o.act = take(sizeof(float) * kMaxSlots * kMaxM * kF);
+    o.act = take(sizeof(float) * 2 * kMaxSlots * kMaxM * kF);
     o.ids = take(sizeof(int32_t) * kMaxM * kK);
     o.wts = take(sizeof(float) * kMaxM * kK);
     o.part_val = take(sizeof(float) * kMaxParts * kMaxM);

@@ -554,7 +554,7 @@ int fgm_read_status(void *ws, size_t ws_bytes, int clear, int32_t *status, void 
 
 namespace {
 
-constexpr size_t kNoAllocScratchBytes = size_t(2) << 20;  // >= fgm_workspace_bytes(8, 0)
+constexpr size_t kNoAllocScratchBytes = size_t(4) << 20;  // >= fgm_workspace_bytes(8, 0)
 
 }  // namespace
 

@@ -55,6 +55,7 @@ constexpr int kSlotBytes = 16 * kRowStride;   // 46080
 constexpr int kDownTiles = 4;                 // 16-row down tiles per ring slot (64 x 704 bytes)
 constexpr int kTerms = 3;                     // E4M3 terms per activation
 constexpr int kSharedSlot = kMaxSlots - 1;
+constexpr uint32_t kActPending = 0x7FC0DEADu;   // NaN marker: activation row not written yet
 constexpr int kMinCtas = 128;                 // the persistent kernel needs at least this many SMs
 constexpr int kMaxGuRows = 8 * ((kMaxSlots * (kF / 8) + kMinCtas - 1) / kMinCtas);   // routed row pairs per CTA
 constexpr int kMaxDownRows = kMaxSlots * kH / kMinCtas + 2;       // down rows per CTA
@@ -94,7 +95,7 @@ struct Params {
 // for CTA G/2 only a per-stage timeline [l][kTraceStages][8] of SM clock64
 // values = {producer issue, data landed, products done, slot released, last
 // exchange posted, consumer wait begun, -, layer start}.
-constexpr int kTracePoints = 13;
+constexpr int kTracePoints = 12;
 constexpr int kTraceStages = 48;
 constexpr int kTraceDetail = 8;
 
@@ -118,7 +119,6 @@ struct __align__(128) Smem {
     unsigned long long full[kStages];
     unsigned long long empty[kStages];
     unsigned long long route;
-    unsigned slot_gen[kMaxSlots];   // layers so far (this one included) in which slot s was used
     int abort;
     int last;
 };
@@ -668,8 +668,6 @@ __global__ void __launch_bounds__(kThreads, 1) k_fused(const __grid_constant__ P
         }
         mbar_init(&s.route, 1);
         s.abort = 0;
-        for (int i = 0; i < kMaxSlots; ++i)
-            s.slot_gen[i] = 0;
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     }
     __syncthreads();
@@ -875,6 +873,24 @@ __global__ void __launch_bounds__(kThreads, 1) k_fused(const __grid_constant__ P
     uint32_t bx[4][NB][4];   // packed activation columns of this warp's K-slice (gate/up)
     float fa_x[3], fb_x[3];  // their term weights
     int cur_pb = 0;               // routing buffer of the current layer
+    float *act_cur = ws.act;      // activation buffer of the current layer (alternates)
+    // Activation buffers carry a pending marker until their rows are written
+    // (the down rows poll for it). mark_pending(buf, n_used) marks buffer buf
+    // for tokens < M: every slot if n_used == 0, else the first n_used slots and
+    // the shared one. The caller guarantees that no reader of the buffer's
+    // previous contents is left and that its next writers come after a grid
+    // barrier.
+    auto mark_pending = [&](int buf, int n_used) {
+        const float4 pend4 = make_float4(__uint_as_float(kActPending), __uint_as_float(kActPending),
+                                         __uint_as_float(kActPending), __uint_as_float(kActPending));
+        const int rows = (n_used == 0 ? kMaxSlots : n_used + 1) * M;
+        float *base = ws.act + (size_t)buf * kMaxSlots * kMaxM * kF;
+        for (int i = cta * kConsumers + tid; i < rows * (kF / 4); i += G * kConsumers) {
+            const int r = i / (kF / 4), c4 = i % (kF / 4);
+            const int slot = n_used == 0 ? r / M : (r / M < n_used ? r / M : kSharedSlot);
+            __stcg(reinterpret_cast<float4 *>(base + ((size_t)slot * kMaxM + r % M) * kF) + c4, pend4);
+        }
+    };
     // lm_head: lanes 0..3 keep the running best of tokens 2 lane, 2 lane + 1
     // over the tiles this warp reduces
     float best_v[2] = {-INFINITY, -INFINITY};
@@ -896,7 +912,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_fused(const __grid_constant__ P
                 const float sg = s.sc_g[k0 + r0], su = s.sc_u[k0 + r0];
                 const float ca = m.w >= 0 ? s.comb[cur_pb][m.w][qa] : 1.0f;
                 const float cb = m.w >= 0 ? s.comb[cur_pb][m.w][qb] : 1.0f;
-                float *base = ws.act + (size_t)aslot * kMaxM * kF + i + r0;
+                float *base = act_cur + (size_t)aslot * kMaxM * kF + i + r0;
                 gu_epilogue(base + qa * kF, base + qb * kF, f, sg, su, ca, cb, qa < M,
                             qb < M && (NB == 3 || qa == 0));
             }
@@ -1009,6 +1025,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_fused(const __grid_constant__ P
         };
         cur_layer = l;
         cur_pb = pb;
+        act_cur = ws.act + (size_t)(l & 1) * kMaxSlots * kMaxM * kF;
         layer_stage0 = stage;
         if (detail && tid == 0)
             detail[((size_t)l * kTraceStages) * kTraceDetail + 7] = clock64();
@@ -1162,6 +1179,8 @@ __global__ void __launch_bounds__(kThreads, 1) k_fused(const __grid_constant__ P
                 }
             }
         }
+        if (l == 0)
+            mark_pending(0, 0);   // this layer's buffer (the next one is marked after its down rows)
         stamp(3);
         stamp(4);
         grid_barrier();
@@ -1307,8 +1326,6 @@ __global__ void __launch_bounds__(kThreads, 1) k_fused(const __grid_constant__ P
             stamp(6);
             const int U = s.n_unique[pb];
             const Range rg = gu_routed_rows(U, cta, G);
-            if (tid < U || tid == kSharedSlot)
-                ++s.slot_gen[tid];   // read in phase C, after the next barrier
             // row scales of this CTA's routed gate/up rows and of its down rows,
             // copied asynchronously (cp.async); each thread waits for its copies
             // before the first routed tile, and the next exchange barrier makes
@@ -1384,57 +1401,8 @@ __global__ void __launch_bounds__(kThreads, 1) k_fused(const __grid_constant__ P
         }
         cp_async_wait_all();   // (CTAs without routed gate/up rows: the down scales)
         stamp(7);
-        // Phase C reads only the activation rows of this CTA's (at most two)
-        // slots: each CTA publishes the rows it finished per slot (one release
-        // after its gate/up work), and waits for the row counters of the slots
-        // it reads (704 rows per use of the slot) instead of a grid barrier.
-        consumer_sync();
-        if (tid == 0) {
-            const int U = s.n_unique[pb];
-            const Range rg = gu_routed_rows(U, cta, G);
-            __threadfence();
-            if (rsh.end > rsh.begin)
-                asm volatile("red.relaxed.gpu.global.add.u32 [%0], %1;" ::"l"(ws.sync + 2 + kSharedSlot),
-                             "r"(rsh.end - rsh.begin)
-                             : "memory");
-            if (rg.end > rg.begin) {
-                for (int u = rg.begin / kF; u <= (rg.end - 1) / kF; ++u) {
-                    const int rows = min(rg.end, (u + 1) * kF) - max(rg.begin, u * kF);
-                    asm volatile("red.relaxed.gpu.global.add.u32 [%0], %1;" ::"l"(ws.sync + 2 + u), "r"(rows)
-                                 : "memory");
-                }
-            }
-        }
-        stamp(12);
-        if (tid == 0 && !*reinterpret_cast<volatile int *>(&s.abort)) {
-            const int U = s.n_unique[pb];
-            const Range rd = split((long long)(U + 1) * kH, cta, G);
-            if (rd.end > rd.begin) {
-                for (int si = rd.begin / kH; si <= (rd.end - 1) / kH; ++si) {
-                    const int cs = si < U ? si : kSharedSlot;
-                    const unsigned target = static_cast<unsigned>(kF) * s.slot_gen[cs];
-                    const unsigned *cnt = ws.sync + 2 + cs;
-                    bool done = false;
-                    for (int it = 0; !done; ++it) {
-                        unsigned v;
-                        asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(cnt) : "memory");
-                        done = v >= target;
-                        if (!done && (it & 63) == 63 && gtime() > deadline) {
-                            s.abort = 1;
-                            if (atomicOr(status, FGM_STATUS_WAIT_TIMEOUT) == 0) {
-                                status[1] = 7;
-                                status[2] = cta;
-                                status[3] = (int)v;
-                                status[4] = (int)target;
-                            }
-                            break;
-                        }
-                    }
-                    if (!done)
-                        break;
-                }
-            }
-        }
+        // Phase C polls the activation rows it reads until the pending marker
+        // is gone (no fence or counter between the phases).
         consumer_sync();
         stamp(8);
         // -------------------------------------------------------- phase C
@@ -1456,14 +1424,38 @@ __global__ void __launch_bounds__(kThreads, 1) k_fused(const __grid_constant__ P
                     float v[16];
                     if (g < M) {
                         const int aslot = si < U ? si : kSharedSlot;
-                        const float *ar = ws.act + ((size_t)aslot * kMaxM + g) * kF + 64 * warp + 16 * q;
+                        const float *ar = act_cur + ((size_t)aslot * kMaxM + g) * kF + 64 * warp + 16 * q;
+                        // written by the gate/up epilogues of other CTAs: poll until no
+                        // value carries the pending marker (bounded by the deadline)
+                        for (int it = 0;; ++it) {
+                            bool ready = true;
 #pragma unroll
-                        for (int k = 0; k < 4; ++k) {
-                            const float4 f = ldcg4(ar + 4 * k);
-                            v[4 * k] = f.x;
-                            v[4 * k + 1] = f.y;
-                            v[4 * k + 2] = f.z;
-                            v[4 * k + 3] = f.w;
+                            for (int k = 0; k < 4; ++k) {
+                                const float4 f = ldcg4(ar + 4 * k);
+                                v[4 * k] = f.x;
+                                v[4 * k + 1] = f.y;
+                                v[4 * k + 2] = f.z;
+                                v[4 * k + 3] = f.w;
+                            }
+#pragma unroll
+                            for (int i = 0; i < 16; ++i)
+                                ready = ready && __float_as_uint(v[i]) != kActPending;
+                            if (ready)
+                                break;
+                            if ((it & 15) == 15 &&
+                                (*reinterpret_cast<volatile int *>(&s.abort) || gtime() > deadline)) {
+                                *reinterpret_cast<volatile int *>(&s.abort) = 1;
+                                if (atomicOr(status, FGM_STATUS_WAIT_TIMEOUT) == 0) {
+                                    status[1] = 7;
+                                    status[2] = cta;
+                                    status[3] = warp;
+                                    status[4] = aslot;
+                                }
+#pragma unroll
+                                for (int i = 0; i < 16; ++i)
+                                    v[i] = 0.0f;
+                                break;
+                            }
                         }
                     } else {
 #pragma unroll
@@ -1584,6 +1576,11 @@ __global__ void __launch_bounds__(kThreads, 1) k_fused(const __grid_constant__ P
                 }
             }
         }
+        // The next layer writes the other buffer: mark the slots it held two
+        // layers ago (all of them after layer 0). Its last readers were the down
+        // rows of layer l - 1, all done before this layer began.
+        if (l + 1 < n_layers)
+            mark_pending((l + 1) & 1, l == 0 ? 0 : s.n_unique[(l - 1) & 1]);
         stamp(9);
         grid_barrier();
     }
@@ -1758,8 +1755,6 @@ __global__ void __launch_bounds__(kThreads, 1) k_fused(const __grid_constant__ P
             p.out[1] = arg[a];
         }
     }
-    if (tid < kMaxSlots)
-        bar_ctr[2 + tid] = 0;
     if (tid == 0) {
         bar_ctr[1] = 0;
         atomicExch(bar_ctr, 0u);

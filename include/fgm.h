@@ -122,7 +122,7 @@ int fgm_moe_layer_fwd(const fgm_layer *layer, const uint16_t *x, uint16_t *y, in
  * synchronisation. The operation is the same as fgm_moe_layer_fwd (same
  * arguments, same results); the pages describe no such variant, it is an
  * interface convenience only.
- *  - Scratch: a fixed device array inside the library (2 MiB, enough for
+ *  - Scratch: a fixed device array inside the library (4 MiB, enough for
  *    M <= FGM_MAX_M = 8 tokens), reserved when the library's CUDA module is
  *    loaded. The call allocates nothing; M outside [1, 8] returns
  *    FGM_ERR_INVALID_ARG with a message naming the limit.
@@ -205,18 +205,17 @@ long long fgm_set_wait_limit_ns(long long ns);
 
 /* Profiling aid: when buf (DEVICE, n int64 entries) is non-NULL, each later
  * persistent-kernel launch records %globaltimer stamps (ns). Per CTA at the
- * phase boundaries of layer l: entry [(l * 13 + k) * G + cta] with k = 0 layer
+ * phase boundaries of layer l: entry [(l * 12 + k) * G + cta] with k = 0 layer
  * start, 1 norm/router partials ready, 2 after their reduction, 3 activation
  * terms ready, 4 shared gate/up done, 5 after barrier 1, 10 top-k done,
- * 11 expert list done, 6 routing known, 7 routed gate/up done, 12 finished
- * rows published, 8 the activation rows this CTA reads complete, 9 down done;
- * then [(L*13) * G + cta] after the last layer and [(L*13 + 1) * G + cta] at
- * the end (G = CTAs, one
+ * 11 expert list done, 6 routing known, 7 routed gate/up done, 8 start of
+ * the down rows, 9 down done; then [(L*12) * G + cta] after the last layer
+ * and [(L*12 + 1) * G + cta] at the end (G = CTAs, one
  * per SM). Then, for CTA G/2 only, [L][48][8] SM clock64 values per ring stage
  * of each layer: producer issue, data landed (consumer wait over), products
  * done, slot released, last exchange of the stage posted, consumer wait
  * begun, unused, and (stage 0 only) the layer start. A buffer
- * shorter than (L*13 + 2) * G + L*48*8 entries disables recording. NULL stops. */
+ * shorter than (L*12 + 2) * G + L*48*8 entries disables recording. NULL stops. */
 int fgm_set_phase_trace(long long *buf, size_t n);
 
 /* Test hook for failure detection: the next persistent-kernel launch adds one
@@ -231,8 +230,8 @@ int fgm_read_status(void *ws, size_t ws_bytes, int clear, int32_t *status, void 
 /* After FGM_STATUS_WAIT_TIMEOUT: where the first wait gave up, as 4 int32
  * (HOST report): {site, block, warp, index}; site 1 = ring slot free
  * (producer), 2 = routing known (producer), 3 = ring data landed, 6 = grid
- * barrier, 7 = activation rows of an expert complete (for 6 and 7: warp =
- * counter value, index = target). Synchronises the stream. */
+ * barrier (warp = counter value, index = target), 7 = activation rows of an
+ * expert written (index = its slot). Synchronises the stream. */
 int fgm_read_wait_report(void *ws, size_t ws_bytes, int32_t *report, void *stream);
 
 /* Message describing the last error returned on the calling thread. */
