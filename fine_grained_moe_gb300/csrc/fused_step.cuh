@@ -58,7 +58,7 @@ constexpr int kSharedSlot = kMaxSlots - 1;
 constexpr uint32_t kActPending = 0x7FC0DEADu;   // NaN marker: activation row not written yet
 constexpr int kMinCtas = 128;                 // the persistent kernel needs at least this many SMs
 constexpr int kMaxGuRows = 8 * ((kMaxSlots * (kF / 8) + kMinCtas - 1) / kMinCtas);   // routed row pairs per CTA
-constexpr int kMaxDownRows = kMaxSlots * kH / kMinCtas + 2;       // down rows per CTA
+constexpr int kMaxDownRows = 16 * (kMaxSlots * (kH / 16) / kMinCtas + 5);   // down rows per CTA (see down_rows)
 
 enum Mode { kModeLayer = 0, kModeStack = 1, kModeVerify = 2, kModeLmHead = 3 };
 enum TileKind { kTileGateUp = 0, kTileDown = 1, kTileLmHead = 2 };
@@ -372,12 +372,28 @@ __device__ __forceinline__ Range gu_routed_rows(int U, int cta, int G)
 // cut at every 64-row boundary of a slot. CTAs visit their stages in a
 // rotated order so that CTAs working on different experts add into different
 // rows of the residual at any moment.
+// Down rows of one CTA, in 16-row tiles, dealt so that gate/up and down work
+// together are even: a gate/up tile (8 row pairs of 2816 bytes) counts as 3
+// down tiles (16 rows of 704 bytes; measured stage times are about 1 : 0.3),
+// and a CTA with one more gate/up tile than another gets about 3 fewer down
+// tiles. Cumulative over CTAs: 16 (units(c) - 3 * gate/up tiles before c).
+__device__ __forceinline__ Range down_rows(int U, int cta, int G)
+{
+    constexpr int kGuTiles = kF / 8;
+    constexpr int kW = 3;
+    const long long units = (long long)(U + 1) * (kW * kGuTiles + kH / 16);
+    const long long gtiles = (long long)(U + 1) * kGuTiles;
+    const int b = static_cast<int>(units * cta / G - kW * (gtiles * cta / G));
+    const int e = static_cast<int>(units * (cta + 1) / G - kW * (gtiles * (cta + 1) / G));
+    return Range{16 * b, 16 * e};
+}
+
 struct DownStages {
     int begin, end;   // CTA range in the flattened (slot, row) space
     int k0, n, rot;   // first 64-row block, number of blocks, rotation
     __device__ DownStages(int U, int cta, int G)
     {
-        const Range r = split((long long)(U + 1) * kH, cta, G);
+        const Range r = down_rows(U, cta, G);
         begin = r.begin;
         end = r.end;
         constexpr int kBlk = kDownTiles * 16;   // 64 rows
@@ -1337,7 +1353,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_fused(const __grid_constant__ P
                 cp_async4(&s.sc_u[k], L.up_s + row);
             }
             {
-                const Range rd = split((long long)(U + 1) * kH, cta, G);
+                const Range rd = down_rows(U, cta, G);
                 for (int k = tid; k < rd.end - rd.begin; k += kConsumers) {
                     const int pos = rd.begin + k;
                     const int si = pos / kH;
