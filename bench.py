@@ -204,6 +204,18 @@ def write_phase_trace(path, fgm, layers, emb, x, draft, ws, arr, dev):
     lines.append("point                      last CTA (us)   median CTA (us)   from layer start")
     for k in TRACE_ORDER:
         lines.append(f"{TRACE_POINTS[k]:26s} {last[k]:12.2f} {med[k]:16.2f}")
+    # per-CTA mean over layers of "down done" (from each layer's first start): stragglers
+    dd = torch.zeros(G, dtype=torch.float64)
+    gd = torch.zeros(G, dtype=torch.float64)
+    for l in range(N_LAYERS):
+        base = tr[l * NTP].min()
+        dd += (tr[l * NTP + 9] - base) / 1e3 / N_LAYERS
+        gd += (tr[l * NTP + 7] - base) / 1e3 / N_LAYERS
+    order = torch.argsort(dd, descending=True)
+    lines.append("slowest CTAs (mean down done / routed gate/up done, us): " + ", ".join(
+        f"{int(c)}: {float(dd[c]):.2f}/{float(gd[c]):.2f}" for c in order[:8]))
+    lines.append(f"down done p10/p50/p90: {float(dd.quantile(0.1)):.2f} / {float(dd.quantile(0.5)):.2f} / "
+                 f"{float(dd.quantile(0.9)):.2f} us")
     tail = tr[N_LAYERS * NTP + 1].max() - tr[N_LAYERS * NTP].min()
     lines.append(f"lm_head + accept (last CTA end - first CTA after layers): {float(tail) / 1e3:.2f} us")
     for l in (1, N_LAYERS // 2):
