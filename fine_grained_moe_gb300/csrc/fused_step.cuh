@@ -1,37 +1,40 @@
 // Persistent verify-step kernel: one cooperative launch runs every layer of
 // the MoE stack (and, for the verify step, the lm_head argmax and greedy
-// accept) with grid-wide barriers between the phases of a layer.
+// accept).
 //
 // CTA layout: one CTA per SM; 11 MMA warps and 1 producer warp.
-//  * The producer warp streams weight rows from HBM into a 3-slot shared
+//  * The producer warp streams weight rows from HBM into a 4-slot shared
 //    memory ring with cp.async.bulk (TMA bulk copies) completing on mbarriers.
 //    Weight loads never depend on activations, so the producer runs ahead of
-//    the consumers across grid barriers; it only waits for the routing of a
-//    layer before fetching that layer's routed experts.
+//    the consumers across phase boundaries; it only waits for the routing of
+//    a layer before fetching that layer's routed experts.
 //  * MMA warps split K: warp w owns a fixed 256-byte (gate/up, lm_head) or
 //    64-byte (down) slice of every row and keeps the activations of that
 //    slice in registers as mma B fragments. Each weight tile is 16 rows; the
 //    products run on the tensor cores (mma.sync m16n8k32 E4M3 for experts,
-//    m16n8k16 bf16 for the lm_head) with the M <= 8 tokens as the n = 8
-//    dimension. The 11 partials of a stage meet in shared memory; after a
-//    barrier of the MMA warps, 32 threads per tile sum them and apply the
-//    epilogue (row scales, gated GELU and router weight for gate/up; row
-//    scales and fp32 atomic accumulation into the residual for down; a
-//    running argmax per token for the lm_head).
+//    m16n8k16 bf16 for the lm_head). The 11 partials of a tile meet in a
+//    double-buffered shared-memory exchange; after one barrier, rotating
+//    reducer warps sum them and apply the epilogue (row scales, gated GELU
+//    and router weight for gate/up; row scales and fp32 atomic accumulation
+//    into the residual for down; a running argmax per token for the lm_head).
 //  * Experts read E4M3 weights as they are stored; the fp32 activations are
 //    written as a sum of 3 E4M3 terms (each the rounding residual of the
-//    previous one times 16) under a power-of-two scale per warp and token,
+//    previous one times 16) under a power-of-two scale per K-slice and token,
 //    so products are exact and each activation carries <= 2^-12 relative
-//    error (twice finer than an f16 rounding).
+//    error. The B fragment columns hold (token, term) pairs: NB = 2 blocks of
+//    8 columns for M <= 5, NB = 3 for M <= 8 (see column_of).
 //
 // Phases of layer l (every CTA):
-//  A  RMSNorm of h (stack) -> activation terms; CTA e < 128 computes router
-//     logit e; the shared expert's gate/up rows (split over all CTAs).
+//  A  RMSNorm sums of h and router logit e (CTA e < 128); the gate/up
+//     activation terms are split once per grid (one warp per token and
+//     K-slice) into the workspace.
 //  -- grid barrier
 //  B  softmax/top-8/renormalise + distinct-expert list (every CTA, same
-//     result); routed gate/up rows split evenly over CTAs by row pairs.
-//  -- grid barrier
-//  C  down rows of every distinct expert and the shared one, split evenly;
+//     result); gate/up tiles: shared-expert tiles, then routed ones, in whole
+//     8-row tiles dealt over the CTAs.
+//  C  down rows of every distinct expert and the shared one, dealt against
+//     each CTA's gate/up tiles; each CTA polls the activation entries it
+//     reads until their pending marker is gone (no barrier between B and C);
 //     results (already weighted by the router) are added into the fp32
 //     residual h with atomics.
 //  -- grid barrier
