@@ -364,10 +364,11 @@ __device__ __forceinline__ Range gu_shared_rows(int cta)
 
 __device__ __forceinline__ Range gu_routed_rows(int U, int cta, int G)
 {
-    constexpr int kTiles = kF / 8;
-    const long long total = (long long)(U + 1) * kTiles;
-    const int b = static_cast<int>(total * cta / G) - min(cta, kTiles);
-    const int e = static_cast<int>(total * (cta + 1) / G) - min(cta + 1, kTiles);
+    // 32-bit arithmetic: (U + 1) * 88 * G < 2^31 for U < 65, G < 65536 / 88
+    constexpr unsigned kTiles = kF / 8;
+    const unsigned total = static_cast<unsigned>(U + 1) * kTiles;
+    const int b = static_cast<int>(total * cta / G) - min(cta, (int)kTiles);
+    const int e = static_cast<int>(total * (cta + 1) / G) - min(cta + 1, (int)kTiles);
     return Range{8 * b, 8 * e};
 }
 
@@ -382,12 +383,14 @@ __device__ __forceinline__ Range gu_routed_rows(int U, int cta, int G)
 // tiles. Cumulative over CTAs: 16 (units(c) - 3 * gate/up tiles before c).
 __device__ __forceinline__ Range down_rows(int U, int cta, int G)
 {
-    constexpr int kGuTiles = kF / 8;
-    constexpr int kW = 3;
-    const long long units = (long long)(U + 1) * (kW * kGuTiles + kH / 16);
-    const long long gtiles = (long long)(U + 1) * kGuTiles;
-    const int b = static_cast<int>(units * cta / G - kW * (gtiles * cta / G));
-    const int e = static_cast<int>(units * (cta + 1) / G - kW * (gtiles * (cta + 1) / G));
+    // 32-bit arithmetic: (U + 1) * 440 * G < 2^32 for U < 65, G <= 152 * 1000
+    constexpr unsigned kGuTiles = kF / 8;
+    constexpr unsigned kW = 3;
+    const unsigned units = static_cast<unsigned>(U + 1) * (kW * kGuTiles + kH / 16);
+    const unsigned gtiles = static_cast<unsigned>(U + 1) * kGuTiles;
+    const unsigned c0 = cta, c1 = cta + 1;
+    const int b = static_cast<int>(units * c0 / G - kW * (gtiles * c0 / G));
+    const int e = static_cast<int>(units * c1 / G - kW * (gtiles * c1 / G));
     return Range{16 * b, 16 * e};
 }
 
