@@ -167,8 +167,8 @@ __device__ __forceinline__ bool mbar_try(unsigned long long *b, uint32_t parity)
 // deadline passes (then raises the abort flag and the status bit).
 // On timeout the first wait to give up records where: status[1] = site, status[2] =
 // block, status[3] = warp, status[4] = the stage/post index it waited for.
-__device__ __forceinline__ bool mbar_wait(unsigned long long *b, uint32_t parity, Smem &s,
-                                          long long deadline, int32_t *status, int site = 0, int index = 0)
+__device__ __noinline__ bool mbar_wait_slow(unsigned long long *b, uint32_t parity, Smem &s, long long deadline,
+                                            int32_t *status, int site, int index)
 {
     for (int it = 0;; ++it) {
         if (mbar_try(b, parity))
@@ -188,6 +188,18 @@ __device__ __forceinline__ bool mbar_wait(unsigned long long *b, uint32_t parity
             }
         }
     }
+}
+
+// The common case inline (the phase has usually completed), the bounded
+// slow path out of line: one copy of it keeps the kernel's hot loops small.
+__device__ __forceinline__ bool mbar_wait(unsigned long long *b, uint32_t parity, Smem &s, long long deadline,
+                                          int32_t *status, int site = 0, int index = 0)
+{
+#pragma unroll 1
+    for (int it = 0; it < 8; ++it)
+        if (mbar_try(b, parity))
+            return true;
+    return mbar_wait_slow(b, parity, s, deadline, status, site, index);
 }
 
 // 16-byte shared-memory load as volatile asm: it keeps its place ahead of the
@@ -627,8 +639,8 @@ __device__ __forceinline__ void gu_products(const uint4 (&ra)[4], const uint4 (&
 // Gate/up epilogue of one reduced tile: the lane holds gate (x, y) and up
 // (z, w) of one row for its tokens a and b; writes act = comb *
 // gelu_tanh(s_g g) * (s_u u) at dst_a / dst_b.
-__device__ __forceinline__ void gu_epilogue(float *dst_a, float *dst_b, float4 f, float sg, float su, float ca,
-                                            float cb, bool ta, bool tb)
+__device__ __noinline__ void gu_epilogue(float *dst_a, float *dst_b, float4 f, float sg, float su, float ca,
+                                         float cb, bool ta, bool tb)
 {
     if (ta)
         __stcg(dst_a, gelu_tanh(sg * f.x) * (su * f.z) * ca);
@@ -1238,7 +1250,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_fused(const __grid_constant__ P
                 }
                 uint32_t top_key = 0, my_key = 0;
                 int my_i = 0;
-#pragma unroll
+#pragma unroll 1
                 for (int rr = 0; rr < kK; ++rr) {
                     const uint32_t lk = max(max(key[0], key[1]), max(key[2], key[3]));
                     const uint32_t gk = __reduce_max_sync(0xFFFFFFFFu, lk);
