@@ -60,6 +60,44 @@ def measured_peaks():
         return FALLBACK_HBM_GBS, "fallback"
 
 
+# ---------------------------------------------------------------- ncu traffic
+KERNEL_SOURCES = ("fine_grained_moe_gb300/csrc/fused_step.cuh", "fine_grained_moe_gb300/csrc/common.cuh",
+                  "fine_grained_moe_gb300/csrc/fgm.cu")
+TRAFFIC_PROFILE = os.path.join("profiles", "k_fused_verify_step_traffic.md")
+
+
+def kernel_source_hash():
+    """sha256 over the sources of the persistent kernel (a changed kernel voids
+    a traffic figure taken on an older one)."""
+    import hashlib
+    h = hashlib.sha256()
+    for rel in KERNEL_SOURCES:
+        with open(os.path.join(ROOT, rel), "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()
+
+
+def captured_traffic():
+    """DRAM bytes (read + write) of one verify-step launch from the committed ncu
+    summary, or None when that summary was taken on other kernel sources."""
+    try:
+        with open(os.path.join(ROOT, TRAFFIC_PROFILE)) as f:
+            text = f.read()
+    except OSError:
+        return None
+    fields = {}
+    for line in text.splitlines():
+        if ":" in line and line.startswith("- "):
+            k, v = line[2:].split(":", 1)
+            fields[k.strip()] = v.strip().strip("`")
+    if fields.get("kernel sources sha256") != kernel_source_hash():
+        return None
+    try:
+        return int(fields["traffic per launch (bytes)"])
+    except (KeyError, ValueError):
+        return None
+
+
 # ---------------------------------------------------------------- clocks
 class ClockSampler:
     """nvidia-smi sampling of SM clocks and throttle reasons during the timed region."""
@@ -367,7 +405,7 @@ def run_ours(args, rank, world):
             "peak_kind": f"{peak_kind} copy bandwidth",
             "unit": "GB/s",
             "frac": round(achieved / peak, 4),
-            "traffic": None,
+            "traffic": (captured_traffic() if args.path == "fused" else None),
             "algorithmic_bytes_per_launch": int(bytes_total / K),
         },
         "e2e": {"value": round(e2e_tok_all / e2e_max, 2), "unit": "tokens/s",

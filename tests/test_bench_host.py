@@ -52,3 +52,16 @@ def test_reference_arm_idle_on_other_ranks():
     import bench
     args = argparse.Namespace(steps=3, warmup=3)
     assert bench.run_reference(args, rank=1, world=2) is None
+
+
+def test_traffic_figure_only_for_the_kernel_it_was_taken_on(tmp_path, monkeypatch):
+    sys.path.insert(0, ROOT)
+    import bench
+    prof = tmp_path / "traffic.md"
+    monkeypatch.setattr(bench, "TRAFFIC_PROFILE", str(prof))
+    assert bench.captured_traffic() is None          # no summary
+    prof.write_text(f"- kernel sources sha256: `{bench.kernel_source_hash()}`\n"
+                    "- traffic per launch (bytes): 5278000000\n")
+    assert bench.captured_traffic() == 5278000000
+    prof.write_text("- kernel sources sha256: `0000`\n- traffic per launch (bytes): 5278000000\n")
+    assert bench.captured_traffic() is None          # taken on other kernel sources
