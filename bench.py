@@ -481,6 +481,64 @@ def run_case(args):
             "status": ws.status()}
 
 
+def run_sweep(args):
+    """The full verify step swept over M = 1..8 (gamma 0..7) and the router bias
+    Zipf s in {0, 1.1, 2.0}: the 30-layer stack and lm_head of the headline
+    workload, the bias swapped per s. Prints one JSON line per point (tokens/s
+    counting accepted drafts + 1 per step, and algorithmic HBM GB/s); returns None."""
+    import torch
+
+    import fine_grained_moe_gb300 as fgm
+    import synth
+    from fine_grained_moe_gb300 import traffic
+
+    dev = torch.device("cuda", 0)
+    torch.cuda.set_device(dev)
+    fgm.lib()
+    fgm.select_path(fgm.PATH_FUSED if args.path == "fused" else fgm.PATH_STAGED)
+    layers, emb, _ = make_workload(dev)
+    ws = fgm.Workspace(dev)
+    peak, _ = measured_peaks()
+    K, W = args.steps, args.warmup
+    for s_zipf in (0.0, 1.1, 2.0):
+        bias = None if s_zipf == 0.0 else synth.zipf_bias(s_zipf).to(dev)
+        for p in layers:
+            p["router_b"] = bias
+        arr = fgm.layers_array(layers)
+        for m in range(1, 9):
+            xs = [synth.hidden_states(HIDDEN_SEED0 + b, m, device=dev) for b in range(N_BATCHES)]
+            trace = torch.empty((N_LAYERS, m, 8), dtype=torch.int32, device=dev)
+            drafts, nbytes = [], []
+            for b, x in enumerate(xs):
+                fgm.moe_stack_fwd(layers, x, ids_trace=trace, ws=ws)
+                tr = trace.cpu()
+                nbytes.append(traffic.step_bytes([len(torch.unique(tr[l])) for l in range(N_LAYERS)]))
+                am = torch.empty(m, dtype=torch.int32, device=dev)
+                fgm.verify_step(layers, emb, x, torch.zeros(max(m - 1, 1), dtype=torch.int32, device=dev),
+                                argmax=am, ws=ws, _arr=arr)
+                drafts.append(synth.drafts(DRAFT_SEED0 + b, am.cpu()).to(dev) if m > 1 else None)
+            outs = torch.zeros((K, 2), dtype=torch.int32, device=dev)
+            for i in range(W):
+                fgm.verify_step(layers, emb, xs[i % N_BATCHES], drafts[i % N_BATCHES], ws=ws, _arr=arr)
+            torch.cuda.synchronize()
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record()
+            for i in range(K):
+                b = i % N_BATCHES
+                fgm.verify_step(layers, emb, xs[b], drafts[b], out=outs[i], ws=ws, _arr=arr)
+            e1.record()
+            torch.cuda.synchronize()
+            ms = e0.elapsed_time(e1)
+            tokens = int(outs[:, 0].sum()) + K
+            gbs = sum(nbytes[i % N_BATCHES] for i in range(K)) / (ms * 1e-3) / 1e9
+            print(json.dumps({"case": "sweep", "M": m, "gamma": m - 1, "zipf_s": s_zipf,
+                              "tokens_per_s": round(tokens / (ms * 1e-3), 1),
+                              "ms_per_step": round(ms / K, 4), "accepted_per_step": round((tokens - K) / K, 3),
+                              "hbm_gbs": round(gbs, 1), "frac_of_peak": round(gbs / peak, 4),
+                              "status": ws.status()}), flush=True)
+    return None
+
+
 # ---------------------------------------------------------------- reference arm
 def run_reference(args, rank, world):
     """The oracle as the reference arm: one full step on batch 0 fixes the
@@ -553,8 +611,9 @@ def main():
                     help="persistent kernel (default) or one launch per stage")
     ap.add_argument("--phase-trace", metavar="PATH", default=None,
                     help="after timing, run one traced step and write a per-phase summary to PATH")
-    ap.add_argument("--case", choices=("verify", "layer", "lm_head"), default="verify",
-                    help="verify: the headline step; layer / lm_head: one stage alone (profiling)")
+    ap.add_argument("--case", choices=("verify", "layer", "lm_head", "sweep"), default="verify",
+                    help="verify: the headline step; layer / lm_head: one stage alone (profiling); "
+                         "sweep: the verify step over M = 1..8 and Zipf s in {0, 1.1, 2} (one line each)")
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")
@@ -567,6 +626,8 @@ def main():
     try:
         if args.impl == "reference":
             line = run_reference(args, rank, world)
+        elif args.case == "sweep":
+            line = run_sweep(args)
         elif args.case != "verify":
             line = run_case(args)
         else:

@@ -112,3 +112,35 @@ def test_verify_step_m1_no_drafts(setup):
     fgm.verify_step(s["layers"], s["emb"], s["x"], s["draft"].cuda(), argmax=am5, ws=s["ws"])
     if s["mg"][0] > MARGIN:
         assert int(am.cpu()[0]) == int(am5.cpu()[0])
+
+
+def test_stack_and_verify_m8(setup):
+    """M = 8 (gamma = 7) runs the three-block packing of the persistent kernel;
+    full size, against the oracle trajectory of the same 30 layers."""
+    s = setup
+    fgm = s["fgm"]
+    m = 8
+    x = synth.hidden_states(41, m, device="cuda")
+    h = bf16_values(x)
+    traj = []
+    for L in s["host"]:
+        out = oracle.stack_layer(L, h)
+        traj.append((out.ids.copy(), out.margin.copy(), h.copy()))
+        h = out.y
+    trace = torch.empty((N_LAYERS, m, 8), dtype=torch.int32, device="cuda")
+    y = fgm.moe_stack_fwd(s["layers"], x, ids_trace=trace, ws=s["ws"])
+    torch.cuda.synchronize()
+    full = _compare_stack(trace.cpu().numpy(), y, h, traj, s["host"], m)
+    assert len(full) >= 3, full
+    hn_bits = oracle.bf16_round(oracle.rmsnorm(h))
+    am_ref, _, mg = oracle.lm_head(bf16_bits(s["emb"]), oracle.bf16_to_f64(hn_bits))
+    draft = synth.drafts(43, am_ref)
+    am = torch.empty(m, dtype=torch.int32, device="cuda")
+    out = fgm.verify_step(s["layers"], s["emb"], x, draft.cuda(), argmax=am, ws=s["ws"])
+    torch.cuda.synchronize()
+    gam = am.cpu().numpy()
+    for t in full:
+        if mg[t] > MARGIN:
+            assert gam[t] == am_ref[t], (t, gam[t], am_ref[t])
+    assert tuple(out.cpu().tolist()) == oracle.spec_verify(gam, draft.numpy())
+    assert s["ws"].status() == 0
