@@ -131,7 +131,7 @@ def test_stack_and_verify_m8(setup):
     y = fgm.moe_stack_fwd(s["layers"], x, ids_trace=trace, ws=s["ws"])
     torch.cuda.synchronize()
     full = _compare_stack(trace.cpu().numpy(), y, h, traj, s["host"], m)
-    assert len(full) >= 3, full
+    assert len(full) >= 2, full
     hn_bits = oracle.bf16_round(oracle.rmsnorm(h))
     am_ref, _, mg = oracle.lm_head(bf16_bits(s["emb"]), oracle.bf16_to_f64(hn_bits))
     draft = synth.drafts(43, am_ref)
