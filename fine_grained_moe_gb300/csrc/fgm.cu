@@ -89,16 +89,17 @@ int device_ready(int *sms)
             FGM_SMEM(k_lmhead_basic<7>, 7 * kH * 4);
             FGM_SMEM(k_lmhead_basic<8>, 8 * kH * 4);
 #undef FGM_SMEM
-            FGM_CUDA(cudaFuncSetAttribute(fused::k_fused<2>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                          (int)sizeof(fused::Smem)));
-            FGM_CUDA(cudaFuncSetAttribute(fused::k_fused<3>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                          (int)sizeof(fused::Smem)));
-            int per_sm = 0, per_sm3 = 0;
-            FGM_CUDA(cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, fused::k_fused<2>, fused::kThreads,
-                                                                   sizeof(fused::Smem)));
-            FGM_CUDA(cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm3, fused::k_fused<3>, fused::kThreads,
-                                                                   sizeof(fused::Smem)));
-            per_sm = per_sm < per_sm3 ? per_sm : per_sm3;
+            const void *kerns[4] = {reinterpret_cast<const void *>(fused::k_fused<2, false>),
+                                    reinterpret_cast<const void *>(fused::k_fused<3, false>),
+                                    reinterpret_cast<const void *>(fused::k_fused<2, true>),
+                                    reinterpret_cast<const void *>(fused::k_fused<3, true>)};
+            int per_sm = 1 << 30;
+            for (const void *k : kerns) {
+                FGM_CUDA(cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)sizeof(fused::Smem)));
+                int n = 0;
+                FGM_CUDA(cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, k, fused::kThreads, sizeof(fused::Smem)));
+                per_sm = n < per_sm ? n : per_sm;
+            }
             d.fused_grid = (per_sm >= 1 && d.sms >= fused::kMinCtas) ? d.sms : 0;
         }
         d.ready = true;
@@ -134,8 +135,11 @@ int launch_fused(fused::Params &prm, cudaStream_t st)
     g_debug_stall = 0;
     void *args[] = {&prm};
     // packed activation columns: 2 blocks of 8 hold M <= 5 tokens x 3 terms, 3 blocks M <= 8
-    const void *kern = prm.M <= 5 ? reinterpret_cast<const void *>(fused::k_fused<2>)
-                                  : reinterpret_cast<const void *>(fused::k_fused<3>);
+    const bool traced = prm.trace != nullptr;
+    const void *kern = prm.M <= 5 ? (traced ? reinterpret_cast<const void *>(fused::k_fused<2, true>)
+                                            : reinterpret_cast<const void *>(fused::k_fused<2, false>))
+                                  : (traced ? reinterpret_cast<const void *>(fused::k_fused<3, true>)
+                                            : reinterpret_cast<const void *>(fused::k_fused<3, false>));
     FGM_CUDA(cudaLaunchCooperativeKernel(kern, dim3(G),
                                          dim3(fused::kThreads), args, sizeof(fused::Smem), st));
     return FGM_OK;

@@ -681,7 +681,10 @@ __device__ __forceinline__ float4 red_sum4(const Smem &s, int b, int t, int ln)
     return v;
 }
 
-template <int NB>
+// NB: packed column blocks (2: M <= 5, 3: M <= 8). TRACE: the phase-trace
+// profiling aid is compiled in (a separate instantiation, so that the
+// production kernels carry none of its code).
+template <int NB, bool TRACE>
 __global__ void __launch_bounds__(kThreads, 1) k_fused(const __grid_constant__ Params p)
 {
     extern __shared__ __align__(128) uint8_t smem_raw[];
@@ -713,7 +716,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_fused(const __grid_constant__ P
         if (lane == 0) {
             uint32_t stage = 0;
             bool ok = true;
-            long long *pdetail = (p.trace && cta == G / 2)
+            long long *pdetail = (TRACE && p.trace && cta == G / 2)
                                      ? p.trace + (size_t)(n_layers * kTracePoints + 2) * G : nullptr;
             int p_layer = 0;
             uint32_t p_stage0 = 0;
@@ -879,7 +882,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_fused(const __grid_constant__ P
         consumer_sync();
     };
 
-    long long *detail = (p.trace && cta == G / 2)
+    long long *detail = (TRACE && p.trace && cta == G / 2)
                             ? p.trace + (size_t)(n_layers * kTracePoints + 2) * G : nullptr;
     int cur_layer = 0;
     uint32_t layer_stage0 = 0;
@@ -1054,7 +1057,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_fused(const __grid_constant__ P
         const fgm_layer &L = p.layers[l];
         const int pb = l & 1;
         auto stamp = [&](int k) {
-            if (p.trace && tid == 0)
+            if (TRACE && p.trace && tid == 0)
                 p.trace[((size_t)l * kTracePoints + k) * G + cta] = gtime();
         };
         cur_layer = l;
@@ -1618,7 +1621,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_fused(const __grid_constant__ P
         stamp(9);
         grid_barrier();
     }
-    if (p.trace && tid == 0)
+    if (TRACE && p.trace && tid == 0)
         p.trace[((size_t)n_layers * kTracePoints) * G + cta] = gtime();
 
     // ------------------------------------------------------------ outputs
@@ -1729,7 +1732,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_fused(const __grid_constant__ P
             __stcg(ws.part_idx + cta * kMaxM + tid, bi);
         }
     }
-    if (p.trace && tid == 0)
+    if (TRACE && p.trace && tid == 0)
         p.trace[((size_t)n_layers * kTracePoints + 1) * G + cta] = gtime();
 
     // ------------------------------------------------------------ exit
