@@ -681,6 +681,105 @@ __device__ __forceinline__ float4 red_sum4(const Smem &s, int b, int t, int ln)
     return v;
 }
 
+// Writes the pending marker into an activation buffer (tokens < M): every
+// slot if n_used == 0, else the first n_used slots and the shared one. Thread
+// `first` of `stride` cooperating threads; out of line (cold code).
+__device__ __noinline__ void mark_act_pending(float *base, int n_used, int M, int first, int stride)
+{
+    const float4 pend4 = make_float4(__uint_as_float(kActPending), __uint_as_float(kActPending),
+                                     __uint_as_float(kActPending), __uint_as_float(kActPending));
+    const int rows = (n_used == 0 ? kMaxSlots : n_used + 1) * M;
+    for (int i = first; i < rows * (kF / 4); i += stride) {
+        const int r = i / (kF / 4), c4 = i % (kF / 4);
+        const int slot = n_used == 0 ? r / M : (r / M < n_used ? r / M : kSharedSlot);
+        __stcg(reinterpret_cast<float4 *>(base + ((size_t)slot * kMaxM + r % M) * kF) + c4, pend4);
+    }
+}
+
+// Packed down-phase B fragments of one expert slot for this warp's 64-wide
+// K-slice, out of line (called once per slot and layer).
+template <int NB>
+struct DownCols {
+    uint32_t b[NB][4];
+    float fa[3], fb[3];
+};
+
+// act_slot: the slot's activations [token][704]. Token g's 16 values (lanes
+// 4g..4g+3) are polled until no value carries the pending marker (bounded by
+// the deadline; on timeout the abort flag and status are set and zeros used),
+// split into terms under a power-of-two scale, and moved into the packed
+// columns (column g of block j from lane 4 token + q).
+template <int NB>
+__device__ __noinline__ DownCols<NB> down_columns(const float *act_slot, int M, int warp, int lane, int *abort,
+                                                  long long deadline, int32_t *status, int aslot)
+{
+    const int g = lane >> 2, q = lane & 3;
+    float v[16];
+    if (g < M) {
+        const float *ar = act_slot + (size_t)g * kF + 64 * warp + 16 * q;
+        for (int it = 0;; ++it) {
+            bool ready = true;
+#pragma unroll
+            for (int k = 0; k < 4; ++k) {
+                const float4 f = ldcg4(ar + 4 * k);
+                v[4 * k] = f.x;
+                v[4 * k + 1] = f.y;
+                v[4 * k + 2] = f.z;
+                v[4 * k + 3] = f.w;
+            }
+#pragma unroll
+            for (int i = 0; i < 16; ++i)
+                ready = ready && __float_as_uint(v[i]) != kActPending;
+            if (ready)
+                break;
+            if ((it & 15) == 15 && (*reinterpret_cast<volatile int *>(abort) || gtime() > deadline)) {
+                *reinterpret_cast<volatile int *>(abort) = 1;
+                if (atomicOr(status, FGM_STATUS_WAIT_TIMEOUT) == 0) {
+                    status[1] = 7;
+                    status[2] = blockIdx.x;
+                    status[3] = warp;
+                    status[4] = aslot;
+                }
+#pragma unroll
+                for (int i = 0; i < 16; ++i)
+                    v[i] = 0.0f;
+                break;
+            }
+        }
+    } else {
+#pragma unroll
+        for (int i = 0; i < 16; ++i)
+            v[i] = 0.0f;
+    }
+    float amax = 0.0f;
+#pragma unroll
+    for (int i = 0; i < 16; ++i)
+        amax = fmaxf(amax, fabsf(v[i]));
+    const float S = term_scale(quad_max(amax));
+    uint32_t T[kTerms][4];
+    split16_into(v, S, T);
+    DownCols<NB> r;
+#pragma unroll
+    for (int j = 0; j < NB; ++j) {
+        int tok, term;
+        column_of<NB>(j, g, tok, term);
+        const bool ok = tok >= 0 && tok < M;
+        const int src = 4 * (tok >= 0 ? tok : 0) + q;
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+            const uint32_t w0 = __shfl_sync(0xFFFFFFFFu, T[0][k], src);
+            const uint32_t w1 = __shfl_sync(0xFFFFFFFFu, T[1][k], src);
+            const uint32_t w2 = __shfl_sync(0xFFFFFFFFu, T[2][k], src);
+            r.b[j][k] = ok ? (term == 0 ? w0 : term == 1 ? w1 : w2) : 0u;
+        }
+    }
+    const int qb = NB == 2 ? 4 : q + 4;
+    const float sa = __shfl_sync(0xFFFFFFFFu, S, 4 * q);
+    const float sb = __shfl_sync(0xFFFFFFFFu, S, 4 * qb);
+    column_weights<NB>(sa, sb, q, M, r.fa, r.fb);
+    return r;
+}
+
 // NB: packed column blocks (2: M <= 5, 3: M <= 8). TRACE: the phase-trace
 // profiling aid is compiled in (a separate instantiation, so that the
 // production kernels carry none of its code).
@@ -918,15 +1017,8 @@ __global__ void __launch_bounds__(kThreads, 1) k_fused(const __grid_constant__ P
     // previous contents is left and that its next writers come after a grid
     // barrier.
     auto mark_pending = [&](int buf, int n_used) {
-        const float4 pend4 = make_float4(__uint_as_float(kActPending), __uint_as_float(kActPending),
-                                         __uint_as_float(kActPending), __uint_as_float(kActPending));
-        const int rows = (n_used == 0 ? kMaxSlots : n_used + 1) * M;
-        float *base = ws.act + (size_t)buf * kMaxSlots * kMaxM * kF;
-        for (int i = cta * kConsumers + tid; i < rows * (kF / 4); i += G * kConsumers) {
-            const int r = i / (kF / 4), c4 = i % (kF / 4);
-            const int slot = n_used == 0 ? r / M : (r / M < n_used ? r / M : kSharedSlot);
-            __stcg(reinterpret_cast<float4 *>(base + ((size_t)slot * kMaxM + r % M) * kF) + c4, pend4);
-        }
+        mark_act_pending(ws.act + (size_t)buf * kMaxSlots * kMaxM * kF, n_used, M, cta * kConsumers + tid,
+                         G * kConsumers);
     };
     // lm_head: lanes 0..3 keep the running best of tokens 2 lane, 2 lane + 1
     // over the tiles this warp reduces
@@ -1450,91 +1542,25 @@ __global__ void __launch_bounds__(kThreads, 1) k_fused(const __grid_constant__ P
             // their activation terms (this warp's 64-wide K-slice, token g) are
             // prepared once, up front.
             const int si0 = ds.begin / kH;
-            uint32_t bd[2][NB][4];   // packed activation columns per slot
-            float fa_d[2][3], fb_d[2][3];
+            DownCols<NB> dc[2];   // packed activation columns of the (at most two) slots
 #pragma unroll
             for (int h2 = 0; h2 < 2; ++h2) {
                 const int si = si0 + h2;
                 const bool slot_ok = si <= U && (h2 == 0 || ds.end > (si0 + 1) * kH);   // same for the whole CTA
                 if (slot_ok) {
-                    // token g's 16 values of this K-slice, split into terms (lanes 4g..4g+3)
-                    float v[16];
-                    if (g < M) {
-                        const int aslot = si < U ? si : kSharedSlot;
-                        const float *ar = act_cur + ((size_t)aslot * kMaxM + g) * kF + 64 * warp + 16 * q;
-                        // written by the gate/up epilogues of other CTAs: poll until no
-                        // value carries the pending marker (bounded by the deadline)
-                        for (int it = 0;; ++it) {
-                            bool ready = true;
-#pragma unroll
-                            for (int k = 0; k < 4; ++k) {
-                                const float4 f = ldcg4(ar + 4 * k);
-                                v[4 * k] = f.x;
-                                v[4 * k + 1] = f.y;
-                                v[4 * k + 2] = f.z;
-                                v[4 * k + 3] = f.w;
-                            }
-#pragma unroll
-                            for (int i = 0; i < 16; ++i)
-                                ready = ready && __float_as_uint(v[i]) != kActPending;
-                            if (ready)
-                                break;
-                            if ((it & 15) == 15 &&
-                                (*reinterpret_cast<volatile int *>(&s.abort) || gtime() > deadline)) {
-                                *reinterpret_cast<volatile int *>(&s.abort) = 1;
-                                if (atomicOr(status, FGM_STATUS_WAIT_TIMEOUT) == 0) {
-                                    status[1] = 7;
-                                    status[2] = cta;
-                                    status[3] = warp;
-                                    status[4] = aslot;
-                                }
-#pragma unroll
-                                for (int i = 0; i < 16; ++i)
-                                    v[i] = 0.0f;
-                                break;
-                            }
-                        }
-                    } else {
-#pragma unroll
-                        for (int i = 0; i < 16; ++i)
-                            v[i] = 0.0f;
-                    }
-                    float amax = 0.0f;
-#pragma unroll
-                    for (int i = 0; i < 16; ++i)
-                        amax = fmaxf(amax, fabsf(v[i]));
-                    const float S = term_scale(quad_max(amax));
-                    uint32_t T[kTerms][4];
-                    split16_into(v, S, T);
-                    // packed column g of block j: its (token, term) words from lane 4 token + q
-#pragma unroll
-                    for (int j = 0; j < NB; ++j) {
-                        int tok, term;
-                        column_of<NB>(j, g, tok, term);
-                        const bool ok = tok >= 0 && tok < M;
-                        const int src = 4 * (tok >= 0 ? tok : 0) + q;
-#pragma unroll
-                        for (int k = 0; k < 4; ++k) {
-                            const uint32_t w0 = __shfl_sync(0xFFFFFFFFu, T[0][k], src);
-                            const uint32_t w1 = __shfl_sync(0xFFFFFFFFu, T[1][k], src);
-                            const uint32_t w2 = __shfl_sync(0xFFFFFFFFu, T[2][k], src);
-                            bd[h2][j][k] = ok ? (term == 0 ? w0 : term == 1 ? w1 : w2) : 0u;
-                        }
-                    }
-                    const int qb = NB == 2 ? 4 : q + 4;
-                    const float sa = __shfl_sync(0xFFFFFFFFu, S, 4 * q);
-                    const float sb = __shfl_sync(0xFFFFFFFFu, S, 4 * qb);
-                    column_weights<NB>(sa, sb, q, M, fa_d[h2], fb_d[h2]);
+                    const int aslot = si < U ? si : kSharedSlot;
+                    dc[h2] = down_columns<NB>(act_cur + (size_t)aslot * kMaxM * kF, M, warp, lane, &s.abort, deadline,
+                                              status, aslot);
                 } else {
 #pragma unroll
                     for (int j = 0; j < NB; ++j)
 #pragma unroll
                         for (int k = 0; k < 4; ++k)
-                            bd[h2][j][k] = 0u;
+                            dc[h2].b[j][k] = 0u;
 #pragma unroll
                     for (int t = 0; t < 3; ++t) {
-                        fa_d[h2][t] = 0.0f;
-                        fb_d[h2][t] = 0.0f;
+                        dc[h2].fa[t] = 0.0f;
+                        dc[h2].fb[t] = 0.0f;
                     }
                 }
             }
@@ -1551,11 +1577,11 @@ __global__ void __launch_bounds__(kThreads, 1) k_fused(const __grid_constant__ P
                 for (int jj = 0; jj < NB; ++jj)
 #pragma unroll
                     for (int k = 0; k < 4; ++k)
-                        bt[jj][k] = hs ? bd[1][jj][k] : bd[0][jj][k];
+                        bt[jj][k] = hs ? dc[1].b[jj][k] : dc[0].b[jj][k];
 #pragma unroll
                 for (int t = 0; t < 3; ++t) {
-                    fa[t] = hs ? fa_d[1][t] : fa_d[0][t];
-                    fb[t] = hs ? fb_d[1][t] : fb_d[0][t];
+                    fa[t] = hs ? dc[1].fa[t] : dc[0].fa[t];
+                    fb[t] = hs ? dc[1].fb[t] : dc[0].fb[t];
                 }
                 const bool got = stage_wait();
                 const uint8_t *slot = s.ring[stage % kStages];
