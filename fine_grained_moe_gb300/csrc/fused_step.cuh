@@ -1169,6 +1169,8 @@ __global__ void __launch_bounds__(kThreads, 1) k_fused(const __grid_constant__ P
             const bool from_x = (p.mode == kModeLayer) || l == 0;
             const bool norm = p.mode != kModeLayer;
             const bool router_cta = cta < kE;
+            // only the router CTAs and those hosting a term-split unit read h here
+            const bool need_h = router_cta || (G - 1 - cta) * kMW < M * kMW;
             float v[4][16];
             const uint16_t *wrow = L.router_w + (size_t)cta * kH + 256 * warp + 16 * q;
             // router row of this CTA (its K-slice positions): fetch into L1
@@ -1180,7 +1182,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_fused(const __grid_constant__ P
             }
             // router bias of this CTA's expert, fetched early (off the critical path)
             const float rbias = (router_cta && tid < M && L.router_b) ? __ldg(L.router_b + cta) : 0.0f;
-            if (g < M) {
+            if (g < M && need_h) {
                 if (from_x)
                     load_slice_bf16(p.x + (size_t)g * kH, warp, q, v);
                 else
