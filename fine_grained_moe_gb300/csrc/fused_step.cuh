@@ -338,20 +338,6 @@ __device__ __forceinline__ float quad_sum(float v)
     return v + __shfl_xor_sync(0xFFFFFFFFu, v, 2);
 }
 
-// Term weights for the two token columns (2q, 2q+1) a thread's accumulator
-// holds: inv[t][0/1] = 1 / (S_col * 16^t). S of token g lives in lanes 4g..4g+3.
-__device__ __forceinline__ void column_inv(float S, int q, float (&inv)[kTerms][2])
-{
-    const float s0 = __shfl_sync(0xFFFFFFFFu, S, 8 * q);
-    const float s1 = __shfl_sync(0xFFFFFFFFu, S, 8 * q + 4);
-    float f = 1.0f;
-#pragma unroll
-    for (int t = 0; t < kTerms; ++t) {
-        inv[t][0] = f / s0;
-        inv[t][1] = f / s1;
-        f *= 0.0625f;
-    }
-}
 
 // ---------------------------------------------------------------- work plans
 // Both the producer and the consumers walk the same sequence of ring stages.
@@ -599,40 +585,6 @@ __device__ __forceinline__ void split_terms4(float (&y)[4], uint32_t (&w)[kTerms
             y[2] = (y[2] - dh.x) * 16.0f;
             y[3] = (y[3] - dh.y) * 16.0f;
         }
-    }
-}
-
-// Gate/up products of one 16-row tile over warp w's 256-byte K-slice; the
-// terms are combined with their weights into the 16 x 8 partial `out`.
-__device__ __forceinline__ void gu_products(const uint4 (&ra)[4], const uint4 (&rb)[4], const uint32_t (&b)[4][kTerms][4],
-                                            const float (&inv)[kTerms][2], float (&out)[4])
-{
-    // two accumulator sets (even / odd chunks) halve the dependent mma chains
-    float acc[2][kTerms][4];
-#pragma unroll
-    for (int h = 0; h < 2; ++h)
-#pragma unroll
-        for (int t = 0; t < kTerms; ++t)
-#pragma unroll
-            for (int e = 0; e < 4; ++e)
-                acc[h][t][e] = 0.0f;
-#pragma unroll
-    for (int c = 0; c < 4; ++c) {
-        const uint32_t a0[4] = {ra[c].x, rb[c].x, ra[c].y, rb[c].y};
-        const uint32_t a1[4] = {ra[c].z, rb[c].z, ra[c].w, rb[c].w};
-#pragma unroll
-        for (int t = 0; t < kTerms; ++t) {
-            mma_e4m3(acc[c & 1][t], a0, b[c][t][0], b[c][t][1]);
-            mma_e4m3(acc[c & 1][t], a1, b[c][t][2], b[c][t][3]);
-        }
-    }
-#pragma unroll
-    for (int e = 0; e < 4; ++e) {
-        float v = 0.0f;
-#pragma unroll
-        for (int t = 0; t < kTerms; ++t)
-            v += (acc[0][t][e] + acc[1][t][e]) * inv[t][e & 1];
-        out[e] = v;
     }
 }
 
@@ -1194,8 +1146,9 @@ __global__ void __launch_bounds__(kThreads, 1) k_fused(const __grid_constant__ P
                     for (int i = 0; i < 16; ++i)
                         v[c][i] = 0.0f;
             }
-            // scales of this CTA's shared-expert gate/up rows (read after the
-            // consumer barrier below)
+            // scales of this CTA's shared-expert gate/up rows, copied asynchronously;
+            // each thread waits for its copies before the first gate/up tile, and
+            // the exchange barrier that follows makes them visible to the reducers
             for (int i = tid; i < rsh.end - rsh.begin; i += kConsumers) {
                 cp_async4(&s.sc_g[kMaxGuRows + i], L.gate_s + (size_t)kShared * kF + rsh.begin + i);
                 cp_async4(&s.sc_u[kMaxGuRows + i], L.up_s + (size_t)kShared * kF + rsh.begin + i);
