@@ -11,7 +11,8 @@ renormalised; expert = GELU-tanh(gate) * up then down, each weight row
 dequantised from E4M3 with its fp32 row scale; layer = routed experts
 weighted by the router plus the shared expert with weight 1; stack layer =
 h + layer(RMSNorm(h)); lm_head = bf16 embedding rows dotted with the final
-hidden rows, argmax with ties to the lower index; greedy verify = longest
+hidden rows, argmax with ties to the lower index (the FP8 variant: E4M3
+rows times their fp32 row scale); greedy verify = longest
 draft prefix equal to the target argmax of the preceding position.
 """
 
@@ -83,6 +84,7 @@ def lib():
         L.fgmo_stack_layer.argtypes = [ctypes.POINTER(_Dims), ctypes.POINTER(_Layer), vp, ci, cd,
                                        vp, vp, vp]
         L.fgmo_lm_head.argtypes = [vp, i64, ci, vp, ci, vp, vp, vp]
+        L.fgmo_lm_head_fp8.argtypes = [vp, vp, i64, ci, vp, ci, vp, vp, vp]
         L.fgmo_spec_verify.argtypes = [vp, vp, ci, vp]
         L.fgmo_num_threads.restype = ci
         L.fgmo_set_num_threads.argtypes = [ci]
@@ -272,6 +274,22 @@ def lm_head(emb_bits, h) -> tuple[np.ndarray, np.ndarray, np.ndarray]:
     mx = np.empty(M, np.float64)
     mg = np.empty(M, np.float64)
     lib().fgmo_lm_head(_p(e), V, H, _p(h), M, _p(am), _p(mx), _p(mg))
+    return am, mx, mg
+
+
+def lm_head_fp8(q, scale, h) -> tuple[np.ndarray, np.ndarray, np.ndarray]:
+    """FP8 lm_head argmax over E4M3 rows q [V, H] with fp32 row scales [V]:
+    returns (argmax int32 [M], max logit [M], top-1 minus top-2 [M])."""
+    q = _c(q, np.uint8)
+    sc = _c(scale, np.float32)
+    h = _c(h, np.float64)
+    V, H = q.shape
+    M = h.shape[0]
+    assert sc.shape == (V,) and h.shape[1] == H and 1 <= M <= 16
+    am = np.empty(M, np.int32)
+    mx = np.empty(M, np.float64)
+    mg = np.empty(M, np.float64)
+    lib().fgmo_lm_head_fp8(_p(q), _p(sc), V, H, _p(h), M, _p(am), _p(mx), _p(mg))
     return am, mx, mg
 
 

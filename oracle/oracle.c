@@ -348,12 +348,52 @@ void fgmo_stack_layer(const fgmo_dims *d, const fgmo_layer *L, double *h, int M,
     free(y);
 }
 
-/* Tied lm_head with argmax: z_{t,v} = sum_j E[v][j] h_t[j] over the bf16
- * embedding rows; argmax[t] (ties to the lower index), maxlogit[t] and the
- * gap to the runner-up margin[t]. Rows are independent; the loop visits each
- * embedding row once for all M tokens. */
-void fgmo_lm_head(const uint16_t *emb, int64_t V, int H, const double *h, int M, int32_t *argmax,
-                  double *maxlogit, double *margin)
+/* Logits of one vocabulary row v for the M hidden rows: z[t] = sum_j E[v][j] h_t[j],
+ * summed in natural j order. The two storage formats of the embedding: */
+typedef void (*fgmo_row_logits)(const void *rows, int64_t v, int H, const double *h, int M, double *z);
+
+typedef struct {
+    const uint8_t *q;     /* [V][H] E4M3 codes */
+    const float *scale;   /* [V] fp32 row scales */
+} fgmo_fp8_rows;
+
+/* bf16 rows, decoded by the format's formula. */
+static void row_logits_bf16(const void *rows, int64_t v, int H, const double *h, int M, double *z)
+{
+    const uint16_t *emb = (const uint16_t *)rows;
+    int j, t;
+    for (t = 0; t < M; ++t)
+        z[t] = 0.0;
+    for (j = 0; j < H; ++j) {
+        double e = fgmo_bf16_decode(emb[v * H + j]);
+        for (t = 0; t < M; ++t)
+            z[t] += e * h[(int64_t)t * H + j];
+    }
+}
+
+/* E4M3 rows with one fp32 scale per row, the expert weights' format applied to
+ * the embedding: z = s_v * (Q_v h), the same form as the gate/up products. */
+static void row_logits_fp8(const void *rows, int64_t v, int H, const double *h, int M, double *z)
+{
+    const fgmo_fp8_rows *r = (const fgmo_fp8_rows *)rows;
+    int j, t;
+    for (t = 0; t < M; ++t)
+        z[t] = 0.0;
+    for (j = 0; j < H; ++j) {
+        double e = fgmo_e4m3_decode(r->q[v * H + j]);
+        for (t = 0; t < M; ++t)
+            z[t] += e * h[(int64_t)t * H + j];
+    }
+    for (t = 0; t < M; ++t)
+        z[t] *= (double)r->scale[v];
+}
+
+/* Argmax over the V rows of the logits of each token: argmax[t] (ties to the
+ * lower index), maxlogit[t] and the gap to the runner-up margin[t]. Rows are
+ * independent; each row is visited once for all M tokens. NaN logits never
+ * win; if every logit of a token is NaN its argmax is -1. */
+static void lm_head_argmax(fgmo_row_logits row_logits, const void *rows, int64_t V, int H, const double *h,
+                           int M, int32_t *argmax, double *maxlogit, double *margin)
 {
     int t;
     double best[16], second[16];
@@ -378,14 +418,7 @@ void fgmo_lm_head(const uint16_t *emb, int64_t V, int H, const double *h, int M,
         }
 #pragma omp for schedule(static)
         for (v = 0; v < V; ++v) {
-            int j;
-            for (tt = 0; tt < M; ++tt)
-                z[tt] = 0.0;
-            for (j = 0; j < H; ++j) {
-                double e = fgmo_bf16_decode(emb[v * H + j]);
-                for (tt = 0; tt < M; ++tt)
-                    z[tt] += e * h[(int64_t)tt * H + j];
-            }
+            row_logits(rows, v, H, h, M, z);
             for (tt = 0; tt < M; ++tt) {
                 if (z[tt] > lb[tt]) {
                     ls[tt] = lb[tt];
@@ -416,6 +449,29 @@ void fgmo_lm_head(const uint16_t *emb, int64_t V, int H, const double *h, int M,
         if (margin)
             margin[t] = best[t] - second[t];
     }
+}
+
+/* Tied lm_head with argmax over the bf16 embedding rows. */
+void fgmo_lm_head(const uint16_t *emb, int64_t V, int H, const double *h, int M, int32_t *argmax,
+                  double *maxlogit, double *margin)
+{
+    lm_head_argmax(row_logits_bf16, emb, V, H, h, M, argmax, maxlogit, margin);
+}
+
+/* FP8 lm_head with argmax ("llm-decoding", §"Lever 1: fewer bytes (FP8
+ * weights)": every weight, the tied 262,144-word output projection included,
+ * stored in 8 bits and dequantised for the product; §"First principles:
+ * compute-bound or memory-bound?" counts that projection at a fifth of a
+ * token's bytes in BF16). The embedding is stored as E4M3 codes q[V][H] with
+ * one fp32 scale per row, z_{t,v} = scale[v] * sum_j e4m3(q[v][j]) h_t[j];
+ * outputs and tie rule as fgmo_lm_head. */
+void fgmo_lm_head_fp8(const uint8_t *q, const float *scale, int64_t V, int H, const double *h, int M,
+                      int32_t *argmax, double *maxlogit, double *margin)
+{
+    fgmo_fp8_rows rows;
+    rows.q = q;
+    rows.scale = scale;
+    lm_head_argmax(row_logits_fp8, &rows, V, H, h, M, argmax, maxlogit, margin);
 }
 
 /* Greedy verify: target[0..M-1] are the target's argmax tokens at the M

@@ -18,6 +18,9 @@ benchmark configurations):
                          to E4M3 with scale = max|row| / 448 (fp32) by
                          torch's float8_e4m3fn cast (round to nearest even);
   * tied embedding       [V, 2816] ~N(0, 0.02), rounded to bf16;
+                         its 8-bit copy for the FP8 lm_head: the expert
+                         weights' per-row E4M3 quantiser applied to those
+                         bf16 rows;
   * draft tokens         d_i equals the target token of position i-1 with
                          probability p (0.7), else uniform over [0, V).
 Every draw comes from a torch.Generator seeded explicitly. Values depend on
@@ -106,6 +109,19 @@ def embedding(seed: int, *, vocab: int = VOCAB, device="cpu", hidden: int = HIDD
         e[r0:r1] = (torch.randn((r1 - r0, hidden), generator=g, device=device,
                                 dtype=torch.float32) * std).to(torch.bfloat16)
     return e
+
+
+def embedding_fp8(emb: torch.Tensor, *, chunk_rows: int = 1 << 14) -> tuple[torch.Tensor, torch.Tensor]:
+    """The tied embedding stored in 8 bits: per-row E4M3 codes (uint8 [V, H]) and
+    fp32 row scales [V], by the quantiser of the expert weights applied to the
+    bf16 rows (on the tensor's device, in row chunks)."""
+    V, H = emb.shape
+    q = torch.empty((V, H), dtype=torch.uint8, device=emb.device)
+    sc = torch.empty(V, dtype=torch.float32, device=emb.device)
+    for r0 in range(0, V, chunk_rows):
+        r1 = min(V, r0 + chunk_rows)
+        q[r0:r1], sc[r0:r1] = quantize_rows_e4m3(emb[r0:r1].to(torch.float32))
+    return q, sc
 
 
 def drafts(seed: int, target, *, vocab: int = VOCAB, p: float = 0.7) -> torch.Tensor:
