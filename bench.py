@@ -428,8 +428,9 @@ def run_ours(args, rank, world):
 def run_case(args):
     """One stage alone, for profiling: `layer` = one MoE layer at M = 5 with the
     Zipf(1.1) bias (four weight copies and eight inputs rotate, so L2 never
-    serves a repeated expert); `lm_head` = the 262,144-word lm_head argmax at
-    M = 5. Prints a JSON line with the stage's HBM GB/s."""
+    serves a repeated expert); `lm_head` / `lm_head_fp8` = the 262,144-word
+    lm_head argmax at M = 5, bf16 or E4M3 rows (one call = the argmax kernel
+    and the cross-CTA reduction). Prints a JSON line with the stage's HBM GB/s."""
     import torch
 
     import fine_grained_moe_gb300 as fgm
@@ -456,6 +457,13 @@ def run_case(args):
         run = lambda i: fgm.moe_layer_fwd(calls[i][0], calls[i][1], ws=ws)
         unit_bytes = nbytes
         name = "one MoE layer, M=5, Zipf s=1.1 (4 weight copies rotate)"
+    elif args.case == "lm_head_fp8":
+        emb_q, emb_s = synth.embedding_fp8(synth.embedding(EMB_SEED, device=dev))
+        torch.cuda.empty_cache()
+        am = torch.empty(M, dtype=torch.int32, device=dev)
+        run = lambda i: fgm.lm_head_argmax_fp8(emb_q, emb_s, xs[i % N_BATCHES], argmax=am, ws=ws)
+        unit_bytes = [traffic.lm_head_fp8_bytes()] * max(K, W)
+        name = "lm_head argmax, 262144 x 2816 E4M3 + fp32 row scales, M=5"
     else:
         emb = synth.embedding(EMB_SEED, device=dev)
         am = torch.empty(M, dtype=torch.int32, device=dev)
@@ -539,6 +547,70 @@ def run_sweep(args):
     return None
 
 
+def run_verify_fp8(args):
+    """The headline verify step with the FP8 lm_head in place of the bf16 one:
+    same 30-layer stack, inputs and draft recipe (drafts copy the FP8 head's
+    own argmax with probability 0.7). Returns one JSON line (tokens/s counting
+    accepted drafts + 1 per step, algorithmic HBM GB/s)."""
+    import torch
+
+    import fine_grained_moe_gb300 as fgm
+    import synth
+    from fine_grained_moe_gb300 import traffic
+
+    dev = torch.device("cuda", 0)
+    torch.cuda.set_device(dev)
+    fgm.lib()
+    fgm.select_path(fgm.PATH_FUSED if args.path == "fused" else fgm.PATH_STAGED)
+    layers, emb, xs = make_workload(dev)
+    emb_q, emb_s = synth.embedding_fp8(emb)
+    del emb
+    torch.cuda.empty_cache()
+    arr = fgm.layers_array(layers)
+    ws = fgm.Workspace(dev)
+    uniq, drafts = [], []
+    trace = torch.empty((N_LAYERS, M, 8), dtype=torch.int32, device=dev)
+    for b, x in enumerate(xs):
+        fgm.moe_stack_fwd(layers, x, ids_trace=trace, ws=ws)
+        tr = trace.cpu()
+        uniq.append([len(torch.unique(tr[l])) for l in range(N_LAYERS)])
+        am = torch.empty(M, dtype=torch.int32, device=dev)
+        fgm.verify_step_fp8_head(layers, emb_q, emb_s, x, torch.zeros(GAMMA, dtype=torch.int32, device=dev),
+                                 argmax=am, ws=ws, _arr=arr)
+        drafts.append(synth.drafts(DRAFT_SEED0 + b, am.cpu()).to(dev))
+    nbytes = [traffic.step_bytes(u, fp8_lm_head=True) for u in uniq]
+    K, W = args.steps, args.warmup
+    outs = torch.zeros((K, 2), dtype=torch.int32, device=dev)
+    for i in range(W):
+        b = i % N_BATCHES
+        fgm.verify_step_fp8_head(layers, emb_q, emb_s, xs[b], drafts[b], ws=ws, _arr=arr)
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    with ClockSampler(dev.index) as clk:
+        e0.record()
+        for i in range(K):
+            b = i % N_BATCHES
+            fgm.verify_step_fp8_head(layers, emb_q, emb_s, xs[b], drafts[b], out=outs[i], ws=ws, _arr=arr)
+        e1.record()
+        torch.cuda.synchronize()
+    ms = e0.elapsed_time(e1)
+    tokens = int(outs[:, 0].sum().cpu()) + K
+    gbs = sum(nbytes[i % N_BATCHES] for i in range(K)) / (ms * 1e-3) / 1e9
+    peak, kind = measured_peaks()
+    clocks = clk.summary()
+    return {"case": "verify_fp8", "path": args.path,
+            "workload": "full verify step, M=5 (gamma=4), Zipf s=1.1, 30 layers, "
+                        "262144x2816 E4M3 lm_head with fp32 row scales",
+            "steps": K, "warmup": W, "tokens_per_s": round(tokens / (ms * 1e-3), 2),
+            "ms_per_step": round(ms / K, 4), "accepted_per_step": round((tokens - K) / K, 3),
+            "algorithmic_bytes_per_step": int(statistics.mean(nbytes)),
+            "hbm_gbs": round(gbs, 1), "frac_of_peak": round(gbs / peak, 4), "peak": peak, "peak_kind": kind,
+            "launches_per_step": 4 if args.path == "fused" else 2 + N_LAYERS * 5 + 3,
+            "clocks": {"sm_mhz": clocks["sm_mhz"], "sm_max_mhz": clocks["sm_max_mhz"],
+                       "reasons": clocks["reasons"]},
+            "status": ws.status()}
+
+
 # ---------------------------------------------------------------- reference arm
 def run_reference(args, rank, world):
     """The oracle as the reference arm: one full step on batch 0 fixes the
@@ -611,9 +683,11 @@ def main():
                     help="persistent kernel (default) or one launch per stage")
     ap.add_argument("--phase-trace", metavar="PATH", default=None,
                     help="after timing, run one traced step and write a per-phase summary to PATH")
-    ap.add_argument("--case", choices=("verify", "layer", "lm_head", "sweep"), default="verify",
-                    help="verify: the headline step; layer / lm_head: one stage alone (profiling); "
-                         "sweep: the verify step over M = 1..8 and Zipf s in {0, 1.1, 2} (one line each)")
+    ap.add_argument("--case", choices=("verify", "layer", "lm_head", "lm_head_fp8", "verify_fp8", "sweep"),
+                    default="verify",
+                    help="verify: the headline step; layer / lm_head / lm_head_fp8: one stage alone "
+                         "(profiling); verify_fp8: the step with the FP8 lm_head; sweep: the verify step "
+                         "over M = 1..8 and Zipf s in {0, 1.1, 2} (one line each)")
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")
@@ -628,6 +702,8 @@ def main():
             line = run_reference(args, rank, world)
         elif args.case == "sweep":
             line = run_sweep(args)
+        elif args.case == "verify_fp8":
+            line = run_verify_fp8(args)
         elif args.case != "verify":
             line = run_case(args)
         else:

@@ -64,9 +64,11 @@ def lib() -> ctypes.CDLL:
             "fgm_moe_layer_fwd_noalloc": (ci, [LP, vp, vp, ci, vp, vp, vp]),
             "fgm_moe_stack_fwd": (ci, [LP, ci, vp, vp, ci, vp, vp, sz, vp]),
             "fgm_lm_head_argmax": (ci, [vp, i64, vp, ci, vp, vp, vp, sz, vp]),
+            "fgm_lm_head_argmax_fp8": (ci, [vp, vp, i64, vp, ci, vp, vp, vp, sz, vp]),
             "fgm_spec_verify": (ci, [vp, vp, ci, vp, vp]),
             "fgm_verify_step": (ci, [LP, ci, vp, i64, vp, vp, ci, vp, vp, vp, sz, vp]),
             "fgm_verify_step_host": (ci, [LP, ci, vp, i64, vp, vp, ci, vp, vp, sz, vp]),
+            "fgm_verify_step_fp8_head": (ci, [LP, ci, vp, vp, i64, vp, vp, ci, vp, vp, vp, sz, vp]),
             "fgm_read_status": (ci, [vp, sz, ci, vp, vp]),
             "fgm_select_path": (ci, [ci]),
             "fgm_set_phase_trace": (ci, [vp, sz]),
@@ -270,6 +272,28 @@ def lm_head_argmax(emb: torch.Tensor, h: torch.Tensor, argmax: torch.Tensor | No
     return argmax
 
 
+def _fp8_rows(emb_q: torch.Tensor, emb_s: torch.Tensor) -> int:
+    if emb_q.dim() != 2 or emb_q.shape[1] != HIDDEN or emb_q.dtype != torch.uint8:
+        raise FgmError(f"expected uint8 [V, {HIDDEN}] E4M3 codes, got {tuple(emb_q.shape)} {emb_q.dtype}")
+    if emb_s.dtype != torch.float32 or tuple(emb_s.shape) != (emb_q.shape[0],):
+        raise FgmError(f"expected fp32 [{emb_q.shape[0]}] row scales, got {tuple(emb_s.shape)} {emb_s.dtype}")
+    return int(emb_q.shape[0])
+
+
+def lm_head_argmax_fp8(emb_q: torch.Tensor, emb_s: torch.Tensor, h: torch.Tensor,
+                       argmax: torch.Tensor | None = None, maxlogit: torch.Tensor | None = None,
+                       ws: Workspace | None = None, stream=None) -> torch.Tensor:
+    """argmax_v emb_s[v] * (e4m3(emb_q[v]) . h[t]) for each of the M rows of bf16 h;
+    returns int32 [M]."""
+    M = _m(h)
+    V = _fp8_rows(emb_q, emb_s)
+    argmax = torch.empty(M, dtype=torch.int32, device=h.device) if argmax is None else argmax
+    ws = _ws(ws, h.device)
+    _check(lib().fgm_lm_head_argmax_fp8(_ptr(emb_q), _ptr(emb_s), V, _ptr(h), M, _ptr(argmax),
+                                        _ptr(maxlogit), ws.ptr, ws.nbytes, _stream(stream)))
+    return argmax
+
+
 def spec_verify(target: torch.Tensor, draft: torch.Tensor, out: torch.Tensor | None = None,
                 stream=None) -> torch.Tensor:
     """Greedy acceptance; returns int32 [2] = {accepted drafts, next token}."""
@@ -292,6 +316,23 @@ def verify_step(layers, emb: torch.Tensor, x: torch.Tensor, draft: torch.Tensor 
     _check(lib().fgm_verify_step(arr, len(arr), _ptr(emb), int(emb.shape[0]), _ptr(x),
                                  _ptr(draft) if M > 1 else None, M, _ptr(argmax), _ptr(out), ws.ptr,
                                  ws.nbytes, _stream(stream)))
+    return out
+
+
+def verify_step_fp8_head(layers, emb_q: torch.Tensor, emb_s: torch.Tensor, x: torch.Tensor,
+                         draft: torch.Tensor | None, out: torch.Tensor | None = None,
+                         argmax: torch.Tensor | None = None, ws: Workspace | None = None, stream=None,
+                         _arr=None) -> torch.Tensor:
+    """verify_step with the FP8 lm_head (E4M3 rows emb_q, fp32 row scales emb_s);
+    returns int32 [2] = {accepted drafts, next token} on the device."""
+    M = _m(x)
+    V = _fp8_rows(emb_q, emb_s)
+    out = torch.empty(2, dtype=torch.int32, device=x.device) if out is None else out
+    ws = _ws(ws, x.device)
+    arr = _layers_array(layers) if _arr is None else _arr
+    _check(lib().fgm_verify_step_fp8_head(arr, len(arr), _ptr(emb_q), _ptr(emb_s), V, _ptr(x),
+                                          _ptr(draft) if M > 1 else None, M, _ptr(argmax), _ptr(out),
+                                          ws.ptr, ws.nbytes, _stream(stream)))
     return out
 
 

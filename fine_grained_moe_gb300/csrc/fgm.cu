@@ -1,6 +1,6 @@
 // C ABI of the library (declared in include/fgm.h): argument validation,
 // workspace carving and launch sequencing. Every stage of the step runs in
-// the CUDA kernels of basic_kernels.cuh / fused_step.cuh.
+// the CUDA kernels of basic_kernels.cuh / fused_step.cuh / lm_head_fp8.cuh.
 #include <stdarg.h>
 #include <stdio.h>
 #include <string.h>
@@ -9,6 +9,7 @@
 
 #include "basic_kernels.cuh"
 #include "fused_step.cuh"
+#include "lm_head_fp8.cuh"
 
 namespace fgm {
 namespace {
@@ -281,6 +282,32 @@ int check_vocab(const uint16_t *emb, int64_t V)
     return FGM_OK;
 }
 
+int check_vocab_fp8(const uint8_t *emb_q, const float *emb_s, int64_t V)
+{
+    if (!emb_q || !aligned16(emb_q))
+        return fail(FGM_ERR_INVALID_ARG, "emb_q is NULL or not 16-byte aligned");
+    if (!emb_s || (reinterpret_cast<uintptr_t>(emb_s) & 3u))
+        return fail(FGM_ERR_INVALID_ARG, "emb_s is NULL or not 4-byte aligned");
+    if (V < 1 || V > 0x7FFFFFFFLL)
+        return fail(FGM_ERR_INVALID_ARG, "V = %lld outside [1, 2^31)", (long long)V);
+    return FGM_OK;
+}
+
+// FP8 lm_head partials for the bf16 rows hb, then the cross-CTA argmax (and,
+// with draft/out, greedy acceptance).
+int run_lmhead_fp8(const uint8_t *emb_q, const float *emb_s, int64_t V, const uint16_t *hb, int M,
+                   int32_t *argmax, float *maxlogit, const int32_t *draft, int32_t *out, const Ws &w,
+                   int sms, cudaStream_t st)
+{
+    const int G = fp8head::grid_for(V, sms);
+    fp8head::k_lmhead_fp8<<<G, fp8head::kThreads, 0, st>>>(emb_q, emb_s, static_cast<int>(V), hb, M, w.part_val,
+                                                         w.part_idx);
+    FGM_CHECK_LAUNCH();
+    k_argmax_final<<<1, 256, 0, st>>>(w.part_val, w.part_idx, G, M, argmax, maxlogit, draft, out, w.status);
+    FGM_CHECK_LAUNCH();
+    return FGM_OK;
+}
+
 // The stack on w.h (already holding the input), layer by layer.
 int run_stack(const fgm_layer *layers, int n_layers, int M, const Ws &w, int32_t *ids_trace,
               cudaStream_t st)
@@ -433,6 +460,53 @@ int fgm_lm_head_argmax(const uint16_t *emb, int64_t V, const uint16_t *h, int M,
                                       w.status);
     FGM_CHECK_LAUNCH();
     return FGM_OK;
+}
+
+int fgm_lm_head_argmax_fp8(const uint8_t *emb_q, const float *emb_s, int64_t V, const uint16_t *h, int M,
+                           int32_t *argmax, float *maxlogit, void *ws, size_t ws_bytes, void *stream)
+{
+    int sms = 0;
+    FGM_TRY(check_m(M));
+    FGM_TRY(check_vocab_fp8(emb_q, emb_s, V));
+    if (!h || !aligned16(h) || !argmax)
+        return fail(FGM_ERR_INVALID_ARG, "h/argmax NULL or h not 16-byte aligned");
+    FGM_TRY(check_ws(ws, ws_bytes, M, V));
+    FGM_TRY(device_ready(&sms));
+    return run_lmhead_fp8(emb_q, emb_s, V, h, M, argmax, maxlogit, nullptr, nullptr, ws_carve(ws), sms,
+                          static_cast<cudaStream_t>(stream));
+}
+
+int fgm_verify_step_fp8_head(const fgm_layer *layers, int n_layers, const uint8_t *emb_q, const float *emb_s,
+                             int64_t V, const uint16_t *x, const int32_t *draft, int M, int32_t *argmax,
+                             int32_t *out, void *ws, size_t ws_bytes, void *stream)
+{
+    int sms = 0;
+    FGM_TRY(check_m(M));
+    FGM_TRY(check_layers(layers, n_layers));
+    FGM_TRY(check_vocab_fp8(emb_q, emb_s, V));
+    if (!x || !aligned16(x) || !out || (M > 1 && !draft))
+        return fail(FGM_ERR_INVALID_ARG, "x/out NULL, x misaligned, or draft NULL with M > 1");
+    FGM_TRY(check_ws(ws, ws_bytes, M, V));
+    FGM_TRY(device_ready(&sms));
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    Ws w = ws_carve(ws);
+    // the stack leaves the final fp32 residual stream in w.h
+    if (g_path == FGM_PATH_FUSED) {
+        fused::Params prm = fused_params(fused::kModeStack, M, w);
+        for (int l = 0; l < n_layers; ++l)
+            prm.layers[l] = layers[l];
+        prm.n_layers = n_layers;
+        prm.x = x;
+        prm.y = w.hb;   // bf16 copy of h, overwritten by the final norm below
+        FGM_TRY(launch_fused(prm, st));
+    } else {
+        k_bf16_to_f32<<<8, 256, 0, st>>>(x, M * kH, w.h);
+        FGM_CHECK_LAUNCH();
+        FGM_TRY(run_stack(layers, n_layers, M, w, nullptr, st));
+    }
+    k_rmsnorm<<<M, 256, 0, st>>>(w.h, nullptr, w.hb);
+    FGM_CHECK_LAUNCH();
+    return run_lmhead_fp8(emb_q, emb_s, V, w.hb, M, argmax ? argmax : w.argmax, nullptr, draft, out, w, sms, st);
 }
 
 int fgm_spec_verify(const int32_t *target, const int32_t *draft, int M, int32_t *out, void *stream)

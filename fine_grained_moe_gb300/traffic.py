@@ -35,13 +35,19 @@ def lm_head_bytes(vocab: int = VOCAB, hidden: int = HIDDEN, weight_bytes: int = 
     return vocab * hidden * weight_bytes
 
 
+def lm_head_fp8_bytes(vocab: int = VOCAB, hidden: int = HIDDEN) -> int:
+    """The embedding as E4M3 codes plus one fp32 scale per row."""
+    return vocab * hidden + 4 * vocab
+
+
 def step_bytes(unique_per_layer, *, vocab: int = VOCAB, with_lm_head: bool = True,
-               n_shared: int = 1, with_bias: bool = True) -> int:
+               n_shared: int = 1, with_bias: bool = True, fp8_lm_head: bool = False) -> int:
     """Unique bytes of one step: for each layer the router and (unique routed +
-    shared) experts; then the bf16 tied embedding once."""
+    shared) experts; then the tied embedding once (bf16, or E4M3 with row
+    scales)."""
     total = 0
     for u in unique_per_layer:
         total += (int(u) + n_shared) * expert_bytes() + router_bytes(with_bias=with_bias)
     if with_lm_head:
-        total += lm_head_bytes(vocab)
+        total += lm_head_fp8_bytes(vocab) if fp8_lm_head else lm_head_bytes(vocab)
     return total

@@ -161,6 +161,24 @@ int fgm_moe_stack_fwd(const fgm_layer *layers, int n_layers, const uint16_t *x, 
 int fgm_lm_head_argmax(const uint16_t *emb, int64_t V, const uint16_t *h, int M, int32_t *argmax,
                        float *maxlogit, void *ws, size_t ws_bytes, void *stream);
 
+/* FP8 lm_head fused with argmax: the tied embedding stored as E4M3 codes with
+ * one fp32 scale per row (the expert weights' format),
+ *   z_{t,v} = emb_s[v] * sum_j e4m3(emb_q[v][j]) * h[t][j]
+ * (fp32 accumulation), argmax over v with ties to the lower index. Half the
+ * bytes of fgm_lm_head_argmax. Source: "llm-decoding" §"Lever 1: fewer bytes
+ * (FP8 weights)" (every weight stored in 8 bits) and §"First principles:
+ * compute-bound or memory-bound?" (the BF16 lm_head is a fifth of the bytes).
+ *  emb_q     uint8 [V][2816] E4M3 codes (16-byte aligned), 1 <= V < 2^31
+ *  emb_s     fp32 [V] row scales (4-byte aligned)
+ *  h         bf16 [M][2816] final hidden states (16-byte aligned)
+ *  argmax    int32 [M] output
+ *  maxlogit  fp32 [M] or NULL: the winning logit
+ * A row holding the NaN code gives NaN logits, which never win; if every
+ * logit of a token is NaN its argmax is 0 and FGM_STATUS_NONFINITE_LOGITS is
+ * raised. */
+int fgm_lm_head_argmax_fp8(const uint8_t *emb_q, const float *emb_s, int64_t V, const uint16_t *h, int M,
+                           int32_t *argmax, float *maxlogit, void *ws, size_t ws_bytes, void *stream);
+
 /* Greedy acceptance of gamma = M - 1 drafted tokens: a = largest j <= gamma
  * with draft[0..j-1] == target[0..j-1]; out = {a, target[a]} (the accepted
  * count and the token emitted after the accepted drafts). Source:
@@ -183,6 +201,14 @@ int fgm_spec_verify(const int32_t *target, const int32_t *draft, int M, int32_t 
 int fgm_verify_step(const fgm_layer *layers, int n_layers, const uint16_t *emb, int64_t V,
                     const uint16_t *x, const int32_t *draft, int M, int32_t *argmax, int32_t *out,
                     void *ws, size_t ws_bytes, void *stream);
+
+/* fgm_verify_step with the FP8 lm_head of fgm_lm_head_argmax_fp8 in place of
+ * the bf16 one (same stack, final norm and acceptance).
+ *  emb_q    uint8 [V][2816] E4M3 codes;  emb_s  fp32 [V] row scales
+ *  other arguments as fgm_verify_step */
+int fgm_verify_step_fp8_head(const fgm_layer *layers, int n_layers, const uint8_t *emb_q, const float *emb_s,
+                             int64_t V, const uint16_t *x, const int32_t *draft, int M, int32_t *argmax,
+                             int32_t *out, void *ws, size_t ws_bytes, void *stream);
 
 /* fgm_verify_step with HOST input and output buffers: copies x_host
  * (bf16 [M][2816]) and draft_host (int32 [M-1]) into the workspace, runs the

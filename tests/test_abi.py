@@ -63,6 +63,14 @@ def test_argument_checks_fail_before_launch(lib):
     assert lib.fgm_lm_head_argmax(buf, 0, buf, 1, buf, None, buf, 4096, None) == -1
     assert lib.fgm_lm_head_argmax(ctypes.c_void_p(ctypes.addressof(buf) + 1), 10, buf, 1, buf, None,
                                   buf, 4096, None) == -1
+    # FP8 lm_head: NULL or misaligned codes / scales, V out of range
+    assert lib.fgm_lm_head_argmax_fp8(None, buf, 10, buf, 1, buf, None, buf, 4096, None) == -1
+    assert lib.fgm_lm_head_argmax_fp8(buf, ctypes.c_void_p(ctypes.addressof(buf) + 2), 10, buf, 1, buf,
+                                      None, buf, 4096, None) == -1
+    assert lib.fgm_lm_head_argmax_fp8(buf, buf, 0, buf, 1, buf, None, buf, 4096, None) == -1
+    assert b"V = 0" in lib.fgm_last_error()
+    assert lib.fgm_verify_step_fp8_head(arr, 1, buf, buf, 10, buf, None, 2, None, buf, buf, 4096,
+                                        None) == -1
     # spec_verify: draft missing with M > 1
     assert lib.fgm_spec_verify(buf, None, 3, buf, None) == -1
     # workspace too small / misaligned

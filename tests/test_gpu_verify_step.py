@@ -43,7 +43,7 @@ def setup(request):
     am, mx, mg = oracle.lm_head(bf16_bits(emb), oracle.bf16_to_f64(hn_bits))
     draft = synth.drafts(33, am)
     yield dict(fgm=fgm, layers=layers, emb=emb, x=x, h_ref=h, traj=traj, host=host, am=am, mg=mg,
-               draft=draft, ws=fgm.Workspace("cuda"))
+               draft=draft, hn=oracle.bf16_to_f64(hn_bits), ws=fgm.Workspace("cuda"))
     fgm.select_path(prev)
 
 
@@ -57,15 +57,20 @@ def test_stack_30_layers(setup):
     assert s["ws"].status() == 0
 
 
-def _comparable_prefix(s):
-    """Positions whose whole trajectory matched the oracle and whose argmax is
-    decided by more than the margin."""
+def _matched_positions(s):
+    """Positions whose routing matched the oracle's in every layer."""
     trace = torch.empty((N_LAYERS, M, 8), dtype=torch.int32, device="cuda")
     y = s["fgm"].moe_stack_fwd(s["layers"], s["x"], ids_trace=trace, ws=s["ws"])
     torch.cuda.synchronize()
-    full = set(_compare_stack(trace.cpu().numpy(), y, s["h_ref"], s["traj"], s["host"], M))
-    ok = [t in full and s["mg"][t] > MARGIN for t in range(M)]
-    return ok
+    return set(_compare_stack(trace.cpu().numpy(), y, s["h_ref"], s["traj"], s["host"], M))
+
+
+def _comparable_prefix(s, margins=None):
+    """Positions whose whole trajectory matched the oracle and whose argmax is
+    decided by more than the margin (the bf16 head's unless given)."""
+    full = _matched_positions(s)
+    mg = s["mg"] if margins is None else margins
+    return [t in full and mg[t] > MARGIN for t in range(M)]
 
 
 def test_verify_step_accept_and_next(setup):
@@ -143,4 +148,29 @@ def test_stack_and_verify_m8(setup):
         if mg[t] > MARGIN:
             assert gam[t] == am_ref[t], (t, gam[t], am_ref[t])
     assert tuple(out.cpu().tolist()) == oracle.spec_verify(gam, draft.numpy())
+    assert s["ws"].status() == 0
+
+
+def test_verify_step_fp8_head(setup):
+    """The same step with the FP8 lm_head: the embedding's E4M3 copy read by
+    the FP8 kernel, against the oracle's FP8 head on the oracle's own final
+    normed hidden rows; drafts copy that head's argmax with probability 0.7."""
+    s = setup
+    fgm = s["fgm"]
+    q, sc = synth.embedding_fp8(s["emb"])
+    am_ref, _, mg_ref = oracle.lm_head_fp8(q.cpu().numpy(), sc.cpu().numpy(), s["hn"])
+    draft = synth.drafts(34, am_ref)
+    am = torch.empty(M, dtype=torch.int32, device="cuda")
+    out = fgm.verify_step_fp8_head(s["layers"], q, sc, s["x"], draft.cuda(), argmax=am, ws=s["ws"])
+    torch.cuda.synchronize()
+    ok = _comparable_prefix(s, mg_ref)
+    gam = am.cpu().numpy()
+    for t in range(M):
+        if ok[t]:
+            assert gam[t] == am_ref[t], (t, gam[t], am_ref[t])
+    a, nxt = out.cpu().tolist()
+    assert (a, nxt) == oracle.spec_verify(gam, draft.numpy())
+    a_ref, nxt_ref = oracle.spec_verify(am_ref, draft.numpy())
+    if all(ok[:a_ref + 1]):
+        assert (a, nxt) == (a_ref, nxt_ref)
     assert s["ws"].status() == 0

@@ -50,3 +50,15 @@ def test_fp8_step_sizes():
     assert traffic.step_bytes([35] * 30) / 1e9 == pytest.approx(7.94, abs=0.01)
     # one C0-size layer, no lm_head
     assert traffic.step_bytes([8], with_lm_head=False, with_bias=False) == 9 * 5964288 + 720896
+
+
+def test_fp8_lm_head_halves_the_embedding_bytes():
+    # 262,144 x 2816 codes + one fp32 scale per row; the page's 738M-parameter
+    # projection at one byte each (§"Where the 7.36 GB goes")
+    g = _golden()
+    b = traffic.lm_head_fp8_bytes()
+    assert b == 262144 * 2816 + 4 * 262144
+    assert (b - 4 * 262144) / 1e6 == pytest.approx(g["lm_head_params_m"], abs=0.5)
+    assert traffic.lm_head_bytes() - b == 262144 * (2816 - 4)
+    assert (traffic.step_bytes([20] * 30, fp8_lm_head=True)
+            == traffic.step_bytes([20] * 30) - traffic.lm_head_bytes() + b)
