@@ -89,6 +89,7 @@ int device_ready(int *sms)
             FGM_SMEM(k_lmhead_basic<6>, 6 * kH * 4);
             FGM_SMEM(k_lmhead_basic<7>, 7 * kH * 4);
             FGM_SMEM(k_lmhead_basic<8>, 8 * kH * 4);
+            FGM_SMEM(fp8head::k_lmhead_fp8, fp8head::kSmemBytes);
 #undef FGM_SMEM
             const void *kerns[4] = {reinterpret_cast<const void *>(fused::k_fused<2, false>),
                                     reinterpret_cast<const void *>(fused::k_fused<3, false>),
@@ -300,7 +301,7 @@ int run_lmhead_fp8(const uint8_t *emb_q, const float *emb_s, int64_t V, const ui
                    int sms, cudaStream_t st)
 {
     const int G = fp8head::grid_for(V, sms);
-    fp8head::k_lmhead_fp8<<<G, fp8head::kThreads, 0, st>>>(emb_q, emb_s, static_cast<int>(V), hb, M, w.part_val,
+    fp8head::k_lmhead_fp8<<<G, fp8head::kThreads, fp8head::kSmemBytes, st>>>(emb_q, emb_s, static_cast<int>(V), hb, M, w.part_val,
                                                          w.part_idx);
     FGM_CHECK_LAUNCH();
     k_argmax_final<<<1, 256, 0, st>>>(w.part_val, w.part_idx, G, M, argmax, maxlogit, draft, out, w.status);

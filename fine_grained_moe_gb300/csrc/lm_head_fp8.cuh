@@ -10,10 +10,9 @@
 // Design (one pass over q at HBM speed):
 //  * One CTA per SM, 16 warps. Warp w owns whole 16-row tiles of the
 //    vocabulary, tiles w, w + W, ... (W = warps in the grid), and reads each
-//    tile's 45 KB once with 16-byte streaming loads that skip L1. A lane reads
-//    16 bytes of row g = lane / 4 and of row g + 8 per 64-byte K-block, so four
-//    lanes cover 64 contiguous bytes of a row and a warp step touches full
-//    32-byte sectors only.
+//    tile's 45 KB once. A lane copies 16 bytes of row g = lane / 4 and of row
+//    g + 8 per 64-byte K-block, so four lanes cover 64 contiguous bytes of a
+//    row and a warp step touches full 32-byte sectors only.
 //  * Products on the tensor cores: mma.sync m16n8k16 with f16 operands and
 //    fp32 accumulation. The E4M3 codes become f16 through the hardware
 //    conversion (every E4M3 value is exact in f16); the 8 MMA columns are the
@@ -26,8 +25,11 @@
 //    power of two 2^s so that its largest |h| lies in [2^14, 2^15): bf16
 //    inputs of any magnitude fit f16's range, the scaling is exact, and the
 //    logit is unscaled exactly by 2^-s in the epilogue.
-//  * Loads run one pipeline step (4 K-blocks, 4 KB per warp) ahead of the
-//    products, including across tile boundaries, so ~64 KB per SM is in flight.
+//  * Copies run through a per-warp ring in shared memory: each lane issues
+//    cp.async (L1 bypassed) for its own bytes kDepth - 1 = 4 steps of 2 KB
+//    per warp ahead of the products, across tile boundaries too, so 128 KB
+//    per SM is in flight without holding registers (a register double buffer
+//    held 64 KB and left the loads latency-bound).
 //  * Epilogue per tile: row scale, unscale, running (max, lowest index) per
 //    token; then a warp and CTA reduction to one partial per CTA, reduced
 //    across CTAs by k_argmax_final.
@@ -44,18 +46,32 @@ constexpr int kRows = 16;                  // vocabulary rows per warp tile (the
 constexpr int kPitch = kH + 8;             // f16 per token row in shared memory (16-byte pad)
 constexpr int kBlock = 64;                 // K elements per lane quad and K-block (4 lanes x 16 bytes)
 constexpr int kBlocks = kH / kBlock;       // 44 K-blocks per row
-constexpr int kGroup = 4;                  // K-blocks per pipeline step
-constexpr int kSteps = kBlocks / kGroup;   // 11 steps per tile
+constexpr int kGroup = 2;                  // K-blocks per pipeline step
+constexpr int kSteps = kBlocks / kGroup;   // 22 steps per tile
+constexpr int kDepth = 5;                  // ring stages per warp (kDepth - 1 steps in flight)
+constexpr int kStageVecs = 2 * kGroup * 32;                      // 16-byte vectors per stage (2 KB)
+constexpr int kHsBytes = kMaxM * kPitch * 2;                     // f16 hidden rows
+constexpr int kSmemBytes = kHsBytes + kWarps * kDepth * kStageVecs * 16;  // dynamic shared memory
 static_assert(kH % (kBlock * kGroup) == 0, "hidden width must split into whole pipeline steps");
+static_assert(kHsBytes % 16 == 0, "the ring must start on a 16-byte boundary");
 
-// 16 bytes of a stream read once: no L1 allocation, L2 fetches 256-byte spans.
-__device__ __forceinline__ uint4 ld_stream16(const uint8_t *p)
+__device__ __forceinline__ uint32_t smem_u32(const void *p)
 {
-    uint4 v;
-    asm("ld.global.nc.L1::no_allocate.L2::256B.v4.u32 {%0, %1, %2, %3}, [%4];"
-        : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
-        : "l"(p));
-    return v;
+    return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+
+// 16 bytes global -> shared, bypassing L1; L2 fetches the surrounding 256 bytes.
+__device__ __forceinline__ void cp_async16(uint32_t dst, const uint8_t *src)
+{
+    asm volatile("cp.async.cg.shared.global.L2::256B [%0], [%1], 16;" ::"r"(dst), "l"(src) : "memory");
+}
+
+__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
+
+template <int N>
+__device__ __forceinline__ void cp_async_wait()
+{
+    asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory");
 }
 
 // Two E4M3 codes (low byte = lower k) to an f16x2 word (low half = lower k); exact.
@@ -82,7 +98,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                  const uint16_t *__restrict__ hb, int M, float *__restrict__ part_val,
                  int32_t *__restrict__ part_idx)
 {
-    __shared__ __align__(16) uint16_t hs[kMaxM * kPitch];   // f16 bits of h * 2^s, zero rows for t >= M
+    extern __shared__ __align__(16) uint8_t dsm[];          // [kHsBytes] hidden rows, then the rings
+    uint16_t *hs = reinterpret_cast<uint16_t *>(dsm);       // f16 bits of h * 2^s, zero rows for t >= M
     __shared__ unsigned amax_bits[kMaxM];
     __shared__ float up[kMaxM], down[kMaxM];                 // 2^s and 2^-s per token
     __shared__ float rv[kWarps][kMaxM];
@@ -128,10 +145,18 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     __syncthreads();
 
-    // 4. stream the tiles
+    // 4. stream the tiles through this warp's ring of kDepth stages. A stage
+    //    is one pipeline step of the warp's current tile: per lane kGroup
+    //    K-blocks of rows g and g + 8, 16 bytes each, copied by the lane
+    //    itself with cp.async; chunk j = 2 b + (row g + 8) of lane l sits at
+    //    ring[stage][j][l], so the lane's loads and copies are conflict-free.
+    //    Each lane reads back only its own copies, so the wait on its own
+    //    commit groups is all the synchronisation a stage needs.
     const int T = (V + kRows - 1) / kRows;
     const int W = gridDim.x * kWarps;
     const uint16_t *hrow = hs + g * kPitch + 16 * t;   // B operand: token g, this lane's 16 k per block
+    const uint4 *ring = reinterpret_cast<const uint4 *>(dsm + kHsBytes) + (size_t)warp * kDepth * kStageVecs;
+    const uint32_t ring_lane = smem_u32(ring + lane);
     float bv[2] = {-INFINITY, -INFINITY};               // tokens 2t, 2t + 1
     int32_t bi[2] = {0x7FFFFFFF, 0x7FFFFFFF};
 
@@ -141,59 +166,58 @@ __global__ void __launch_bounds__(kThreads, 1)
         pa = q + (size_t)r0 * kH + 16 * t;
         pb = q + (size_t)r1 * kH + 16 * t;
     };
-
-    int tile = blockIdx.x * kWarps + warp;
-    uint4 cur[kGroup][2], nxt[kGroup][2];
-    const uint8_t *pa = q, *pb = q;
-    if (tile < T) {
-        row_ptrs(tile, pa, pb);
+    // issue side: tile `it`, step `is` of the next stage to copy; once past the
+    // last tile it commits empty groups, so the wait below counts uniformly
+    int it = blockIdx.x * kWarps + warp, is = 0;
+    const uint8_t *ia = q, *ib = q;
+    if (it < T)
+        row_ptrs(it, ia, ib);
+    auto issue = [&](int slot) {
+        if (it < T) {
+            const uint32_t dst = ring_lane + static_cast<uint32_t>(slot * kStageVecs) * 16u;
 #pragma unroll
-        for (int b = 0; b < kGroup; ++b) {
-            cur[b][0] = ld_stream16(pa + b * kBlock);
-            cur[b][1] = ld_stream16(pb + b * kBlock);
+            for (int b = 0; b < kGroup; ++b) {
+                cp_async16(dst + (2 * b) * 32 * 16, ia + (is * kGroup + b) * kBlock);
+                cp_async16(dst + (2 * b + 1) * 32 * 16, ib + (is * kGroup + b) * kBlock);
+            }
+            if (++is == kSteps) {
+                is = 0;
+                it += W;
+                if (it < T)
+                    row_ptrs(it, ia, ib);
+            }
         }
-    }
-    while (tile < T) {
-        const int ntile = tile + W;
-        const uint8_t *na = pa, *nb = pb;
-        if (ntile < T)
-            row_ptrs(ntile, na, nb);
+        cp_async_commit();
+    };
+#pragma unroll
+    for (int d = 0; d < kDepth - 1; ++d)
+        issue(d);
+
+    int slot = 0;
+    for (int tile = blockIdx.x * kWarps + warp; tile < T; tile += W) {
         const int r0 = tile * kRows + g, r1 = r0 + 8;
         const float s0 = scale[min(r0, V - 1)], s1 = scale[min(r1, V - 1)];
         float c[4] = {0.0f, 0.0f, 0.0f, 0.0f};
 #pragma unroll
         for (int s = 0; s < kSteps; ++s) {
-            if (s + 1 < kSteps) {
-#pragma unroll
-                for (int b = 0; b < kGroup; ++b) {
-                    nxt[b][0] = ld_stream16(pa + ((s + 1) * kGroup + b) * kBlock);
-                    nxt[b][1] = ld_stream16(pb + ((s + 1) * kGroup + b) * kBlock);
-                }
-            } else if (ntile < T) {
-#pragma unroll
-                for (int b = 0; b < kGroup; ++b) {
-                    nxt[b][0] = ld_stream16(na + b * kBlock);
-                    nxt[b][1] = ld_stream16(nb + b * kBlock);
-                }
-            }
+            issue(slot == 0 ? kDepth - 1 : slot - 1);   // the stage consumed last (its reads are done)
+            cp_async_wait<kDepth - 1>();                // this lane's copies of stage `slot` landed
+            const uint4 *st = ring + slot * kStageVecs + lane;
 #pragma unroll
             for (int b = 0; b < kGroup; ++b) {
                 const int kb = s * kGroup + b;
+                const uint4 va = st[(2 * b) * 32], vb = st[(2 * b + 1) * 32];
                 const uint4 h0 = *reinterpret_cast<const uint4 *>(hrow + kb * kBlock);
                 const uint4 h1 = *reinterpret_cast<const uint4 *>(hrow + kb * kBlock + 8);
                 const uint32_t hw[8] = {h0.x, h0.y, h0.z, h0.w, h1.x, h1.y, h1.z, h1.w};
-                const uint32_t wa[4] = {cur[b][0].x, cur[b][0].y, cur[b][0].z, cur[b][0].w};
-                const uint32_t wb[4] = {cur[b][1].x, cur[b][1].y, cur[b][1].z, cur[b][1].w};
+                const uint32_t wa[4] = {va.x, va.y, va.z, va.w};
+                const uint32_t wb[4] = {vb.x, vb.y, vb.z, vb.w};
 #pragma unroll
                 for (int i = 0; i < 4; ++i)
                     mma_f16(c, e4m3x2_to_f16x2(wa[i]), e4m3x2_to_f16x2(wb[i]), e4m3x2_to_f16x2(wa[i] >> 16),
                             e4m3x2_to_f16x2(wb[i] >> 16), hw[2 * i], hw[2 * i + 1]);
             }
-#pragma unroll
-            for (int b = 0; b < kGroup; ++b) {
-                cur[b][0] = nxt[b][0];
-                cur[b][1] = nxt[b][1];
-            }
+            slot = slot + 1 == kDepth ? 0 : slot + 1;
         }
         // c[u]: row r0, token 2t + u; c[2 + u]: row r1, token 2t + u
 #pragma unroll
@@ -217,10 +241,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                 }
             }
         }
-        tile = ntile;
-        pa = na;
-        pb = nb;
     }
+    cp_async_wait<0>();   // nothing of this lane may be in flight when the CTA exits
 
     // 5. warp (lanes of equal t), then CTA
 #pragma unroll
