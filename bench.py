@@ -605,7 +605,7 @@ def run_verify_fp8(args):
             "ms_per_step": round(ms / K, 4), "accepted_per_step": round((tokens - K) / K, 3),
             "algorithmic_bytes_per_step": int(statistics.mean(nbytes)),
             "hbm_gbs": round(gbs, 1), "frac_of_peak": round(gbs / peak, 4), "peak": peak, "peak_kind": kind,
-            "launches_per_step": 4 if args.path == "fused" else 2 + N_LAYERS * 5 + 3,
+            "launches_per_step": 2 if args.path == "fused" else 1 + N_LAYERS * 5 + 1,
             "clocks": {"sm_mhz": clocks["sm_mhz"], "sm_max_mhz": clocks["sm_max_mhz"],
                        "reasons": clocks["reasons"]},
             "status": ws.status()}

@@ -22,6 +22,7 @@ constexpr int kShared = kE;            // index of the shared expert
 constexpr int kMaxSlots = kMaxM * kK + 1;  // distinct routed experts + shared
 constexpr int kMaxParts = 2048;        // lm_head per-CTA partials kept in the workspace
 constexpr float kEps = FGM_RMS_EPS;
+constexpr int kSyncLmHeadDone = 127;   // workspace sync word counting finished FP8 lm_head CTAs
 
 // Device scratch carved out of the caller's workspace (see ws_layout()).
 struct Ws {
@@ -43,7 +44,8 @@ struct Ws {
     int32_t *io_draft; // [8]
     int32_t *io_out;   // [2]
     int32_t *status;   // [1] FGM_STATUS_* bits
-    unsigned *sync;    // [128] [0] grid barrier, [1] exit count, [2 + s] completed activation rows of slot s
+    unsigned *sync;    // [128] [0] grid barrier, [1] exit count, [2 + s] completed activation rows of slot s,
+                       // [kSyncLmHeadDone] CTAs done in the FP8 lm_head
     uint8_t *xterms;   // [8][3][2816] E4M3 terms of the gate/up input of the current layer
     float *xscale;     // [8][11] their power-of-two scale per token and 256-wide K-slice
 };

@@ -89,7 +89,8 @@ int device_ready(int *sms)
             FGM_SMEM(k_lmhead_basic<6>, 6 * kH * 4);
             FGM_SMEM(k_lmhead_basic<7>, 7 * kH * 4);
             FGM_SMEM(k_lmhead_basic<8>, 8 * kH * 4);
-            FGM_SMEM(fp8head::k_lmhead_fp8, fp8head::kSmemBytes);
+            FGM_SMEM(fp8head::k_lmhead_fp8<false>, fp8head::kSmemBytes);
+            FGM_SMEM(fp8head::k_lmhead_fp8<true>, fp8head::kSmemBytes);
 #undef FGM_SMEM
             const void *kerns[4] = {reinterpret_cast<const void *>(fused::k_fused<2, false>),
                                     reinterpret_cast<const void *>(fused::k_fused<3, false>),
@@ -294,17 +295,31 @@ int check_vocab_fp8(const uint8_t *emb_q, const float *emb_s, int64_t V)
     return FGM_OK;
 }
 
-// FP8 lm_head partials for the bf16 rows hb, then the cross-CTA argmax (and,
-// with draft/out, greedy acceptance).
-int run_lmhead_fp8(const uint8_t *emb_q, const float *emb_s, int64_t V, const uint16_t *hb, int M,
+// FP8 lm_head argmax in one launch (and, with draft/out, greedy acceptance).
+// h: bf16 rows, or with `norm` the fp32 residual stream to normalise first.
+int run_lmhead_fp8(const uint8_t *emb_q, const float *emb_s, int64_t V, const void *h, bool norm, int M,
                    int32_t *argmax, float *maxlogit, const int32_t *draft, int32_t *out, const Ws &w,
                    int sms, cudaStream_t st)
 {
+    fp8head::Args a;
+    a.q = emb_q;
+    a.scale = emb_s;
+    a.V = static_cast<int>(V);
+    a.h = h;
+    a.M = M;
+    a.part_val = w.part_val;
+    a.part_idx = w.part_idx;
+    a.done = w.sync + kSyncLmHeadDone;
+    a.argmax = argmax;
+    a.maxlogit = maxlogit;
+    a.draft = draft;
+    a.out = out;
+    a.status = w.status;
     const int G = fp8head::grid_for(V, sms);
-    fp8head::k_lmhead_fp8<<<G, fp8head::kThreads, fp8head::kSmemBytes, st>>>(emb_q, emb_s, static_cast<int>(V), hb, M, w.part_val,
-                                                         w.part_idx);
-    FGM_CHECK_LAUNCH();
-    k_argmax_final<<<1, 256, 0, st>>>(w.part_val, w.part_idx, G, M, argmax, maxlogit, draft, out, w.status);
+    if (norm)
+        fp8head::k_lmhead_fp8<true><<<G, fp8head::kThreads, fp8head::kSmemBytes, st>>>(a);
+    else
+        fp8head::k_lmhead_fp8<false><<<G, fp8head::kThreads, fp8head::kSmemBytes, st>>>(a);
     FGM_CHECK_LAUNCH();
     return FGM_OK;
 }
@@ -473,7 +488,7 @@ int fgm_lm_head_argmax_fp8(const uint8_t *emb_q, const float *emb_s, int64_t V, 
         return fail(FGM_ERR_INVALID_ARG, "h/argmax NULL or h not 16-byte aligned");
     FGM_TRY(check_ws(ws, ws_bytes, M, V));
     FGM_TRY(device_ready(&sms));
-    return run_lmhead_fp8(emb_q, emb_s, V, h, M, argmax, maxlogit, nullptr, nullptr, ws_carve(ws), sms,
+    return run_lmhead_fp8(emb_q, emb_s, V, h, false, M, argmax, maxlogit, nullptr, nullptr, ws_carve(ws), sms,
                           static_cast<cudaStream_t>(stream));
 }
 
@@ -498,16 +513,15 @@ int fgm_verify_step_fp8_head(const fgm_layer *layers, int n_layers, const uint8_
             prm.layers[l] = layers[l];
         prm.n_layers = n_layers;
         prm.x = x;
-        prm.y = w.hb;   // bf16 copy of h, overwritten by the final norm below
+        prm.y = w.hb;   // bf16 copy of h (unused: the lm_head kernel normalises w.h itself)
         FGM_TRY(launch_fused(prm, st));
     } else {
         k_bf16_to_f32<<<8, 256, 0, st>>>(x, M * kH, w.h);
         FGM_CHECK_LAUNCH();
         FGM_TRY(run_stack(layers, n_layers, M, w, nullptr, st));
     }
-    k_rmsnorm<<<M, 256, 0, st>>>(w.h, nullptr, w.hb);
-    FGM_CHECK_LAUNCH();
-    return run_lmhead_fp8(emb_q, emb_s, V, w.hb, M, argmax ? argmax : w.argmax, nullptr, draft, out, w, sms, st);
+    return run_lmhead_fp8(emb_q, emb_s, V, w.h, true, M, argmax ? argmax : w.argmax, nullptr, draft, out, w, sms,
+                          st);
 }
 
 int fgm_spec_verify(const int32_t *target, const int32_t *draft, int M, int32_t *out, void *stream)

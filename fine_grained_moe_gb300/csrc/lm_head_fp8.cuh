@@ -31,10 +31,15 @@
 //    per SM is in flight without holding registers (a register double buffer
 //    held 64 KB and left the loads latency-bound).
 //  * Epilogue per tile: row scale, unscale, running (max, lowest index) per
-//    token; then a warp and CTA reduction to one partial per CTA, reduced
-//    across CTAs by k_argmax_final.
+//    token; then a warp and CTA reduction to one partial per CTA. The last
+//    CTA to finish (a completion count in the workspace) reduces the
+//    partials and applies greedy acceptance, so a call is one launch.
+//  * For the verify step the kernel also applies the final unit RMSNorm to
+//    the fp32 residual stream in its prologue (NORM), while the first ring
+//    stages are already streaming in.
 #pragma once
 
+#include "basic_kernels.cuh"
 #include "common.cuh"
 
 namespace fgm {
@@ -91,75 +96,54 @@ __device__ __forceinline__ void mma_f16(float (&c)[4], uint32_t a0, uint32_t a1,
         : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
 }
 
-// Per-CTA argmax partials over the rows this CTA's warps visit:
-// part_val/part_idx[blockIdx.x][t] for t < M (ties to the lower row).
-__global__ void __launch_bounds__(kThreads, 1)
-    k_lmhead_fp8(const uint8_t *__restrict__ q, const float *__restrict__ scale, int V,
-                 const uint16_t *__restrict__ hb, int M, float *__restrict__ part_val,
-                 int32_t *__restrict__ part_idx)
+// Arguments of one launch.
+struct Args {
+    const uint8_t *q;       // [V][2816] E4M3 codes
+    const float *scale;     // [V] row scales
+    int V;
+    const void *h;          // bf16 [M][2816] rows, or (NORM) the fp32 residual stream [M][2816]
+    int M;
+    float *part_val;        // [gridDim.x][8] per-CTA best logit
+    int32_t *part_idx;      // [gridDim.x][8] and its row
+    unsigned *done;         // CTAs finished; 0 between launches (the last CTA resets it)
+    int32_t *argmax;        // [M] output
+    float *maxlogit;        // [M] output or NULL
+    const int32_t *draft;   // [M - 1] drafts (used when out != NULL)
+    int32_t *out;           // [2] {accepted, next} or NULL
+    int32_t *status;        // FGM_STATUS_* bits
+};
+
+// One pass over the E4M3 rows: per-CTA argmax partials, then the last CTA to
+// finish reduces them (ties to the lower row) and, with `out`, applies greedy
+// acceptance. NORM: the lm_head input is bf16(RMSNorm(h)) of the fp32 rows
+// (unit gain, eps 1e-6), else the given bf16 rows.
+template <bool NORM>
+__global__ void __launch_bounds__(kThreads, 1) k_lmhead_fp8(const Args p)
 {
     extern __shared__ __align__(16) uint8_t dsm[];          // [kHsBytes] hidden rows, then the rings
     uint16_t *hs = reinterpret_cast<uint16_t *>(dsm);       // f16 bits of h * 2^s, zero rows for t >= M
+    __shared__ float rn[kMaxM];                              // NORM: 1 / rms of each row
     __shared__ unsigned amax_bits[kMaxM];
     __shared__ float up[kMaxM], down[kMaxM];                 // 2^s and 2^-s per token
     __shared__ float rv[kWarps][kMaxM];
     __shared__ int32_t ri[kWarps][kMaxM];
+    __shared__ int32_t s_arg[kMaxM];
+    __shared__ int s_last;
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int g = lane >> 2, t = lane & 3;
+    const int M = p.M, V = p.V;
+    const uint8_t *__restrict__ q = p.q;
 
-    // 1. largest finite |h| per token (non-negative floats order like their bits)
-    for (int tk = warp; tk < kMaxM; tk += kWarps) {
-        unsigned m = 0;
-        if (tk < M)
-            for (int k = lane; k < kH; k += 32) {
-                const float a = fabsf(bf16_to_f32(hb[(size_t)tk * kH + k]));
-                if (a < INFINITY)
-                    m = max(m, __float_as_uint(a));
-            }
-        m = __reduce_max_sync(0xFFFFFFFFu, m);
-        if (lane == 0)
-            amax_bits[tk] = m;
-    }
-    __syncthreads();
-    // 2. s = 141 - biased exponent of that max puts it in [2^14, 2^15); a zero or
-    //    subnormal max keeps s = 0. For finite bf16 maxima s >= -113; s <= 126
-    //    keeps 2^s and 2^-s normal floats
-    if (tid < kMaxM) {
-        const int ef = static_cast<int>(amax_bits[tid] >> 23);
-        int s = ef == 0 ? 0 : 141 - ef;
-        s = min(126, s);
-        up[tid] = __uint_as_float(static_cast<unsigned>(127 + s) << 23);
-        down[tid] = __uint_as_float(static_cast<unsigned>(127 - s) << 23);
-    }
-    __syncthreads();
-    // 3. h * 2^s to f16 in shared memory
-    for (int i = tid; i < kMaxM * (kH / 2); i += kThreads) {
-        const int tk = i / (kH / 2), k2 = i - tk * (kH / 2);
-        uint32_t w = 0;
-        if (tk < M) {
-            const float2 v = bf16x2_to_f32(*reinterpret_cast<const uint32_t *>(hb + (size_t)tk * kH + 2 * k2));
-            const __half2 hv = __floats2half2_rn(v.x * up[tk], v.y * up[tk]);
-            w = *reinterpret_cast<const uint32_t *>(&hv);
-        }
-        *reinterpret_cast<uint32_t *>(hs + tk * kPitch + 2 * k2) = w;
-    }
-    __syncthreads();
-
-    // 4. stream the tiles through this warp's ring of kDepth stages. A stage
-    //    is one pipeline step of the warp's current tile: per lane kGroup
-    //    K-blocks of rows g and g + 8, 16 bytes each, copied by the lane
-    //    itself with cp.async; chunk j = 2 b + (row g + 8) of lane l sits at
-    //    ring[stage][j][l], so the lane's loads and copies are conflict-free.
-    //    Each lane reads back only its own copies, so the wait on its own
-    //    commit groups is all the synchronisation a stage needs.
+    // Ring of this warp: kDepth stages. A stage is one pipeline step of the
+    // warp's current tile: per lane kGroup K-blocks of rows g and g + 8, 16
+    // bytes each, copied by the lane itself with cp.async; chunk j = 2 b +
+    // (row g + 8) of lane l sits at ring[stage][j][l], so the lane's copies
+    // and loads are conflict-free. Each lane reads back only its own copies,
+    // so the wait on its own commit groups is all a stage needs.
     const int T = (V + kRows - 1) / kRows;
     const int W = gridDim.x * kWarps;
-    const uint16_t *hrow = hs + g * kPitch + 16 * t;   // B operand: token g, this lane's 16 k per block
     const uint4 *ring = reinterpret_cast<const uint4 *>(dsm + kHsBytes) + (size_t)warp * kDepth * kStageVecs;
     const uint32_t ring_lane = smem_u32(ring + lane);
-    float bv[2] = {-INFINITY, -INFINITY};               // tokens 2t, 2t + 1
-    int32_t bi[2] = {0x7FFFFFFF, 0x7FFFFFFF};
-
     // rows g and g + 8 of tile tl (rows past the end read row V - 1 and are dropped)
     auto row_ptrs = [&](int tl, const uint8_t *&pa, const uint8_t *&pb) {
         const int r0 = min(tl * kRows + g, V - 1), r1 = min(tl * kRows + g + 8, V - 1);
@@ -189,9 +173,80 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         cp_async_commit();
     };
+    // the first stages stream in while the hidden rows are prepared
 #pragma unroll
     for (int d = 0; d < kDepth - 1; ++d)
         issue(d);
+
+    // lm_head input elements 2 k2, 2 k2 + 1 of token tk (tk < M)
+    auto hval2 = [&](int tk, int k2) -> float2 {
+        if constexpr (NORM) {
+            const float2 v = *reinterpret_cast<const float2 *>(static_cast<const float *>(p.h) + (size_t)tk * kH + 2 * k2);
+            return make_float2(bf16_to_f32(f32_to_bf16(v.x * rn[tk])), bf16_to_f32(f32_to_bf16(v.y * rn[tk])));
+        } else {
+            return bf16x2_to_f32(*reinterpret_cast<const uint32_t *>(static_cast<const uint16_t *>(p.h) +
+                                                                     (size_t)tk * kH + 2 * k2));
+        }
+    };
+    // 1. NORM: 1 / sqrt(mean(h^2) + eps) per token
+    if constexpr (NORM) {
+        for (int tk = warp; tk < M; tk += kWarps) {
+            const float *row = static_cast<const float *>(p.h) + (size_t)tk * kH;
+            float ss = 0.0f;
+            for (int k = lane; k < kH; k += 32)
+                ss += row[k] * row[k];
+            ss = warp_sum(ss);
+            if (lane == 0)
+                rn[tk] = 1.0f / sqrtf(ss / static_cast<float>(kH) + kEps);
+        }
+        __syncthreads();
+    }
+    // 2. largest finite |input| per token (non-negative floats order like their bits)
+    for (int tk = warp; tk < kMaxM; tk += kWarps) {
+        unsigned m = 0;
+        if (tk < M)
+            for (int k2 = lane; k2 < kH / 2; k2 += 32) {
+                const float2 v = hval2(tk, k2);
+                const float a = fabsf(v.x), b = fabsf(v.y);
+                if (a < INFINITY)
+                    m = max(m, __float_as_uint(a));
+                if (b < INFINITY)
+                    m = max(m, __float_as_uint(b));
+            }
+        m = __reduce_max_sync(0xFFFFFFFFu, m);
+        if (lane == 0)
+            amax_bits[tk] = m;
+    }
+    __syncthreads();
+    // 3. s = 141 - biased exponent of that max puts it in [2^14, 2^15); a zero or
+    //    subnormal max keeps s = 0. For finite bf16 maxima s >= -113; s <= 126
+    //    keeps 2^s and 2^-s normal floats
+    if (tid < kMaxM) {
+        const int ef = static_cast<int>(amax_bits[tid] >> 23);
+        int s = ef == 0 ? 0 : 141 - ef;
+        s = min(126, s);
+        up[tid] = __uint_as_float(static_cast<unsigned>(127 + s) << 23);
+        down[tid] = __uint_as_float(static_cast<unsigned>(127 - s) << 23);
+    }
+    __syncthreads();
+    // 4. input * 2^s to f16 in shared memory
+    for (int i = tid; i < kMaxM * (kH / 2); i += kThreads) {
+        const int tk = i / (kH / 2), k2 = i - tk * (kH / 2);
+        uint32_t w = 0;
+        if (tk < M) {
+            const float2 v = hval2(tk, k2);
+            const __half2 hv = __floats2half2_rn(v.x * up[tk], v.y * up[tk]);
+            w = *reinterpret_cast<const uint32_t *>(&hv);
+        }
+        *reinterpret_cast<uint32_t *>(hs + tk * kPitch + 2 * k2) = w;
+    }
+    __syncthreads();
+
+    // 5. stream the tiles through the ring
+    const uint16_t *hrow = hs + g * kPitch + 16 * t;   // B operand: token g, this lane's 16 k per block
+    const float *__restrict__ scale = p.scale;
+    float bv[2] = {-INFINITY, -INFINITY};               // tokens 2t, 2t + 1
+    int32_t bi[2] = {0x7FFFFFFF, 0x7FFFFFFF};
 
     int slot = 0;
     for (int tile = blockIdx.x * kWarps + warp; tile < T; tile += W) {
@@ -244,7 +299,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     cp_async_wait<0>();   // nothing of this lane may be in flight when the CTA exits
 
-    // 5. warp (lanes of equal t), then CTA
+    // 6. this CTA's partial: warp (lanes of equal t), then CTA
 #pragma unroll
     for (int o = 4; o < 32; o <<= 1)
 #pragma unroll
@@ -272,8 +327,56 @@ __global__ void __launch_bounds__(kThreads, 1)
                 v = rv[w][tid];
                 ix = ri[w][tid];
             }
-        part_val[blockIdx.x * kMaxM + tid] = v;
-        part_idx[blockIdx.x * kMaxM + tid] = ix;
+        p.part_val[blockIdx.x * kMaxM + tid] = v;
+        p.part_idx[blockIdx.x * kMaxM + tid] = ix;
+    }
+
+    // 7. the last CTA to finish reduces every CTA's partial
+    __syncthreads();
+    if (tid == 0) {
+        __threadfence();   // this CTA's partials before its count
+        s_last = atomicAdd(p.done, 1u) == gridDim.x - 1;
+    }
+    __syncthreads();
+    if (!s_last)
+        return;
+    __threadfence();
+    if (warp < M) {
+        float v = -INFINITY;
+        int32_t ix = 0x7FFFFFFF;
+        for (int c = lane; c < (int)gridDim.x; c += 32) {
+            const float ov = __ldcg(p.part_val + c * kMaxM + warp);
+            const int32_t oi = __ldcg(p.part_idx + c * kMaxM + warp);
+            if (better(ov, oi, v, ix)) {
+                v = ov;
+                ix = oi;
+            }
+        }
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) {
+            const float ov = __shfl_xor_sync(0xFFFFFFFFu, v, o);
+            const int32_t oi = __shfl_xor_sync(0xFFFFFFFFu, ix, o);
+            if (better(ov, oi, v, ix)) {
+                v = ov;
+                ix = oi;
+            }
+        }
+        if (lane == 0) {
+            if (ix == 0x7FFFFFFF) {   // every logit was NaN
+                ix = 0;
+                atomicOr(p.status, FGM_STATUS_NONFINITE_LOGITS);
+            }
+            s_arg[warp] = ix;
+            p.argmax[warp] = ix;
+            if (p.maxlogit)
+                p.maxlogit[warp] = v;
+        }
+    }
+    __syncthreads();
+    if (tid == 0) {
+        if (p.out)
+            accept_greedy(s_arg, p.draft, M, p.out);
+        *p.done = 0u;   // ready for the next launch on this workspace
     }
 }
 

@@ -175,7 +175,9 @@ int fgm_lm_head_argmax(const uint16_t *emb, int64_t V, const uint16_t *h, int M,
  *  maxlogit  fp32 [M] or NULL: the winning logit
  * A row holding the NaN code gives NaN logits, which never win; if every
  * logit of a token is NaN its argmax is 0 and FGM_STATUS_NONFINITE_LOGITS is
- * raised. */
+ * raised. One launch: its CTAs count themselves done in the workspace (a
+ * word fgm_workspace_init zeroes and the call leaves at zero), and the last
+ * one reduces the per-CTA partials. */
 int fgm_lm_head_argmax_fp8(const uint8_t *emb_q, const float *emb_s, int64_t V, const uint16_t *h, int M,
                            int32_t *argmax, float *maxlogit, void *ws, size_t ws_bytes, void *stream);
 
@@ -203,7 +205,9 @@ int fgm_verify_step(const fgm_layer *layers, int n_layers, const uint16_t *emb, 
                     void *ws, size_t ws_bytes, void *stream);
 
 /* fgm_verify_step with the FP8 lm_head of fgm_lm_head_argmax_fp8 in place of
- * the bf16 one (same stack, final norm and acceptance).
+ * the bf16 one (same stack, final norm and acceptance). Two launches: the
+ * stack, then the FP8 lm_head, which applies the final norm to the fp32
+ * residual stream itself and ends with the acceptance.
  *  emb_q    uint8 [V][2816] E4M3 codes;  emb_s  fp32 [V] row scales
  *  other arguments as fgm_verify_step */
 int fgm_verify_step_fp8_head(const fgm_layer *layers, int n_layers, const uint8_t *emb_q, const float *emb_s,

@@ -174,3 +174,15 @@ def test_verify_step_fp8_head(setup):
     if all(ok[:a_ref + 1]):
         assert (a, nxt) == (a_ref, nxt_ref)
     assert s["ws"].status() == 0
+
+
+def test_verify_step_fp8_head_m1(setup):
+    """M = 1 through the FP8 head: no drafts, the next token is the argmax."""
+    s = setup
+    fgm = s["fgm"]
+    q, sc = synth.embedding_fp8(s["emb"])
+    x1 = s["x"][:1].contiguous()
+    am = torch.empty(1, dtype=torch.int32, device="cuda")
+    out = fgm.verify_step_fp8_head(s["layers"], q, sc, x1, None, argmax=am, ws=s["ws"])
+    assert out.cpu().tolist() == [0, int(am.cpu()[0])]
+    assert s["ws"].status() == 0
