@@ -13,18 +13,21 @@
 //    tile's 45 KB once. A lane copies 16 bytes of row g = lane / 4 and of row
 //    g + 8 per 64-byte K-block, so four lanes cover 64 contiguous bytes of a
 //    row and a warp step touches full 32-byte sectors only.
-//  * Products on the tensor cores: mma.sync m16n8k16 with f16 operands and
-//    fp32 accumulation. The E4M3 codes become f16 through the hardware
-//    conversion (every E4M3 value is exact in f16); the 8 MMA columns are the
-//    tokens (absent tokens are zero). Within a K-block the lane's 16 bytes are
-//    four k16 slices: slice i takes bytes 4i..4i+3, the A fragment's k pairs
-//    (2t, 2t+1) and (2t+8, 2t+9) being bytes (4i, 4i+1) and (4i+2, 4i+3) of
-//    lane t's chunk. The B fragment maps k the same way (it depends on t only),
-//    so every product meets its own hidden element.
-//  * The hidden rows live in shared memory as f16, each token scaled by a
-//    power of two 2^s so that its largest |h| lies in [2^14, 2^15): bf16
-//    inputs of any magnitude fit f16's range, the scaling is exact, and the
-//    logit is unscaled exactly by 2^-s in the epilogue.
+//  * Products on the tensor cores as E4M3 x E4M3: mma.sync m16n8k32 with
+//    fp32 accumulation, the weight codes used as they are stored (no
+//    conversion in the loop). The 8 MMA columns are the tokens (absent tokens
+//    are zero). Within a K-block the lane's 16 bytes are two k32 slices:
+//    bytes 0..3 and 4..7 are the A fragment's k 4t..4t+3 and 4t+16..4t+19 of
+//    slice 0, bytes 8..15 those of slice 1; the B fragment maps k the same way
+//    (it depends on t only), so every product meets its own hidden element.
+//  * The hidden rows live in shared memory as two E4M3 terms per value. Each
+//    token is scaled by a power of two 2^s that puts its largest |h| in
+//    [2^7, 2^8); then t0 = e4m3(y) and t1 = e4m3(16 (y - t0)) represent a bf16
+//    y exactly (8 significant bits = 4 + 4) over the 2^13 below the maximum
+//    that matter. The two terms are two accumulators, combined and unscaled
+//    (exactly, by 2^-s) in the epilogue. A conversion of each weight to f16
+//    for an f16 MMA instead kept the ALU pipe half busy and the kernel at
+//    0.86 of the copy bandwidth.
 //  * Copies run through a per-warp ring in shared memory: each lane issues
 //    cp.async (L1 bypassed) for its own bytes kDepth - 1 = 4 steps of 2 KB
 //    per warp ahead of the products, across tile boundaries too, so 128 KB
@@ -48,17 +51,19 @@ namespace fp8head {
 constexpr int kThreads = 512;
 constexpr int kWarps = kThreads / 32;
 constexpr int kRows = 16;                  // vocabulary rows per warp tile (the MMA's M)
-constexpr int kPitch = kH + 8;             // f16 per token row in shared memory (16-byte pad)
-constexpr int kBlock = 64;                 // K elements per lane quad and K-block (4 lanes x 16 bytes)
+constexpr int kTerms = 2;                  // E4M3 terms per hidden value (exact for bf16 inputs)
+constexpr int kColPitch = kH + 64;         // bytes per (term, token) column in shared memory: a 64-byte
+                                           // offset between neighbouring tokens keeps B loads conflict-free
+constexpr int kBlock = 64;                 // K bytes per lane quad and K-block (4 lanes x 16 bytes)
 constexpr int kBlocks = kH / kBlock;       // 44 K-blocks per row
 constexpr int kGroup = 2;                  // K-blocks per pipeline step
 constexpr int kSteps = kBlocks / kGroup;   // 22 steps per tile
 constexpr int kDepth = 5;                  // ring stages per warp (kDepth - 1 steps in flight)
 constexpr int kStageVecs = 2 * kGroup * 32;                      // 16-byte vectors per stage (2 KB)
-constexpr int kHsBytes = kMaxM * kPitch * 2;                     // f16 hidden rows
+constexpr int kHsBytes = kTerms * kMaxM * kColPitch;             // hidden-row terms
 constexpr int kSmemBytes = kHsBytes + kWarps * kDepth * kStageVecs * 16;  // dynamic shared memory
 static_assert(kH % (kBlock * kGroup) == 0, "hidden width must split into whole pipeline steps");
-static_assert(kHsBytes % 16 == 0, "the ring must start on a 16-byte boundary");
+static_assert(kHsBytes % 16 == 0 && kColPitch % 128 == 64, "column layout");
 
 __device__ __forceinline__ uint32_t smem_u32(const void *p)
 {
@@ -79,21 +84,28 @@ __device__ __forceinline__ void cp_async_wait()
     asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory");
 }
 
-// Two E4M3 codes (low byte = lower k) to an f16x2 word (low half = lower k); exact.
-__device__ __forceinline__ uint32_t e4m3x2_to_f16x2(uint32_t two)
-{
-    const __half2_raw r = __nv_cvt_fp8x2_to_halfraw2(static_cast<__nv_fp8x2_storage_t>(two & 0xFFFFu), __NV_E4M3);
-    return static_cast<uint32_t>(r.x) | (static_cast<uint32_t>(r.y) << 16);
-}
-
-__device__ __forceinline__ void mma_f16(float (&c)[4], uint32_t a0, uint32_t a1, uint32_t a2, uint32_t a3,
-                                        uint32_t b0, uint32_t b1)
+// D += A (16 x 32, E4M3, row-major) x B (32 x 8, E4M3), fp32 accumulation.
+__device__ __forceinline__ void mma_e4m3(float (&c)[4], uint32_t a0, uint32_t a1, uint32_t a2, uint32_t a3,
+                                         uint32_t b0, uint32_t b1)
 {
     asm volatile(
-        "mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, "
+        "mma.sync.aligned.m16n8k32.row.col.f32.e4m3.e4m3.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, "
         "{%0,%1,%2,%3};"
         : "+f"(c[0]), "+f"(c[1]), "+f"(c[2]), "+f"(c[3])
         : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
+}
+
+// Nearest E4M3 codes of two floats (low byte = a), saturating at +-448.
+__device__ __forceinline__ uint32_t f32x2_to_e4m3x2(float a, float b)
+{
+    return static_cast<uint32_t>(__nv_cvt_float2_to_fp8x2(make_float2(a, b), __NV_SATFINITE, __NV_E4M3));
+}
+
+// The value of an E4M3 code pair as two floats (exact).
+__device__ __forceinline__ float2 e4m3x2_to_f32x2(uint32_t two)
+{
+    const __half2_raw r = __nv_cvt_fp8x2_to_halfraw2(static_cast<__nv_fp8x2_storage_t>(two & 0xFFFFu), __NV_E4M3);
+    return __half22float2(__half2(r));
 }
 
 // Arguments of one launch.
@@ -121,7 +133,7 @@ template <bool NORM>
 __global__ void __launch_bounds__(kThreads, 1) k_lmhead_fp8(const Args p)
 {
     extern __shared__ __align__(16) uint8_t dsm[];          // [kHsBytes] hidden rows, then the rings
-    uint16_t *hs = reinterpret_cast<uint16_t *>(dsm);       // f16 bits of h * 2^s, zero rows for t >= M
+    uint8_t *hs = dsm;   // [term][token][kColPitch] E4M3 terms of h * 2^s, zero for tokens >= M
     __shared__ float rn[kMaxM];                              // NORM: 1 / rms of each row
     __shared__ unsigned amax_bits[kMaxM];
     __shared__ float up[kMaxM], down[kMaxM];                 // 2^s and 2^-s per token
@@ -218,32 +230,40 @@ __global__ void __launch_bounds__(kThreads, 1) k_lmhead_fp8(const Args p)
             amax_bits[tk] = m;
     }
     __syncthreads();
-    // 3. s = 141 - biased exponent of that max puts it in [2^14, 2^15); a zero or
-    //    subnormal max keeps s = 0. For finite bf16 maxima s >= -113; s <= 126
-    //    keeps 2^s and 2^-s normal floats
+    // 3. s = 134 - biased exponent of that max puts it in [2^7, 2^8), below
+    //    E4M3's 448; a zero or subnormal max keeps s = 0. For finite maxima
+    //    s >= -120; s <= 126 keeps 2^s and 2^-s normal floats
     if (tid < kMaxM) {
         const int ef = static_cast<int>(amax_bits[tid] >> 23);
-        int s = ef == 0 ? 0 : 141 - ef;
+        int s = ef == 0 ? 0 : 134 - ef;
         s = min(126, s);
         up[tid] = __uint_as_float(static_cast<unsigned>(127 + s) << 23);
         down[tid] = __uint_as_float(static_cast<unsigned>(127 - s) << 23);
     }
     __syncthreads();
-    // 4. input * 2^s to f16 in shared memory
+    // 4. y = input * 2^s as two E4M3 terms, y = t0 + t1 / 16 with t0 = e4m3(y)
+    //    and t1 = e4m3(16 (y - t0)). A bf16 y has 8 significant bits, t0 holds
+    //    the top 4 and the remainder is a 4-bit multiple of y's ulp, so t1
+    //    holds it exactly while it stays in E4M3's normal range (|y| above
+    //    max * 2^-13; smaller values lose low bits, below 2^-13 of the row's
+    //    largest product)
     for (int i = tid; i < kMaxM * (kH / 2); i += kThreads) {
         const int tk = i / (kH / 2), k2 = i - tk * (kH / 2);
-        uint32_t w = 0;
+        uint32_t w0 = 0, w1 = 0;
         if (tk < M) {
             const float2 v = hval2(tk, k2);
-            const __half2 hv = __floats2half2_rn(v.x * up[tk], v.y * up[tk]);
-            w = *reinterpret_cast<const uint32_t *>(&hv);
+            const float y0 = v.x * up[tk], y1 = v.y * up[tk];
+            w0 = f32x2_to_e4m3x2(y0, y1);
+            const float2 d = e4m3x2_to_f32x2(w0);
+            w1 = f32x2_to_e4m3x2(16.0f * (y0 - d.x), 16.0f * (y1 - d.y));
         }
-        *reinterpret_cast<uint32_t *>(hs + tk * kPitch + 2 * k2) = w;
+        *reinterpret_cast<uint16_t *>(hs + tk * kColPitch + 2 * k2) = static_cast<uint16_t>(w0);
+        *reinterpret_cast<uint16_t *>(hs + (kMaxM + tk) * kColPitch + 2 * k2) = static_cast<uint16_t>(w1);
     }
     __syncthreads();
 
     // 5. stream the tiles through the ring
-    const uint16_t *hrow = hs + g * kPitch + 16 * t;   // B operand: token g, this lane's 16 k per block
+    const uint8_t *hrow = hs + g * kColPitch + 16 * t;   // B operand: token g, this lane's 16 k per block
     const float *__restrict__ scale = p.scale;
     float bv[2] = {-INFINITY, -INFINITY};               // tokens 2t, 2t + 1
     int32_t bi[2] = {0x7FFFFFFF, 0x7FFFFFFF};
@@ -252,7 +272,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_lmhead_fp8(const Args p)
     for (int tile = blockIdx.x * kWarps + warp; tile < T; tile += W) {
         const int r0 = tile * kRows + g, r1 = r0 + 8;
         const float s0 = scale[min(r0, V - 1)], s1 = scale[min(r1, V - 1)];
-        float c[4] = {0.0f, 0.0f, 0.0f, 0.0f};
+        float c[kTerms][4] = {};   // per term: row g tokens 2t, 2t + 1; row g + 8 the same
 #pragma unroll
         for (int s = 0; s < kSteps; ++s) {
             issue(slot == 0 ? kDepth - 1 : slot - 1);   // the stage consumed last (its reads are done)
@@ -261,34 +281,34 @@ __global__ void __launch_bounds__(kThreads, 1) k_lmhead_fp8(const Args p)
 #pragma unroll
             for (int b = 0; b < kGroup; ++b) {
                 const int kb = s * kGroup + b;
+                // bytes 0..7 of the lane's chunk are k32 slice 0 (A words x, y:
+                // k 4t..4t+3 and 4t+16..4t+19 of the MMA), bytes 8..15 slice 1;
+                // the B words of each term follow the same map
                 const uint4 va = st[(2 * b) * 32], vb = st[(2 * b + 1) * 32];
                 const uint4 h0 = *reinterpret_cast<const uint4 *>(hrow + kb * kBlock);
-                const uint4 h1 = *reinterpret_cast<const uint4 *>(hrow + kb * kBlock + 8);
-                const uint32_t hw[8] = {h0.x, h0.y, h0.z, h0.w, h1.x, h1.y, h1.z, h1.w};
-                const uint32_t wa[4] = {va.x, va.y, va.z, va.w};
-                const uint32_t wb[4] = {vb.x, vb.y, vb.z, vb.w};
-#pragma unroll
-                for (int i = 0; i < 4; ++i)
-                    mma_f16(c, e4m3x2_to_f16x2(wa[i]), e4m3x2_to_f16x2(wb[i]), e4m3x2_to_f16x2(wa[i] >> 16),
-                            e4m3x2_to_f16x2(wb[i] >> 16), hw[2 * i], hw[2 * i + 1]);
+                const uint4 h1 = *reinterpret_cast<const uint4 *>(hrow + kMaxM * kColPitch + kb * kBlock);
+                mma_e4m3(c[0], va.x, vb.x, va.y, vb.y, h0.x, h0.y);
+                mma_e4m3(c[1], va.x, vb.x, va.y, vb.y, h1.x, h1.y);
+                mma_e4m3(c[0], va.z, vb.z, va.w, vb.w, h0.z, h0.w);
+                mma_e4m3(c[1], va.z, vb.z, va.w, vb.w, h1.z, h1.w);
             }
             slot = slot + 1 == kDepth ? 0 : slot + 1;
         }
-        // c[u]: row r0, token 2t + u; c[2 + u]: row r1, token 2t + u
+        // c[e][u]: row r0, token 2t + u; c[e][2 + u]: row r1, token 2t + u
 #pragma unroll
         for (int u = 0; u < 2; ++u) {
             const int tk = 2 * t + u;
             if (tk < M) {
                 const float dn = down[tk];
                 if (r0 < V) {
-                    const float z = c[u] * s0 * dn;
+                    const float z = (c[0][u] + c[1][u] * 0.0625f) * s0 * dn;
                     if (better(z, r0, bv[u], bi[u])) {
                         bv[u] = z;
                         bi[u] = r0;
                     }
                 }
                 if (r1 < V) {
-                    const float z = c[2 + u] * s1 * dn;
+                    const float z = (c[0][2 + u] + c[1][2 + u] * 0.0625f) * s1 * dn;
                     if (better(z, r1, bv[u], bi[u])) {
                         bv[u] = z;
                         bi[u] = r1;
