@@ -8,9 +8,11 @@
 //   z_{t,v} = scale[v] * sum_j e4m3(q[v][j]) h[t][j],   argmax over v per token
 //
 // Design (one pass over q at HBM speed):
-//  * One CTA per SM, 16 warps. Warp w owns whole 16-row tiles of the
-//    vocabulary, tiles w, w + W, ... (W = warps in the grid), and reads each
-//    tile's 45 KB once. A lane copies 16 bytes of row g = lane / 4 and of row
+//  * One CTA per SM, 16 warps. CTA b owns a contiguous range of whole 16-row
+//    tiles of the vocabulary, T/G of them to within one (G CTAs), dealt to its
+//    warps round-robin; each tile's 45 KB is read once. (Dealing tiles
+//    round-robin over all warps of the grid left 112 SMs with 112 tiles and 40
+//    with 96: the kernel is bound by per-SM MMA throughput, so that cost ~4%.) A lane copies 16 bytes of row g = lane / 4 and of row
 //    g + 8 per 64-byte K-block, so four lanes cover 64 contiguous bytes of a
 //    row and a warp step touches full 32-byte sectors only.
 //  * Products on the tensor cores as E4M3 x E4M3: mma.sync m16n8k32 with
@@ -153,7 +155,10 @@ __global__ void __launch_bounds__(kThreads, 1) k_lmhead_fp8(const Args p)
     // and loads are conflict-free. Each lane reads back only its own copies,
     // so the wait on its own commit groups is all a stage needs.
     const int T = (V + kRows - 1) / kRows;
-    const int W = gridDim.x * kWarps;
+    // this CTA's tiles: a contiguous range of floor or ceil(T / CTAs), dealt to
+    // its warps round-robin (the SMs, not the warps, share the bandwidth)
+    const int t_begin = static_cast<int>((long long)T * blockIdx.x / gridDim.x);
+    const int t_end = static_cast<int>((long long)T * (blockIdx.x + 1) / gridDim.x);
     const uint4 *ring = reinterpret_cast<const uint4 *>(dsm + kHsBytes) + (size_t)warp * kDepth * kStageVecs;
     const uint32_t ring_lane = smem_u32(ring + lane);
     // rows g and g + 8 of tile tl (rows past the end read row V - 1 and are dropped)
@@ -164,12 +169,12 @@ __global__ void __launch_bounds__(kThreads, 1) k_lmhead_fp8(const Args p)
     };
     // issue side: tile `it`, step `is` of the next stage to copy; once past the
     // last tile it commits empty groups, so the wait below counts uniformly
-    int it = blockIdx.x * kWarps + warp, is = 0;
+    int it = t_begin + warp, is = 0;
     const uint8_t *ia = q, *ib = q;
-    if (it < T)
+    if (it < t_end)
         row_ptrs(it, ia, ib);
     auto issue = [&](int slot) {
-        if (it < T) {
+        if (it < t_end) {
             const uint32_t dst = ring_lane + static_cast<uint32_t>(slot * kStageVecs) * 16u;
 #pragma unroll
             for (int b = 0; b < kGroup; ++b) {
@@ -178,8 +183,8 @@ __global__ void __launch_bounds__(kThreads, 1) k_lmhead_fp8(const Args p)
             }
             if (++is == kSteps) {
                 is = 0;
-                it += W;
-                if (it < T)
+                it += kWarps;
+                if (it < t_end)
                     row_ptrs(it, ia, ib);
             }
         }
@@ -269,7 +274,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_lmhead_fp8(const Args p)
     int32_t bi[2] = {0x7FFFFFFF, 0x7FFFFFFF};
 
     int slot = 0;
-    for (int tile = blockIdx.x * kWarps + warp; tile < T; tile += W) {
+    for (int tile = t_begin + warp; tile < t_end; tile += kWarps) {
         const int r0 = tile * kRows + g, r1 = r0 + 8;
         const float s0 = scale[min(r0, V - 1)], s1 = scale[min(r1, V - 1)];
         float c[kTerms][4] = {};   // per term: row g tokens 2t, 2t + 1; row g + 8 the same
