@@ -5,7 +5,8 @@
  * decoding on a Gemma-4-26B-A4B-shaped mixture of experts: hidden width 2816,
  * 128 routed experts of FFN width 704 plus one always-on shared expert,
  * top-8 routing, FP8-E4M3 expert weights with one fp32 scale per output row,
- * and a tied 262,144-word bf16 lm_head. One call processes M = gamma + 1
+ * and a tied 262,144-word bf16 lm_head (or its E4M3 copy with one fp32 scale
+ * per row, fgm_lm_head_argmax_fp8). One call processes M = gamma + 1
  * tokens (the real token and gamma drafted ones) in a single pass over the
  * weights ("llm-decoding", us-homepage.pages.dev, §"Lever 2: fewer passes
  * (native MTP)": the full model verifies the drafted tokens in one pass).
