@@ -56,6 +56,13 @@ class _Layer(ctypes.Structure):
                 ("down_q", ctypes.c_void_p), ("down_s", ctypes.c_void_p)]
 
 
+class _Mlp(ctypes.Structure):
+    _fields_ = [("F", ctypes.c_int),
+                ("gate_q", ctypes.c_void_p), ("gate_s", ctypes.c_void_p),
+                ("up_q", ctypes.c_void_p), ("up_s", ctypes.c_void_p),
+                ("down_q", ctypes.c_void_p), ("down_s", ctypes.c_void_p)]
+
+
 def lib():
     global _lib
     if _lib is None:
@@ -79,6 +86,9 @@ def lib():
         L.fgmo_router_token.restype = cd
         L.fgmo_router_token.argtypes = [vp, vp, vp, ci, ci, ci, vp, vp, vp]
         L.fgmo_expert_token.argtypes = [ctypes.POINTER(_Dims), ctypes.POINTER(_Layer), ci, vp, vp]
+        L.fgmo_mlp_token.argtypes = [ci, ctypes.POINTER(_Mlp), vp, vp]
+        L.fgmo_moe_layer_dense.argtypes = [ctypes.POINTER(_Dims), ctypes.POINTER(_Layer),
+                                           ctypes.POINTER(_Mlp), vp, ci, vp, vp, vp, vp, vp]
         L.fgmo_moe_layer.argtypes = [ctypes.POINTER(_Dims), ctypes.POINTER(_Layer), vp, ci, vp,
                                      vp, vp, vp, vp]
         L.fgmo_stack_layer.argtypes = [ctypes.POINTER(_Dims), ctypes.POINTER(_Layer), vp, ci, cd,
@@ -213,6 +223,43 @@ class LayerOut:
     logits: np.ndarray | None = None
 
 
+@dataclass
+class MlpParams:
+    """A gated-GELU MLP of any width F (E4M3 rows, fp32 row scales)."""
+    gate_q: np.ndarray   # uint8 [F, H]
+    gate_s: np.ndarray   # float32 [F]
+    up_q: np.ndarray     # uint8 [F, H]
+    up_s: np.ndarray     # float32 [F]
+    down_q: np.ndarray   # uint8 [H, F]
+    down_s: np.ndarray   # float32 [H]
+
+    def __post_init__(self):
+        for n in ("gate_q", "up_q", "down_q"):
+            setattr(self, n, _c(getattr(self, n), np.uint8))
+        for n in ("gate_s", "up_s", "down_s"):
+            setattr(self, n, _c(getattr(self, n), np.float32))
+        F, H = self.gate_q.shape
+        assert self.up_q.shape == (F, H) and self.down_q.shape == (H, F)
+        assert self.gate_s.shape == (F,) and self.up_s.shape == (F,) and self.down_s.shape == (H,)
+
+    @property
+    def H(self) -> int:
+        return self.gate_q.shape[1]
+
+    def _struct(self) -> _Mlp:
+        return _Mlp(self.gate_q.shape[0], _p(self.gate_q), _p(self.gate_s), _p(self.up_q), _p(self.up_s),
+                    _p(self.down_q), _p(self.down_s))
+
+
+def mlp_token(mlp: MlpParams, x) -> np.ndarray:
+    """The MLP on one token x[H]."""
+    x = _c(x, np.float64)
+    out = np.empty(mlp.H, np.float64)
+    m = mlp._struct()
+    lib().fgmo_mlp_token(mlp.H, ctypes.byref(m), _p(x), _p(out))
+    return out
+
+
 def router_token(layer: LayerParams, x) -> tuple[np.ndarray, np.ndarray, float, np.ndarray]:
     x = _c(x, np.float64)
     d = layer.dims
@@ -233,8 +280,9 @@ def expert_token(layer: LayerParams, expert: int, x) -> np.ndarray:
     return out
 
 
-def moe_layer(layer: LayerParams, x) -> LayerOut:
-    """One MoE layer on x[M, H] (no norm, no residual)."""
+def moe_layer(layer: LayerParams, x, dense_shared: MlpParams | None = None) -> LayerOut:
+    """One MoE layer on x[M, H] (no norm, no residual). With ``dense_shared``
+    that MLP is the always-on part in place of the layer's shared expert."""
     x = _c(x, np.float64)
     M = x.shape[0]
     d = layer.dims
@@ -244,8 +292,14 @@ def moe_layer(layer: LayerParams, x) -> LayerOut:
     margin = np.empty(M, np.float64)
     logits = np.empty((M, d.E), np.float64)
     s = layer._struct()
-    lib().fgmo_moe_layer(ctypes.byref(d), ctypes.byref(s), _p(x), M, _p(y), _p(ids), _p(w),
-                         _p(margin), _p(logits))
+    if dense_shared is None:
+        lib().fgmo_moe_layer(ctypes.byref(d), ctypes.byref(s), _p(x), M, _p(y), _p(ids), _p(w),
+                             _p(margin), _p(logits))
+    else:
+        assert dense_shared.H == d.H
+        m = dense_shared._struct()
+        lib().fgmo_moe_layer_dense(ctypes.byref(d), ctypes.byref(s), ctypes.byref(m), _p(x), M, _p(y),
+                                   _p(ids), _p(w), _p(margin), _p(logits))
     return LayerOut(y, ids, w, margin, logits)
 
 

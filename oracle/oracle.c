@@ -262,19 +262,26 @@ double fgmo_router_token(const double *x, const uint16_t *router_w, const float 
     return margin;
 }
 
-/* One expert applied to one token x[H]: g = s_g * (Q_g x), u = s_u * (Q_u x),
+/* A gated-GELU MLP of width F: gate/up rows [F][H] and down rows [H][F] as
+ * E4M3 codes with one fp32 scale per row. An expert is its F = 704 case; the
+ * always-on dense MLP that "llm-decoding" §"Where the 7.36 GB goes" counts at
+ * 2816x2112 is its F = 2112 case. */
+typedef struct {
+    int F;
+    const uint8_t *gate_q;   /* [F][H] */
+    const float *gate_s;     /* [F] */
+    const uint8_t *up_q;     /* [F][H] */
+    const float *up_s;       /* [F] */
+    const uint8_t *down_q;   /* [H][F] */
+    const float *down_s;     /* [H] */
+} fgmo_mlp;
+
+/* The MLP on one token x[H]: g = s_g * (Q_g x), u = s_u * (Q_u x),
  * a = gelu_tanh(g) * u, out = s_d * (Q_d a). Weights are dequantised code by
  * code from E4M3 with their row scale. */
-void fgmo_expert_token(const fgmo_dims *d, const fgmo_layer *L, int expert, const double *x,
-                       double *out)
+void fgmo_mlp_token(int H, const fgmo_mlp *m, const double *x, double *out)
 {
-    const int H = d->H, F = d->F;
-    const uint8_t *qg = L->gate_q + (int64_t)expert * F * H;
-    const uint8_t *qu = L->up_q + (int64_t)expert * F * H;
-    const uint8_t *qd = L->down_q + (int64_t)expert * H * F;
-    const float *sg = L->gate_s + (int64_t)expert * F;
-    const float *su = L->up_s + (int64_t)expert * F;
-    const float *sd = L->down_s + (int64_t)expert * H;
+    const int F = m->F;
     double *a = (double *)malloc(sizeof(double) * F);
     int i, j;
 #pragma omp parallel for schedule(static)
@@ -282,11 +289,11 @@ void fgmo_expert_token(const fgmo_dims *d, const fgmo_layer *L, int expert, cons
         double g = 0.0, u = 0.0;
         int jj;
         for (jj = 0; jj < H; ++jj) {
-            g += fgmo_e4m3_decode(qg[(int64_t)i * H + jj]) * x[jj];
-            u += fgmo_e4m3_decode(qu[(int64_t)i * H + jj]) * x[jj];
+            g += fgmo_e4m3_decode(m->gate_q[(int64_t)i * H + jj]) * x[jj];
+            u += fgmo_e4m3_decode(m->up_q[(int64_t)i * H + jj]) * x[jj];
         }
-        g *= (double)sg[i];
-        u *= (double)su[i];
+        g *= (double)m->gate_s[i];
+        u *= (double)m->up_s[i];
         a[i] = fgmo_gelu_tanh(g) * u;
     }
 #pragma omp parallel for schedule(static)
@@ -294,18 +301,36 @@ void fgmo_expert_token(const fgmo_dims *d, const fgmo_layer *L, int expert, cons
         double acc = 0.0;
         int ii;
         for (ii = 0; ii < F; ++ii)
-            acc += fgmo_e4m3_decode(qd[(int64_t)j * F + ii]) * a[ii];
-        out[j] = (double)sd[j] * acc;
+            acc += fgmo_e4m3_decode(m->down_q[(int64_t)j * F + ii]) * a[ii];
+        out[j] = (double)m->down_s[j] * acc;
     }
     free(a);
 }
 
+/* Expert e of a layer applied to one token x[H]. */
+void fgmo_expert_token(const fgmo_dims *d, const fgmo_layer *L, int expert, const double *x,
+                       double *out)
+{
+    const int H = d->H, F = d->F;
+    fgmo_mlp m;
+    m.F = F;
+    m.gate_q = L->gate_q + (int64_t)expert * F * H;
+    m.gate_s = L->gate_s + (int64_t)expert * F;
+    m.up_q = L->up_q + (int64_t)expert * F * H;
+    m.up_s = L->up_s + (int64_t)expert * F;
+    m.down_q = L->down_q + (int64_t)expert * H * F;
+    m.down_s = L->down_s + (int64_t)expert * H;
+    fgmo_mlp_token(H, &m, x, out);
+}
+
 /* One MoE layer on M tokens x[M][H]:
  *   y_t = sum_i w_{t,i} * expert_{ids_{t,i}}(x_t) + shared(x_t).
+ * shared: the MLP `dense` when given (any width; the layer's own shared
+ * expert is then not used), else expert E when d->n_shared, else nothing.
  * ids[M][k], w[M][k], margin[M] and logits[M][E] are outputs (logits may be
  * NULL). */
-void fgmo_moe_layer(const fgmo_dims *d, const fgmo_layer *L, const double *x, int M, double *y,
-                    int32_t *ids, double *w, double *margin, double *logits)
+void fgmo_moe_layer_dense(const fgmo_dims *d, const fgmo_layer *L, const fgmo_mlp *dense, const double *x,
+                          int M, double *y, int32_t *ids, double *w, double *margin, double *logits)
 {
     const int H = d->H;
     double *tmp = (double *)malloc(sizeof(double) * H);
@@ -323,13 +348,22 @@ void fgmo_moe_layer(const fgmo_dims *d, const fgmo_layer *L, const double *x, in
             for (j = 0; j < H; ++j)
                 yt[j] += w[(int64_t)t * d->k + i] * tmp[j];
         }
-        if (d->n_shared) {
-            fgmo_expert_token(d, L, d->E, xt, tmp);
+        if (dense || d->n_shared) {
+            if (dense)
+                fgmo_mlp_token(H, dense, xt, tmp);
+            else
+                fgmo_expert_token(d, L, d->E, xt, tmp);
             for (j = 0; j < H; ++j)
                 yt[j] += tmp[j];
         }
     }
     free(tmp);
+}
+
+void fgmo_moe_layer(const fgmo_dims *d, const fgmo_layer *L, const double *x, int M, double *y,
+                    int32_t *ids, double *w, double *margin, double *logits)
+{
+    fgmo_moe_layer_dense(d, L, NULL, x, M, y, ids, w, margin, logits);
 }
 
 /* One layer of the stack: h <- h + layer(RMSNorm(h)), in place. */

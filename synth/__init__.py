@@ -17,6 +17,9 @@ benchmark configurations):
                          ~N(0, 0.02) in fp32, then quantised per output row
                          to E4M3 with scale = max|row| / 448 (fp32) by
                          torch's float8_e4m3fn cast (round to nearest even);
+  * dense shared MLP     (the wider always-on variant) gate/up [2112, 2816]
+                         and down [2816, 2112], ~N(0, 0.02), quantised per
+                         output row like the experts;
   * tied embedding       [V, 2816] ~N(0, 0.02), rounded to bf16;
                          its 8-bit copy for the FP8 lm_head: the expert
                          weights' per-row E4M3 quantiser applied to those
@@ -91,6 +94,39 @@ def layer(seed: int, *, device="cpu", s: float = 0.0, hidden: int = HIDDEN, ffn:
         out[name + "_q"] = q
         out[name + "_s"] = sc
     return out
+
+
+def dense_mlp(seed: int, *, width: int = 3 * FFN, device="cpu", hidden: int = HIDDEN,
+              std: float = WEIGHT_STD) -> dict[str, torch.Tensor]:
+    """An always-on gated-GELU MLP of the given width (the 2816 x 2112 dense
+    MLP of the page's byte list): gate_q/up_q uint8 [W, H] with gate_s/up_s
+    f32 [W]; down_q uint8 [H, W] with down_s f32 [H], each quantised per
+    output row (down rows are W wide)."""
+    g = _gen(seed, device)
+    out: dict[str, torch.Tensor] = {}
+    for name, shape in (("gate", (width, hidden)), ("up", (width, hidden)), ("down", (hidden, width))):
+        w = torch.randn(shape, generator=g, device=device, dtype=torch.float32) * std
+        out[name + "_q"], out[name + "_s"] = quantize_rows_e4m3(w)
+        del w
+    return out
+
+
+def dense_mlp_as_experts(mlp: dict[str, torch.Tensor], ffn: int = FFN) -> dict[str, torch.Tensor]:
+    """The same MLP laid out as width / ffn experts of FFN width `ffn`:
+    expert p takes gate/up rows [p ffn, (p+1) ffn) and down columns of the
+    same range; every expert keeps the full-width down rows' scales. A re-
+    layout only: no value changes."""
+    W, H = mlp["gate_q"].shape
+    assert W % ffn == 0
+    n = W // ffn
+    return {
+        "gate_q": mlp["gate_q"].reshape(n, ffn, H).contiguous(),
+        "gate_s": mlp["gate_s"].reshape(n, ffn).contiguous(),
+        "up_q": mlp["up_q"].reshape(n, ffn, H).contiguous(),
+        "up_s": mlp["up_s"].reshape(n, ffn).contiguous(),
+        "down_q": mlp["down_q"].reshape(H, n, ffn).permute(1, 0, 2).contiguous(),
+        "down_s": mlp["down_s"].unsqueeze(0).expand(n, H).contiguous(),
+    }
 
 
 def hidden_states(seed: int, m: int, *, device="cpu", hidden: int = HIDDEN) -> torch.Tensor:
