@@ -96,6 +96,8 @@ def lib():
         L.fgmo_lm_head.argtypes = [vp, i64, ci, vp, ci, vp, vp, vp]
         L.fgmo_lm_head_fp8.argtypes = [vp, vp, i64, ci, vp, ci, vp, vp, vp]
         L.fgmo_spec_verify.argtypes = [vp, vp, ci, vp]
+        L.fgmo_lm_head_logits.argtypes = [vp, i64, ci, vp, ci, vp]
+        L.fgmo_spec_sample.argtypes = [vp, i64, ci, cd, vp, vp, vp, vp, vp]
         L.fgmo_num_threads.restype = ci
         L.fgmo_set_num_threads.argtypes = [ci]
         _lib = L
@@ -356,3 +358,34 @@ def spec_verify(target, draft) -> tuple[int, int]:
     out = np.empty(2, np.int32)
     lib().fgmo_spec_verify(_p(t), _p(d) if d.size else None, M, _p(out))
     return int(out[0]), int(out[1])
+
+
+def lm_head_logits(emb_bits, h) -> np.ndarray:
+    """All logits of the bf16 tied lm_head: float64 [M, V]."""
+    e = _c(emb_bits, np.uint16)
+    h = _c(h, np.float64)
+    V, H = e.shape
+    M = h.shape[0]
+    assert h.shape[1] == H and 1 <= M <= 16
+    z = np.empty((M, V), np.float64)
+    lib().fgmo_lm_head_logits(_p(e), V, H, _p(h), M, _p(z))
+    return z
+
+
+def spec_sample(z, T: float, draft, u_acc, u_next) -> tuple[int, int, float, float]:
+    """Speculative sampling verify at temperature T > 0 with a deterministic
+    drafter, on logits z [M, V] and caller-supplied uniforms u_acc [M-1],
+    u_next [M]. Returns (accepted drafts a, emitted token, accept margin,
+    inverse-CDF gap)."""
+    z = _c(z, np.float64)
+    M, V = z.shape
+    d = _c(draft, np.int32)
+    ua = _c(u_acc, np.float64)
+    un = _c(u_next, np.float64)
+    assert d.shape == (M - 1,) and ua.shape == (M - 1,) and un.shape == (M,) and T > 0
+    assert ((d >= 0) & (d < V)).all()
+    out = np.empty(2, np.int32)
+    mg = np.empty(2, np.float64)
+    lib().fgmo_spec_sample(_p(z), V, M, float(T), _p(d) if d.size else None, _p(ua) if ua.size else None,
+                           _p(un), _p(out), _p(mg))
+    return int(out[0]), int(out[1]), float(mg[0]), float(mg[1])

@@ -522,6 +522,108 @@ void fgmo_spec_verify(const int32_t *target, const int32_t *draft, int M, int32_
     out[1] = target[a];
 }
 
+/* Logits of the tied bf16 lm_head for all V rows: z[t][v] = sum_j E[v][j] h_t[j]
+ * (the quantity fgmo_lm_head takes the argmax of). z is [M][V]. */
+void fgmo_lm_head_logits(const uint16_t *emb, int64_t V, int H, const double *h, int M, double *z)
+{
+    int64_t v;
+#pragma omp parallel for schedule(static)
+    for (v = 0; v < V; ++v) {
+        double zz[16];
+        int t;
+        row_logits_bf16(emb, v, H, h, M, zz);
+        for (t = 0; t < M; ++t)
+            z[(int64_t)t * V + v] = zz[t];
+    }
+}
+
+/* Inverse CDF of the unnormalised weights w[0..V-1] at u in [0, 1): the
+ * smallest v with w_0 + ... + w_v > u * (w_0 + ... + w_{V-1}), summed in
+ * vocabulary order; *gap = distance from u * total to the nearest partial sum
+ * (how far u is from choosing a neighbour). */
+static int64_t inverse_cdf(const double *w, int64_t V, double u, double *gap)
+{
+    double total = 0.0, target, acc = 0.0, prev = 0.0;
+    int64_t v, last = -1;
+    for (v = 0; v < V; ++v)
+        total += w[v];
+    target = u * total;
+    for (v = 0; v < V; ++v) {
+        if (w[v] <= 0.0)
+            continue;
+        last = v;
+        prev = acc;
+        acc += w[v];
+        if (acc > target) {
+            if (gap)
+                *gap = fmin(target - prev, acc - target);
+            return v;
+        }
+    }
+    if (gap)
+        *gap = 0.0;   /* u * total reached the end only through rounding */
+    return last;
+}
+
+/* Speculative sampling verify at temperature T > 0 ("llm-decoding",
+ * §"What we learned": a proposed token is kept only if it passes the
+ * distribution the full model samples from, and a rejected one falls back to
+ * a real model step, so the output distribution equals ordinary decoding).
+ * The drafter here proposes tokens only: its distribution at position i is
+ * one-hot at d_i. Then, with p_i = softmax(z_i / T) over the V logits of
+ * position i:
+ *   for i = 0 .. M-2: accept d_i if u_acc[i] < p_i(d_i); otherwise emit a
+ *     sample of p_i with d_i removed (renormalised), by inverse CDF at
+ *     u_next[i], and stop: out = {i, sample};
+ *   if all M-1 drafts pass: emit a sample of p_{M-1} at u_next[M-1]:
+ *     out = {M-1, sample}.
+ * z is [M][V]; u_acc [M-1] and u_next [M] are uniforms in [0, 1) supplied by
+ * the caller. margin[0] = the smallest |u_acc[i] - p_i(d_i)| over the tested
+ * drafts, margin[1] = the inverse-CDF gap of the emitted sample, relative to
+ * the distribution's total (decisions closer than these may round either
+ * way in another summation order). */
+void fgmo_spec_sample(const double *z, int64_t V, int M, double T, const int32_t *draft, const double *u_acc,
+                      const double *u_next, int32_t *out, double *margin)
+{
+    double *w = (double *)malloc(sizeof(double) * (size_t)V);
+    double acc_margin = INFINITY, gap = 0.0;
+    int i;
+    for (i = 0; i < M; ++i) {
+        const double *zi = z + (int64_t)i * V;
+        double zmax = -INFINITY, total = 0.0;
+        int64_t v, pick;
+        for (v = 0; v < V; ++v)
+            if (zi[v] > zmax)
+                zmax = zi[v];
+        for (v = 0; v < V; ++v) {
+            w[v] = exp((zi[v] - zmax) / T);
+            total += w[v];
+        }
+        if (i < M - 1) {
+            const double pd = w[draft[i]] / total;
+            acc_margin = fmin(acc_margin, fabs(u_acc[i] - pd));
+            if (u_acc[i] < pd)
+                continue;
+            w[draft[i]] = 0.0;
+        }
+        pick = inverse_cdf(w, V, u_next[i], &gap);
+        {
+            double tot = 0.0;
+            for (v = 0; v < V; ++v)
+                tot += w[v];
+            gap = tot > 0.0 ? gap / tot : 0.0;
+        }
+        out[0] = i;
+        out[1] = (int32_t)pick;
+        break;
+    }
+    if (margin) {
+        margin[0] = acc_margin;
+        margin[1] = gap;
+    }
+    free(w);
+}
+
 int fgmo_num_threads(void)
 {
 #ifdef _OPENMP
