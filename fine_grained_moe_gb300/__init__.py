@@ -113,6 +113,21 @@ def _m(x: torch.Tensor) -> int:
     return int(x.shape[0])
 
 
+def _check_like(name: str, t: torch.Tensor, x: torch.Tensor) -> None:
+    """Output rows must match the input rows: bf16 [M, 2816] on x's device."""
+    if tuple(t.shape) != tuple(x.shape) or t.dtype != torch.bfloat16 or t.device != x.device:
+        raise FgmError(f"{name}: expected bf16 {tuple(x.shape)} on {x.device}, got "
+                       f"{tuple(t.shape)} {t.dtype} on {t.device}")
+
+
+def _check_topk(M: int, x: torch.Tensor, topk_ids: torch.Tensor | None, topk_w: torch.Tensor | None) -> None:
+    """Optional routing outputs: int32 / float32 [M, 8] on x's device."""
+    for name, t, dt in (("topk_ids", topk_ids, torch.int32), ("topk_w", topk_w, torch.float32)):
+        if t is not None and (tuple(t.shape) != (M, TOPK) or t.dtype != dt or t.device != x.device):
+            raise FgmError(f"{name}: expected {dt} [{M}, {TOPK}] on {x.device}, got "
+                           f"{tuple(t.shape)} {t.dtype} on {t.device}")
+
+
 def select_path(path: int) -> int:
     """Selects the execution path (PATH_FUSED or PATH_STAGED); returns the previous one."""
     return int(lib().fgm_select_path(int(path)))
@@ -224,6 +239,8 @@ def moe_layer_fwd(layer, x: torch.Tensor, y: torch.Tensor | None = None,
     """One MoE layer (no norm, no residual) on bf16 x[M, 2816]; returns bf16 y."""
     M = _m(x)
     y = torch.empty_like(x) if y is None else y
+    _check_like("y", y, x)
+    _check_topk(M, x, topk_ids, topk_w)
     ws = _ws(ws, x.device)
     L = (layer if isinstance(layer, Layer) else Layer.from_dict(layer)).struct()
     _check(lib().fgm_moe_layer_fwd(ctypes.byref(L), _ptr(x), _ptr(y), M, _ptr(topk_ids), _ptr(topk_w),
@@ -240,6 +257,8 @@ def moe_layer_fwd_noalloc(layer, x: torch.Tensor, y: torch.Tensor,
     one device race on that scratch; make the first call on a device before
     any stream capture starts, since it looks the scratch up."""
     M = _m(x)
+    _check_like("y", y, x)
+    _check_topk(M, x, topk_ids, topk_w)
     L = (layer if isinstance(layer, Layer) else Layer.from_dict(layer)).struct()
     _check(lib().fgm_moe_layer_fwd_noalloc(ctypes.byref(L), _ptr(x), _ptr(y), M, _ptr(topk_ids),
                                            _ptr(topk_w), _stream(stream)))
@@ -252,6 +271,10 @@ def moe_stack_fwd(layers, x: torch.Tensor, y: torch.Tensor | None = None,
     """The stack h <- h + layer(RMSNorm(h)) over ``layers``; returns bf16 h."""
     M = _m(x)
     y = torch.empty_like(x) if y is None else y
+    _check_like("y", y, x)
+    if ids_trace is not None and (tuple(ids_trace.shape) != (len(layers), M, TOPK)
+                                  or ids_trace.dtype != torch.int32 or ids_trace.device != x.device):
+        raise FgmError(f"ids_trace: expected int32 [{len(layers)}, {M}, {TOPK}] on {x.device}")
     ws = _ws(ws, x.device)
     arr = _layers_array(layers)
     _check(lib().fgm_moe_stack_fwd(arr, len(arr), _ptr(x), _ptr(y), M, _ptr(ids_trace), ws.ptr,

@@ -129,7 +129,12 @@ int fgm_moe_layer_fwd(const fgm_layer *layer, const uint16_t *x, uint16_t *y, in
  *    FGM_ERR_INVALID_ARG with a message naming the limit.
  *  - Set-up: the first call on each device, with that device current, looks
  *    up the array's device address (the CUDA runtime may load the module
- *    then). Make that first call before any stream capture begins.
+ *    then). Make that first call before any stream capture begins. The
+ *    address is kept for the life of the process: after cudaDeviceReset (or
+ *    any other teardown of the device's primary context) in the same process
+ *    it is stale, so do not call this entry point again in that process.
+ *    The per-device set-up of every other entry point (the device check and
+ *    kernel attributes) has the same lifetime.
  *  - Each call clears the array's status word and barrier counters on
  *    `stream` before it launches.
  *  - One array per device serves every caller on it: calls on that device

@@ -18,11 +18,22 @@ import synth
 from helpers import REL_TOL, rowwise_rel_err
 
 
+def _lib():
+    """The library, built first when this file runs alone in a fresh tree."""
+    import os
+
+    import fine_grained_moe_gb300 as fgm
+    if not os.path.exists(fgm.LIB_PATH):
+        from fine_grained_moe_gb300 import build
+        build.build()
+    return fgm.lib()
+
+
 def test_noalloc_rejects_m_beyond_its_scratch():
     import fine_grained_moe_gb300 as fgm
     L = fgm.fgm_layer()
     buf = (ctypes.c_uint8 * 4096)()
-    lib = fgm.lib()
+    lib = _lib()
     for M in (0, 9, 64):
         assert lib.fgm_moe_layer_fwd_noalloc(ctypes.byref(L), buf, buf, M, None, None, None) == -1
         assert b"at most 8 tokens" in lib.fgm_last_error()
@@ -40,12 +51,19 @@ def test_noalloc_matches_workspace_call_twice():
         ys = [torch.empty_like(x) for x in xs]
         ids = [torch.empty((x.shape[0], 8), dtype=torch.int32, device="cuda") for x in xs]
         wts = [torch.empty((x.shape[0], 8), dtype=torch.float32, device="cuda") for x in xs]
+        # the first call on the device resolves the scratch address; the device
+        # memory in use (torch's allocator and the driver's view of the whole
+        # device) must not grow across the two calls that follow it
+        fgm.moe_layer_fwd_noalloc(p, xs[0], ys[0])
         torch.cuda.synchronize()
         before = torch.cuda.memory_allocated()
+        free_before, _ = torch.cuda.mem_get_info()
         for i in range(2):   # two calls in a row on the built-in scratch
             fgm.moe_layer_fwd_noalloc(p, xs[i], ys[i], topk_ids=ids[i], topk_w=wts[i])
         torch.cuda.synchronize()
+        free_after, _ = torch.cuda.mem_get_info()
         assert torch.cuda.memory_allocated() == before
+        assert free_after >= free_before
         for i, x in enumerate(xs):
             M = x.shape[0]
             rid = torch.empty((M, 8), dtype=torch.int32, device="cuda")
