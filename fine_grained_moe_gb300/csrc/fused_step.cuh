@@ -56,6 +56,8 @@ constexpr int kStages = 4;                    // ring slots
 constexpr int kRowStride = 2880;              // smem stride of a 2816-byte row (conflict-free 16-byte reads)
 constexpr int kSlotBytes = 16 * kRowStride;   // 46080
 constexpr int kDownTiles = 4;                 // 16-row down tiles per ring slot (64 x 704 bytes)
+constexpr int kRouterCtas = 32;               // the last 32 CTAs compute the router logits,
+constexpr int kRouterRows = FGM_EXPERTS / kRouterCtas;   // 4 rows each (fewer CTAs read the residual)
 constexpr int kTerms = 3;                     // E4M3 terms per activation
 constexpr int kSharedSlot = kMaxSlots - 1;
 constexpr uint32_t kActPending = 0x7FC0DEADu;   // NaN marker: activation row not written yet
@@ -106,7 +108,7 @@ struct __align__(128) Smem {
     uint8_t ring[kStages][kSlotBytes];
     float4 red[2][kMW][2][32];   // per-warp K-slice partials of up to 2 tiles, double-buffered
     float part[kMW][8];
-    float part2[kMW][8];
+    float part2[kRouterRows][kMW][8];
     float best_v[kMW][8];       // lm_head winners per reducing warp and token
     int32_t best_i[kMW][8];
     float comb[2][kMaxSlots][8];
@@ -233,6 +235,19 @@ __device__ __forceinline__ void consumer_sync() { asm volatile("bar.sync 1, %0;"
 
 __device__ __forceinline__ float4 ldcg4(const float *p) { return __ldcg(reinterpret_cast<const float4 *>(p)); }
 
+// 16-byte load for polling another CTA's stores: volatile asm, so every
+// iteration of a polling loop issues it (a plain load may be hoisted out of
+// the loop), relaxed at GPU scope (served by L2, never a stale L1 line).
+__device__ __forceinline__ float4 ld_poll4(const float *p)
+{
+    float4 v;
+    asm volatile("ld.relaxed.gpu.global.v4.f32 {%0,%1,%2,%3}, [%4];"
+                 : "=f"(v.x), "=f"(v.y), "=f"(v.z), "=f"(v.w)
+                 : "l"(p)
+                 : "memory");
+    return v;
+}
+
 // 4-byte asynchronous global -> shared copy and the wait for all of a thread's copies.
 __device__ __forceinline__ void cp_async4(float *dst, const float *src)
 {
@@ -351,44 +366,41 @@ __device__ __forceinline__ Range split(long long total, int part, int parts)
     return Range{static_cast<int>(total * part / parts), static_cast<int>(total * (part + 1) / parts)};
 }
 
-// Gate/up rows of one CTA, in whole 8-row tiles (no stage is partly empty):
-// CTA c < 88 owns shared-expert tile c; the U * 88 routed tiles are dealt so
-// that every CTA's total (shared + routed) is floor or ceil of (U + 1) * 88 / G.
-__device__ __forceinline__ Range gu_shared_rows(int cta)
+// Gate/up tiles (8 row pairs each) of the grid in one list: tiles 0..87 are
+// the shared expert's, then routed slot u's tile t is 88 (u + 1) + t. CTA c
+// takes tiles c, c + G, c + 2 G, ...: its tile k has list index c + k G (the
+// shared tile, if any, is its tile 0). Every expert's tiles are spread over
+// the whole grid, so an expert early in the list has all of its activations
+// written early in the gate/up phase, and the down rows that read them need
+// not wait for the slowest CTA's last tiles.
+constexpr int kGuTiles = kF / 8;   // 88 tiles per expert
+
+__device__ __forceinline__ int gu_tile_count(int U, int cta, int G)
 {
-    constexpr int kTiles = kF / 8;
-    return cta < kTiles ? Range{8 * cta, 8 * cta + 8} : Range{kF, kF};
+    const int total = (U + 1) * kGuTiles;
+    return cta < total ? (total - 1 - cta) / G + 1 : 0;
 }
 
-__device__ __forceinline__ Range gu_routed_rows(int U, int cta, int G)
+// Gate/up tiles of the CTAs before `cta` (the first total % G CTAs take one more).
+__device__ __forceinline__ unsigned gu_tiles_before(int U, int cta, int G)
 {
-    // 32-bit arithmetic: (U + 1) * 88 * G < 2^31 for U < 65, G < 65536 / 88
-    constexpr unsigned kTiles = kF / 8;
-    const unsigned total = static_cast<unsigned>(U + 1) * kTiles;
-    const int b = static_cast<int>(total * cta / G) - min(cta, (int)kTiles);
-    const int e = static_cast<int>(total * (cta + 1) / G) - min(cta + 1, (int)kTiles);
-    return Range{8 * b, 8 * e};
+    const unsigned total = static_cast<unsigned>(U + 1) * kGuTiles;
+    return static_cast<unsigned>(cta) * (total / G) + min(static_cast<unsigned>(cta), total % G);
 }
 
-// Down-phase stages of one CTA: the CTA's row range of the (slot, row) space
-// cut at every 64-row boundary of a slot. CTAs visit their stages in a
-// rotated order so that CTAs working on different experts add into different
-// rows of the residual at any moment.
 // Down rows of one CTA, in 16-row tiles, dealt so that gate/up and down work
 // together are even: a gate/up tile (8 row pairs of 2816 bytes) counts as 3
 // down tiles (16 rows of 704 bytes; measured stage times are about 1 : 0.3),
-// and a CTA with one more gate/up tile than another gets about 3 fewer down
-// tiles. Cumulative over CTAs: 16 (units(c) - 3 * gate/up tiles before c).
+// and a CTA with one more gate/up tile than another gets 3 fewer down tiles.
+// Cumulative over CTAs: 16 (units(c) - 3 * gate/up tiles before c).
 __device__ __forceinline__ Range down_rows(int U, int cta, int G)
 {
     // 32-bit arithmetic: (U + 1) * 440 * G < 2^32 for U < 65, G <= 152 * 1000
-    constexpr unsigned kGuTiles = kF / 8;
     constexpr unsigned kW = 3;
     const unsigned units = static_cast<unsigned>(U + 1) * (kW * kGuTiles + kH / 16);
-    const unsigned gtiles = static_cast<unsigned>(U + 1) * kGuTiles;
     const unsigned c0 = cta, c1 = cta + 1;
-    const int b = static_cast<int>(units * c0 / G - kW * (gtiles * c0 / G));
-    const int e = static_cast<int>(units * c1 / G - kW * (gtiles * c1 / G));
+    const int b = static_cast<int>(units * c0 / G - kW * gu_tiles_before(U, cta, G));
+    const int e = static_cast<int>(units * c1 / G - kW * gu_tiles_before(U, cta + 1, G));
     return Range{16 * b, 16 * e};
 }
 
@@ -673,7 +685,7 @@ __device__ __noinline__ DownCols<NB> down_columns(const float *act_slot, int M, 
             bool ready = true;
 #pragma unroll
             for (int k = 0; k < 4; ++k) {
-                const float4 f = ldcg4(ar + 4 * k);
+                const float4 f = ld_poll4(ar + 4 * k);
                 v[4 * k] = f.x;
                 v[4 * k + 1] = f.y;
                 v[4 * k + 2] = f.z;
@@ -795,57 +807,28 @@ __global__ void __launch_bounds__(kThreads, 1) k_fused(const __grid_constant__ P
                 }
                 ++stage;
             };
-            // The stages of a layer after its routing is known: routed gate/up
-            // row pairs, then down rows (routed experts and the shared one).
-            struct LayerPlan {
-                int U, gb, ge, gpos, di;
-                DownStages ds;
-                __device__ LayerPlan(int U_, int cta_, int G_)
-                    : U(U_), gb(0), ge(0), gpos(0), di(0), ds(U_, cta_, G_)
-                {
-                    const Range rb = gu_routed_rows(U_, cta_, G_);
-                    gb = rb.begin;
-                    ge = rb.end;
-                    gpos = gb;
-                }
-                // next stage: kind 0 = gate/up (slot u, row i, nv pairs), 1 = down (slot si, row j, nv rows)
-                __device__ bool next(int &kind, int &slot, int &row, int &nv)
-                {
-                    if (gpos < ge) {
-                        kind = 0;
-                        slot = gpos / kF;
-                        row = gpos % kF;
-                        nv = min(min(8, kF - row), ge - gpos);
-                        gpos += nv;
-                        return true;
-                    }
-                    if (di < ds.n) {
-                        int pos;
-                        ds.get(di++, pos, nv);
-                        kind = 1;
-                        slot = pos / kH;
-                        row = pos % kH;
-                        return true;
-                    }
-                    return false;
-                }
-            };
             const bool lm_phase = p.mode == kModeVerify || p.mode == kModeLmHead;
             const Range rvoc = lm_phase ? split(p.V, cta, G) : Range{0, 0};
             for (int l = 0; l < n_layers && ok; ++l) {
                 const fgm_layer &L = p.layers[l];
                 p_layer = l;
                 p_stage0 = stage;
-                // this layer's router row (and bias) into L2 ahead of phase A: the
-                // consumers are still in the previous layer's down rows
-                if (l > 0 && cta < kE)
-                    prefetch_l2(L.router_w + (size_t)cta * kH, kH * sizeof(uint16_t));
-                if (l > 0 && cta == kE - 1 && L.router_b)
-                    prefetch_l2(L.router_b, kE * sizeof(float));
-                // phase A: shared expert gate/up rows
-                const Range ra = gu_shared_rows(cta);
-                for (int i = ra.begin; i < ra.end && ok; i += 8)
-                    gu_rows(L, kShared, i, min(8, ra.end - i));
+                // router CTAs: the layer's kRouterRows router rows (and their bias
+                // entries when the bias is 16-byte aligned) as the layer's first stage
+                if (cta >= G - kRouterCtas) {
+                    const int e0 = kRouterRows * (cta - (G - kRouterCtas));
+                    const bool bias = L.router_b && (reinterpret_cast<uintptr_t>(L.router_b) & 15u) == 0;
+                    constexpr uint32_t kRowsBytes = kRouterRows * kH * sizeof(uint16_t);
+                    uint8_t *dst = claim(kRowsBytes + (bias ? kRouterRows * sizeof(float) : 0u));
+                    if (!dst)
+                        break;
+                    bulk_g2s(dst, L.router_w + (size_t)e0 * kH, kRowsBytes, &s.full[stage % kStages]);
+                    if (bias)
+                        bulk_g2s(dst + kRowsBytes, L.router_b + e0, kRouterRows * sizeof(float), &s.full[stage % kStages]);
+                    ++stage;
+                }
+                if (cta < kGuTiles)
+                    gu_rows(L, kShared, 8 * cta, 8);
                 if (!ok)
                     break;
                 ok = mbar_wait(&s.route, l & 1, s, deadline, status, 2, l);
@@ -853,13 +836,17 @@ __global__ void __launch_bounds__(kThreads, 1) k_fused(const __grid_constant__ P
                     break;
                 const int pb = l & 1;
                 const int U = s.n_unique[pb];
-                // phases B and C
-                LayerPlan plan(U, cta, G);
-                int kind, slot, row, nv;
-                while (ok && plan.next(kind, slot, row, nv)) {
-                    if (kind == 0) {
-                        gu_rows(L, s.experts[pb][slot], row, nv);
-                    } else {
+                const int n_gu = gu_tile_count(U, cta, G);
+                for (int k = cta < kGuTiles ? 1 : 0; k < n_gu && ok; ++k) {
+                    const int x = cta + k * G - kGuTiles;
+                    gu_rows(L, s.experts[pb][x / kGuTiles], 8 * (x % kGuTiles), 8);
+                }
+                const DownStages dsp(U, cta, G);
+                for (int di = 0; di < dsp.n && ok; ++di) {
+                    int pos, nv;
+                    dsp.get(di, pos, nv);
+                    const int slot = pos / kH, row = pos % kH;
+                    {
                         const int e = slot < U ? s.experts[pb][slot] : kShared;
                         uint8_t *dst = claim(static_cast<uint32_t>(nv) * kF);
                         if (!dst)
@@ -1116,29 +1103,49 @@ __global__ void __launch_bounds__(kThreads, 1) k_fused(const __grid_constant__ P
         if (l == 0 && p.debug_stall)
             grid_barrier();
         // -------------------------------------------------------- phase A
-        const Range rsh = gu_shared_rows(cta);
+        const int n_sh = cta < kGuTiles ? 1 : 0;
+        const Range rsh = n_sh ? Range{8 * cta, 8 * cta + 8} : Range{kF, kF};
         {
             const bool from_x = (p.mode == kModeLayer) || l == 0;
             const bool norm = p.mode != kModeLayer;
-            const bool router_cta = cta < kE;
+            const bool router_cta = cta >= G - kRouterCtas;
+            const int e0 = kRouterRows * (cta - (G - kRouterCtas));   // first router row (router CTAs)
             // only the router CTAs and those hosting a term-split unit read h here
             const bool need_h = router_cta || (G - 1 - cta) * kMW < M * kMW;
+            // Lane (g, q) holds 64 values of token g in warp w's 256-wide K-slice: fp32
+            // rows at positions 256 w + 64 c + 16 k + 4 q + i (v[c][4 k + i]), bf16 rows
+            // at 256 w + 64 c + 32 k + 8 q + i (v[c][8 k + i]); the four lanes of a token
+            // read contiguous 64 bytes at a time.
             float v[4][16];
-            const uint16_t *wrow = L.router_w + (size_t)cta * kH + 256 * warp + 16 * q;
-            // router row of this CTA (its K-slice positions): fetch into L1
-            // while the activations load
-            if (router_cta) {
-#pragma unroll
-                for (int c = 0; c < 4; ++c)
-                    asm volatile("prefetch.global.L1 [%0];" ::"l"(wrow + 64 * c));
-            }
-            // router bias of this CTA's expert, fetched early (off the critical path)
-            const float rbias = (router_cta && tid < M && L.router_b) ? __ldg(L.router_b + cta) : 0.0f;
             if (g < M && need_h) {
-                if (from_x)
-                    load_slice_bf16(p.x + (size_t)g * kH, warp, q, v);
-                else
-                    load_slice_f32(ws.h + (size_t)g * kH, warp, q, v);
+                if (from_x) {
+                    const uint16_t *xr = p.x + (size_t)g * kH + 256 * warp + 8 * q;
+#pragma unroll
+                    for (int c = 0; c < 4; ++c)
+#pragma unroll
+                        for (int k = 0; k < 2; ++k) {
+                            const uint4 a = *reinterpret_cast<const uint4 *>(xr + 64 * c + 32 * k);
+                            const uint32_t wd[4] = {a.x, a.y, a.z, a.w};
+#pragma unroll
+                            for (int j = 0; j < 4; ++j) {
+                                const float2 f = bf16x2_to_f32(wd[j]);
+                                v[c][8 * k + 2 * j] = f.x;
+                                v[c][8 * k + 2 * j + 1] = f.y;
+                            }
+                        }
+                } else {
+                    const float *hr = ws.h + (size_t)g * kH + 256 * warp + 4 * q;
+#pragma unroll
+                    for (int c = 0; c < 4; ++c)
+#pragma unroll
+                        for (int k = 0; k < 4; ++k) {
+                            const float4 f = ldcg4(hr + 64 * c + 16 * k);
+                            v[c][4 * k] = f.x;
+                            v[c][4 * k + 1] = f.y;
+                            v[c][4 * k + 2] = f.z;
+                            v[c][4 * k + 3] = f.w;
+                        }
+                }
             } else {
 #pragma unroll
                 for (int c = 0; c < 4; ++c)
@@ -1164,48 +1171,85 @@ __global__ void __launch_bounds__(kThreads, 1) k_fused(const __grid_constant__ P
                     ws.h[i] = init;
                 }
             }
+            // router bias of a CTA whose bias entries were not copied with its rows
+            const bool bias_copied = L.router_b && (reinterpret_cast<uintptr_t>(L.router_b) & 15u) == 0;
+            float rbias = 0.0f;
+            if (router_cta && tid < kRouterRows * M && L.router_b && !bias_copied)
+                rbias = __ldg(L.router_b + e0 + tid / M);
             {
-                // sum of squares and the router dot product on the un-normalised
-                // row; RMSNorm is a per-token scale, applied to the dot afterwards
-                float ss = 0.0f, dot = 0.0f;
+                // sum of squares and the router dot products on the un-normalised
+                // row; RMSNorm is a per-token scale, applied to the dots afterwards
+                float ss = 0.0f, dot[kRouterRows];
 #pragma unroll
                 for (int c = 0; c < 4; ++c)
 #pragma unroll
                     for (int i = 0; i < 16; ++i)
                         ss += v[c][i] * v[c][i];
+#pragma unroll
+                for (int j = 0; j < kRouterRows; ++j)
+                    dot[j] = 0.0f;
                 if (router_cta) {
+                    // the layer's router rows arrive as this CTA's first ring stage
+                    const bool got = stage_wait();
+                    const uint8_t *slot = s.ring[stage % kStages];
+                    if (got) {
 #pragma unroll
-                    for (int c = 0; c < 4; ++c) {
-                        const uint4 w0 = __ldg(reinterpret_cast<const uint4 *>(wrow + 64 * c));
-                        const uint4 w1 = __ldg(reinterpret_cast<const uint4 *>(wrow + 64 * c + 8));
-                        const uint32_t w8[8] = {w0.x, w0.y, w0.z, w0.w, w1.x, w1.y, w1.z, w1.w};
+                        for (int j = 0; j < kRouterRows; ++j) {
+                            const uint16_t *wr = reinterpret_cast<const uint16_t *>(slot) + j * kH + 256 * warp;
 #pragma unroll
-                        for (int k = 0; k < 8; ++k) {
-                            const float2 f = bf16x2_to_f32(w8[k]);
-                            dot += f.x * v[c][2 * k] + f.y * v[c][2 * k + 1];
+                            for (int c = 0; c < 4; ++c) {
+                                if (from_x) {
+#pragma unroll
+                                    for (int k = 0; k < 2; ++k) {
+                                        const uint4 w4 = *reinterpret_cast<const uint4 *>(wr + 64 * c + 32 * k + 8 * q);
+                                        const uint32_t w8[4] = {w4.x, w4.y, w4.z, w4.w};
+#pragma unroll
+                                        for (int m = 0; m < 4; ++m) {
+                                            const float2 f = bf16x2_to_f32(w8[m]);
+                                            dot[j] += f.x * v[c][8 * k + 2 * m] + f.y * v[c][8 * k + 2 * m + 1];
+                                        }
+                                    }
+                                } else {
+#pragma unroll
+                                    for (int k = 0; k < 4; ++k) {
+                                        const uint2 w2 = *reinterpret_cast<const uint2 *>(wr + 64 * c + 16 * k + 4 * q);
+                                        const float2 f0 = bf16x2_to_f32(w2.x), f1 = bf16x2_to_f32(w2.y);
+                                        dot[j] += f0.x * v[c][4 * k] + f0.y * v[c][4 * k + 1] + f1.x * v[c][4 * k + 2] +
+                                                  f1.y * v[c][4 * k + 3];
+                                    }
+                                }
+                            }
                         }
+                        if (bias_copied && tid < kRouterRows * M)
+                            rbias = reinterpret_cast<const float *>(slot + kRouterRows * kH * sizeof(uint16_t))[tid / M];
                     }
+                    stage_release();
                 }
                 ss = quad_sum(ss);
-                dot = quad_sum(dot);
+#pragma unroll
+                for (int j = 0; j < kRouterRows; ++j)
+                    dot[j] = quad_sum(dot[j]);
                 if (q == 0) {
                     s.part[warp][g] = ss;
-                    s.part2[warp][g] = dot;
+#pragma unroll
+                    for (int j = 0; j < kRouterRows; ++j)
+                        s.part2[j][warp][g] = dot[j];
                 }
                 stamp(1);
             }
             consumer_sync();
             stamp(2);
             {
-                if (router_cta && tid < M) {
+                if (router_cta && tid < kRouterRows * M) {
+                    const int j = tid / M, t = tid % M;
                     float z = 0.0f, tot = 0.0f;
 #pragma unroll
                     for (int w = 0; w < kMW; ++w) {
-                        z += s.part2[w][tid];
-                        tot += s.part[w][tid];
+                        z += s.part2[j][w][t];
+                        tot += s.part[w][t];
                     }
                     const float rt = norm ? 1.0f / sqrtf(tot / static_cast<float>(kH) + kEps) : 1.0f;
-                    __stcg(ws.logits + tid * kE + cta, z * rt + rbias);
+                    __stcg(ws.logits + t * kE + e0 + j, z * rt + rbias);
                 }
                 // Activation terms of the gate/up products, computed once per grid:
                 // unit (token t, 256-wide K-slice w) is split by warp w' of CTA
@@ -1409,14 +1453,14 @@ __global__ void __launch_bounds__(kThreads, 1) k_fused(const __grid_constant__ P
                 mbar_arrive(&s.route);
             stamp(6);
             const int U = s.n_unique[pb];
-            const Range rg = gu_routed_rows(U, cta, G);
+            const int n_gu = gu_tile_count(U, cta, G);
             // row scales of this CTA's routed gate/up rows and of its down rows,
             // copied asynchronously (cp.async); each thread waits for its copies
             // before the first routed tile, and the next exchange barrier makes
             // them visible to the reducers
-            for (int k = tid; k < rg.end - rg.begin; k += kConsumers) {
-                const int pos = rg.begin + k;
-                const size_t row = (size_t)s.experts[pb][pos / kF] * kF + pos % kF;
+            for (int k = tid; k < 8 * (n_gu - n_sh); k += kConsumers) {
+                const int x = cta + (n_sh + k / 8) * G - kGuTiles;
+                const size_t row = (size_t)s.experts[pb][x / kGuTiles] * kF + 8 * (x % kGuTiles) + k % 8;
                 cp_async4(&s.sc_g[k], L.gate_s + row);
                 cp_async4(&s.sc_u[k], L.up_s + row);
             }
@@ -1437,8 +1481,6 @@ __global__ void __launch_bounds__(kThreads, 1) k_fused(const __grid_constant__ P
             }
             // the shared expert's rows of this CTA first (their copies were issued
             // before the routing was known), then its routed rows
-            const int n_sh = (rsh.end - rsh.begin + 7) / 8;
-            int pos = rg.begin;
             float pend[2][4];
             int4 pend_m = make_int4(0, 0, 0, 0);
             bool have_pend = false;
@@ -1450,24 +1492,24 @@ __global__ void __launch_bounds__(kThreads, 1) k_fused(const __grid_constant__ P
                     cp_async_wait_all();
                     scales_ready = true;
                 }
+                if (it >= n_gu)
+                    break;
                 if (it < n_sh) {
-                    i = rsh.begin + 8 * it;
-                    nv = min(8, rsh.end - i);
+                    i = rsh.begin;
+                    nv = 8;
                     aslot = kSharedSlot;
-                    k0 = kMaxGuRows + 8 * it;
+                    k0 = kMaxGuRows;
                 } else {
-                    if (pos >= rg.end)
-                        break;
-                    const int u = pos / kF;
-                    i = pos % kF;
-                    nv = min(min(8, kF - i), rg.end - pos);
+                    const int x = cta + it * G - kGuTiles;
+                    const int u = x / kGuTiles;
+                    i = 8 * (x % kGuTiles);
+                    nv = 8;
                     aslot = u;
                     cslot = u;
-                    k0 = pos - rg.begin;
-                    pos += nv;
+                    k0 = 8 * (it - n_sh);
                 }
                 const int4 m = make_int4(kTileGateUp | (aslot << 2), i, nv | (k0 << 8), cslot);
-                const bool last = !(it + 1 < n_sh || pos < rg.end);
+                const bool last = it + 1 >= n_gu;
                 if (!have_pend) {
                     gu_tile(pend[0]);
                     pend_m = m;
