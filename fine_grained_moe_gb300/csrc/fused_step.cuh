@@ -56,8 +56,8 @@ constexpr int kStages = 4;                    // ring slots
 constexpr int kRowStride = 2880;              // smem stride of a 2816-byte row (conflict-free 16-byte reads)
 constexpr int kSlotBytes = 16 * kRowStride;   // 46080
 constexpr int kDownTiles = 4;                 // 16-row down tiles per ring slot (64 x 704 bytes)
-constexpr int kRouterCtas = 32;               // the last 32 CTAs compute the router logits,
-constexpr int kRouterRows = FGM_EXPERTS / kRouterCtas;   // 4 rows each (fewer CTAs read the residual)
+constexpr int kRouterCtas = 64;               // the last 64 CTAs compute the router logits,
+constexpr int kRouterRows = FGM_EXPERTS / kRouterCtas;   // 2 rows each (fewer CTAs read the residual)
 constexpr int kTerms = 3;                     // E4M3 terms per activation
 constexpr int kSharedSlot = kMaxSlots - 1;
 constexpr uint32_t kActPending = 0x7FC0DEADu;   // NaN marker: activation row not written yet
@@ -819,13 +819,17 @@ __global__ void __launch_bounds__(kThreads, 1) k_fused(const __grid_constant__ P
                     const int e0 = kRouterRows * (cta - (G - kRouterCtas));
                     const bool bias = L.router_b && (reinterpret_cast<uintptr_t>(L.router_b) & 15u) == 0;
                     constexpr uint32_t kRowsBytes = kRouterRows * kH * sizeof(uint16_t);
-                    uint8_t *dst = claim(kRowsBytes + (bias ? kRouterRows * sizeof(float) : 0u));
+                    uint8_t *dst = claim(kRowsBytes + (bias ? kE * sizeof(float) : 0u));
                     if (!dst)
                         break;
                     bulk_g2s(dst, L.router_w + (size_t)e0 * kH, kRowsBytes, &s.full[stage % kStages]);
                     if (bias)
-                        bulk_g2s(dst + kRowsBytes, L.router_b + e0, kRouterRows * sizeof(float), &s.full[stage % kStages]);
+                        bulk_g2s(dst + kRowsBytes, L.router_b, kE * sizeof(float), &s.full[stage % kStages]);
                     ++stage;
+                    // the next layer's rows into L2 now: their copy is issued near the
+                    // end of this layer, when HBM is busiest
+                    if (l + 1 < n_layers)
+                        prefetch_l2(p.layers[l + 1].router_w + (size_t)e0 * kH, kRowsBytes);
                 }
                 if (cta < kGuTiles)
                     gu_rows(L, kShared, 8 * cta, 8);
@@ -1221,7 +1225,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_fused(const __grid_constant__ P
                             }
                         }
                         if (bias_copied && tid < kRouterRows * M)
-                            rbias = reinterpret_cast<const float *>(slot + kRouterRows * kH * sizeof(uint16_t))[tid / M];
+                            rbias = reinterpret_cast<const float *>(slot + kRouterRows * kH * sizeof(uint16_t))[e0 + tid / M];
                     }
                     stage_release();
                 }
@@ -1252,26 +1256,38 @@ __global__ void __launch_bounds__(kThreads, 1) k_fused(const __grid_constant__ P
                     __stcg(ws.logits + t * kE + e0 + j, z * rt + rbias);
                 }
                 // Activation terms of the gate/up products, computed once per grid:
-                // unit (token t, 256-wide K-slice w) is split by warp w' of CTA
-                // G - 1 - u / 11 (u = 11 t + w, w' = u % 11), 8 values a lane, into
-                // kTerms E4M3 terms under a power-of-two scale per unit.
-                const int u = (G - 1 - cta) * kMW + warp;
-                if (u < M * kMW) {
-                    const int t = u / kMW, w = u % kMW;
+                // unit (token t, 256-wide K-slice w) is split by warp w of CTA G - 1 - t
+                // (a router CTA: it holds the slice in lanes 4 t .. 4 t + 3), 8 values a
+                // lane after a pass through shared memory (the exchange buffer is idle
+                // in phase A), into kTerms E4M3 terms under a power-of-two scale per unit.
+                const int t = G - 1 - cta;
+                if (t < M) {
+                    const int w = warp;
                     const int k0 = 256 * w + 8 * lane;
-                    float xv[8];
-                    if (from_x) {
-                        const uint4 a = *reinterpret_cast<const uint4 *>(p.x + (size_t)t * kH + k0);
-                        const uint32_t wd[4] = {a.x, a.y, a.z, a.w};
+                    float *sx = reinterpret_cast<float *>(&s.red[0][0][0][0]) + 256 * warp;
+                    if (g == t) {
 #pragma unroll
-                        for (int k = 0; k < 4; ++k) {
-                            const float2 f = bf16x2_to_f32(wd[k]);
-                            xv[2 * k] = f.x;
-                            xv[2 * k + 1] = f.y;
+                        for (int c = 0; c < 4; ++c) {
+                            if (from_x) {
+#pragma unroll
+                                for (int k = 0; k < 2; ++k) {
+                                    float4 *d = reinterpret_cast<float4 *>(sx + 64 * c + 32 * k + 8 * q);
+                                    d[0] = make_float4(v[c][8 * k], v[c][8 * k + 1], v[c][8 * k + 2], v[c][8 * k + 3]);
+                                    d[1] = make_float4(v[c][8 * k + 4], v[c][8 * k + 5], v[c][8 * k + 6], v[c][8 * k + 7]);
+                                }
+                            } else {
+#pragma unroll
+                                for (int k = 0; k < 4; ++k)
+                                    *reinterpret_cast<float4 *>(sx + 64 * c + 16 * k + 4 * q) =
+                                        make_float4(v[c][4 * k], v[c][4 * k + 1], v[c][4 * k + 2], v[c][4 * k + 3]);
+                            }
                         }
-                    } else {
-                        const float4 a = ldcg4(ws.h + (size_t)t * kH + k0);
-                        const float4 b = ldcg4(ws.h + (size_t)t * kH + k0 + 4);
+                    }
+                    __syncwarp();
+                    float xv[8];
+                    {
+                        const float4 a = *reinterpret_cast<const float4 *>(sx + 8 * lane);
+                        const float4 b = *reinterpret_cast<const float4 *>(sx + 8 * lane + 4);
                         xv[0] = a.x; xv[1] = a.y; xv[2] = a.z; xv[3] = a.w;
                         xv[4] = b.x; xv[5] = b.y; xv[6] = b.z; xv[7] = b.w;
                     }
