@@ -7,13 +7,16 @@ Workload (one "step"): the full verify step at M = 5 tokens (gamma = 4):
 per-layer seeds 1..30), pre-RMSNorm and residual per layer, a final RMSNorm,
 the 262,144 x 2816 bf16 tied lm_head with argmax, and greedy acceptance of 4
 drafts that copy the target's argmax with probability 0.7. Eight input batches
-(hidden seeds 31..38) rotate across steps. Weights are random-init, inputs
-synthetic.
+(hidden seeds 31..38) and 64 draft seeds (33..96, seed k on batch k mod 8)
+rotate across steps. Weights are random-init, inputs synthetic.
 
-Metric: verified tokens/s (accepted drafts + 1 per step) with every input
-resident in HBM, and the achieved HBM GB/s of the step's unique weight bytes
-against the measured copy bandwidth. A step streams > 5 GB of weights, far
-above the 129 MB L2, so no flush is needed between steps.
+Metric: verified tokens/s with every input resident in HBM, and the achieved
+HBM GB/s of the step's unique weight bytes against the measured copy
+bandwidth. `value` counts 1 + E[a] tokens per step, E[a] = 0.7 + 0.7^2 +
+0.7^3 + 0.7^4 = 1.7731 being the expected accepted count of the draft recipe;
+the line also gives tokens/s at the accepted counts of the timed steps and the
+mean accepted count over all 64 draft seeds. A step streams > 5 GB of weights,
+far above the 129 MB L2, so no flush is needed between steps.
 
   python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
 """
@@ -39,6 +42,8 @@ N_LAYERS = 30
 N_BATCHES = 8
 HIDDEN_SEED0 = 31
 DRAFT_SEED0 = 33
+N_DRAFT_SEEDS = 64
+P_COPY = 0.7   # probability that a draft copies the target's argmax
 EMB_SEED = 32
 WORKLOAD = ("full verify step: 30-layer FP8 MoE stack (Gemma-4-26B-A4B shape, Zipf s=1.1) + "
             "final RMSNorm + 262144x2816 bf16 tied lm_head argmax + greedy accept, M=5 (gamma=4)")
@@ -48,6 +53,34 @@ ROOFLINE_TARGET_GBS = 8000.0
 
 def log(*a):
     print(*a, file=sys.stderr, flush=True)
+
+
+def expected_accept(gamma: int, p: float = P_COPY) -> float:
+    """Expected greedy accepted count when each draft copies the target's argmax
+    with probability p, independently: a >= j exactly when the first j drafts
+    all copy it, so E[a] = sum_{j=1..gamma} p^j (a uniform draft that hits the
+    argmax by chance, 1 in 262,144, is neglected)."""
+    return sum(p ** j for j in range(1, gamma + 1))
+
+
+def cpu_model() -> str:
+    """The host CPU's model name (lscpu, else /proc/cpuinfo, else the machine type)."""
+    try:
+        out = subprocess.run(["lscpu"], capture_output=True, text=True, timeout=10).stdout
+        for line in out.splitlines():
+            if line.startswith("Model name:"):
+                return line.split(":", 1)[1].strip()
+    except Exception:
+        pass
+    try:
+        with open("/proc/cpuinfo") as f:
+            for line in f:
+                if line.lower().startswith("model name"):
+                    return line.split(":", 1)[1].strip()
+    except OSError:
+        pass
+    import platform
+    return platform.machine()
 
 
 def measured_peaks():
@@ -152,13 +185,13 @@ class ClockSampler:
 
 
 # ---------------------------------------------------------------- workload
-def make_workload(device):
+def make_workload(device, n_layers=N_LAYERS, vocab=262144):
     import torch
 
     import synth
     t0 = time.time()
-    layers = [synth.layer(l + 1, device=device, s=S_ZIPF) for l in range(N_LAYERS)]
-    emb = synth.embedding(EMB_SEED, device=device)
+    layers = [synth.layer(l + 1, device=device, s=S_ZIPF) for l in range(n_layers)]
+    emb = synth.embedding(EMB_SEED, device=device, vocab=vocab)
     xs = [synth.hidden_states(HIDDEN_SEED0 + b, M, device=device) for b in range(N_BATCHES)]
     torch.cuda.synchronize()
     log(f"[bench] generated weights in {time.time() - t0:.1f}s")
@@ -196,6 +229,41 @@ def cpu_oracle_step(layers, emb, x, draft_seed, log_prefix="[oracle]"):
     a, nxt = oracle.spec_verify(am, draft)
     log(f"{log_prefix} full step: {compute:.2f}s compute, accepted {a}, cores {oracle.num_threads()}")
     return compute, a, nxt, oracle.num_threads()
+
+
+def cpu_oracle_single_thread(layers, emb, x, n_layers=2):
+    """The oracle on one thread, on a bounded sample of the step: the first
+    n_layers layers and the same fraction of the lm_head rows, scaled to a full
+    step. Returns (seconds per full step, sample description)."""
+    import numpy as np
+    import torch
+
+    import oracle
+    frac = n_layers / N_LAYERS
+    host = []
+    for p in layers[:n_layers]:
+        h = {k: (None if v is None else v.detach().cpu()) for k, v in p.items()}
+        host.append(oracle.LayerParams(
+            router_w=h["router_w"].view(torch.int16).numpy().view(np.uint16),
+            router_b=None if h["router_b"] is None else h["router_b"].numpy(),
+            gate_q=h["gate_q"].numpy(), gate_s=h["gate_s"].numpy(), up_q=h["up_q"].numpy(),
+            up_s=h["up_s"].numpy(), down_q=h["down_q"].numpy(), down_s=h["down_s"].numpy()))
+    v_rows = int(emb.shape[0] * frac)
+    e = emb[:v_rows].detach().cpu().view(torch.int16).numpy().view(np.uint16)
+    prev = oracle.num_threads()
+    oracle.set_num_threads(1)
+    try:
+        t0 = time.perf_counter()
+        h = x.detach().cpu().double().numpy()
+        for L in host:
+            h = oracle.stack_layer(L, h).y
+        oracle.lm_head(e, oracle.bf16_to_f64(oracle.bf16_round(oracle.rmsnorm(h))))
+        secs = (time.perf_counter() - t0) / frac
+    finally:
+        oracle.set_num_threads(prev)
+    log(f"[oracle] one thread: {secs:.2f}s per full step (scaled from {n_layers} layers)")
+    return secs, (f"one thread: first {n_layers} of {N_LAYERS} layers + {v_rows} of {emb.shape[0]} lm_head rows "
+                  f"on batch 0, scaled x{1 / frac:.0f}")
 
 
 # ---------------------------------------------------------------- phase trace
@@ -297,28 +365,39 @@ def run_ours(args, rank, world):
     torch.cuda.set_device(dev)
     fgm.lib()
     fgm.select_path(fgm.PATH_FUSED if args.path == "fused" else fgm.PATH_STAGED)
-    layers, emb, xs = make_workload(dev)
+    nl, V = args.layers, args.vocab
+    full_size = (nl, V) == (N_LAYERS, 262144)
+    if args.phase_trace and not full_size:
+        raise SystemExit("--phase-trace needs the full-size step")
+    layers, emb, xs = make_workload(dev, nl, V)
     arr = fgm.layers_array(layers)
     ws = fgm.Workspace(dev)
     stream = torch.cuda.current_stream()
 
-    # per-batch routing (unique experts per layer) and drafts from the target's argmax
-    uniq, drafts = [], []
-    trace = torch.empty((N_LAYERS, M, 8), dtype=torch.int32, device=dev)
+    # per-batch routing (unique experts per layer) and the target's argmax; draft
+    # seed k drafts for batch k mod 8
+    uniq, ams = [], []
+    trace = torch.empty((nl, M, 8), dtype=torch.int32, device=dev)
     for b, x in enumerate(xs):
         fgm.moe_stack_fwd(layers, x, ids_trace=trace, ws=ws)
         tr = trace.cpu()
-        uniq.append([len(torch.unique(tr[l])) for l in range(N_LAYERS)])
+        uniq.append([len(torch.unique(tr[l])) for l in range(nl)])
         am = torch.empty(M, dtype=torch.int32, device=dev)
         fgm.verify_step(layers, emb, x, torch.zeros(GAMMA, dtype=torch.int32, device=dev), argmax=am,
                         ws=ws, _arr=arr)
-        drafts.append(synth.drafts(DRAFT_SEED0 + b, am.cpu()).to(dev))
-    step_bytes = [traffic.step_bytes(u) for u in uniq]
+        ams.append(am.cpu())
+    drafts = [synth.drafts(DRAFT_SEED0 + k, ams[k % N_BATCHES]).to(dev) for k in range(N_DRAFT_SEEDS)]
+    step_bytes = [traffic.step_bytes(u, vocab=V) for u in uniq]
     K, W = args.steps, args.warmup
+    # accepted count of every (batch, draft seed) pair, untimed
+    acc_all = torch.zeros((N_DRAFT_SEEDS, 2), dtype=torch.int32, device=dev)
+    for k in range(N_DRAFT_SEEDS):
+        fgm.verify_step(layers, emb, xs[k % N_BATCHES], drafts[k], out=acc_all[k], ws=ws, _arr=arr)
+    accepted_mean_all = float(acc_all[:, 0].double().mean())
     outs = torch.zeros((K, 2), dtype=torch.int32, device=dev)
     for i in range(W):
-        b = i % N_BATCHES
-        fgm.verify_step(layers, emb, xs[b], drafts[b], ws=ws, _arr=arr)
+        k = i % N_DRAFT_SEEDS
+        fgm.verify_step(layers, emb, xs[k % N_BATCHES], drafts[k], ws=ws, _arr=arr)
     torch.cuda.synchronize()
 
     ev = [torch.cuda.Event(enable_timing=True) for _ in range(K + 1)]
@@ -328,8 +407,8 @@ def run_ours(args, rank, world):
     with ClockSampler(dev.index) as clk:
         ev[0].record(stream)
         for i in range(K):
-            b = i % N_BATCHES
-            fgm.verify_step(layers, emb, xs[b], drafts[b], out=outs[i], ws=ws, _arr=arr)
+            k = i % N_DRAFT_SEEDS
+            fgm.verify_step(layers, emb, xs[k % N_BATCHES], drafts[k], out=outs[i], ws=ws, _arr=arr)
             ev[i + 1].record(stream)
         torch.cuda.synchronize()
     if world > 1:
@@ -339,7 +418,7 @@ def run_ours(args, rank, world):
     status = ws.status()
     acc = outs.cpu()
     tokens = int(acc[:, 0].sum()) + K
-    bytes_total = sum(step_bytes[i % N_BATCHES] for i in range(K))
+    bytes_total = sum(step_bytes[(i % N_DRAFT_SEEDS) % N_BATCHES] for i in range(K))
 
     if args.phase_trace:
         write_phase_trace(args.phase_trace, fgm, layers, emb, xs[0], drafts[0], ws, arr, dev)
@@ -349,12 +428,12 @@ def run_ours(args, rank, world):
     d_h = [d.cpu().pin_memory() for d in drafts]
     o_h = torch.empty(2, dtype=torch.int32).pin_memory()
     for i in range(min(W, 3)):
-        fgm.verify_step_host(layers, emb, x_h[i % N_BATCHES], d_h[i % N_BATCHES], out_host=o_h, ws=ws, _arr=arr)
+        fgm.verify_step_host(layers, emb, x_h[i % N_BATCHES], d_h[i], out_host=o_h, ws=ws, _arr=arr)
     t0 = time.perf_counter()
     e2e_tokens = 0
     for i in range(K):
-        b = i % N_BATCHES
-        fgm.verify_step_host(layers, emb, x_h[b], d_h[b], out_host=o_h, ws=ws, _arr=arr)
+        k = i % N_DRAFT_SEEDS
+        fgm.verify_step_host(layers, emb, x_h[k % N_BATCHES], d_h[k], out_host=o_h, ws=ws, _arr=arr)
         e2e_tokens += int(o_h[0]) + 1
     e2e_s = time.perf_counter() - t0
 
@@ -371,9 +450,10 @@ def run_ours(args, rank, world):
     ms = total_ms_max / K
     achieved = bytes_total / K / (ms * 1e-3) / 1e9
     clocks = clk.summary()
+    ea = expected_accept(GAMMA)
     line = {
         "metric": METRIC,
-        "value": round(tokens_all / (total_ms_max * 1e-3), 2),
+        "value": round(world * K * (1 + ea) / (total_ms_max * 1e-3), 2),
         "unit": "tokens/s",
         "n_gpus": world,
         "steps": K,
@@ -385,14 +465,20 @@ def run_ours(args, rank, world):
         "dtype": "e4m3 weights, fp32 accumulate; bf16 lm_head",
         "data": "synthetic (random-init weights of the Gemma-4-26B-A4B MoE shape, seeded)",
         "config": {
-            "workload": WORKLOAD, "M": M, "gamma": GAMMA, "zipf_s": S_ZIPF, "layers": N_LAYERS,
-            "vocab": 262144, "batches": N_BATCHES, "parallelism": f"replicas x{world}",
+            "workload": WORKLOAD if full_size else
+            f"profiling case: {nl}-layer FP8 MoE stack + {V}-word bf16 lm_head, otherwise as the full step",
+            "M": M, "gamma": GAMMA, "zipf_s": S_ZIPF, "layers": nl, "vocab": V, "batches": N_BATCHES, "parallelism": f"replicas x{world}",
             "l2": "no flush: each step streams > 5 GB of weights (L2 is 129 MB)",
             "mean_unique_experts_per_layer": round(statistics.mean(sum(uniq, [])), 2),
+            "draft_seeds": N_DRAFT_SEEDS,
+            "tokens_per_step": f"value counts 1 + E[a] = {1 + ea:.4f} (E[a] = sum of 0.7^j, j = 1..4)",
         },
         "hbm_gbs": round(achieved, 1),
         "frac_of_8tbs": round(achieved / ROOFLINE_TARGET_GBS, 4),
+        "expected_accept": round(ea, 4),
+        "tokens_per_s_measured_accept": round(tokens_all / (total_ms_max * 1e-3), 2),
         "accepted_per_step": round((tokens - K) / K, 3),
+        "accepted_mean_all_draft_seeds": round(accepted_mean_all, 3),
         "p50_ms": round(statistics.median(per_step), 4),
         "p99_ms": round(sorted(per_step)[min(K - 1, int(0.99 * K))], 4),
         "path": args.path,
@@ -405,22 +491,28 @@ def run_ours(args, rank, world):
             "peak_kind": f"{peak_kind} copy bandwidth",
             "unit": "GB/s",
             "frac": round(achieved / peak, 4),
-            "traffic": (captured_traffic() if args.path == "fused" else None),
+            "traffic": (captured_traffic() if args.path == "fused" and full_size else None),
             "algorithmic_bytes_per_launch": int(bytes_total / K),
         },
-        "e2e": {"value": round(e2e_tok_all / e2e_max, 2), "unit": "tokens/s",
+        "e2e": {"value": round(world * K * (1 + ea) / e2e_max, 2), "unit": "tokens/s",
+                "measured_accept_value": round(e2e_tok_all / e2e_max, 2),
                 "h2d_bytes_per_step": M * 2816 * 2 + GAMMA * 4, "d2h_bytes_per_step": 8},
-        "gpu_launches": K * (1 if args.path == "fused" else 1 + N_LAYERS * 5 + 3),
+        "gpu_launches": K * (1 if args.path == "fused" else 1 + nl * 5 + 3),
         "clocks": {"sm_mhz": clocks["sm_mhz"], "sm_max_mhz": clocks["sm_max_mhz"],
                    "reasons": clocks["reasons"]},
         "status": status,
     }
-    if world == 1 and not args.no_cpu_baseline:
+    if world == 1 and full_size and not args.no_cpu_baseline:
         secs, a, _, cores = cpu_oracle_step(layers, emb, xs[0], DRAFT_SEED0)
-        line["cpu_baseline"] = {"value": round((a + 1) / secs, 4), "unit": "tokens/s", "cores": cores,
-                                "kind": "oracle",
-                                "sample": "one full verify step (30 layers + lm_head + accept) on batch 0; "
-                                          "host weight copies untimed"}
+        secs1, sample1 = cpu_oracle_single_thread(layers, emb, xs[0])
+        line["cpu_baseline"] = {"value": round((1 + ea) / secs, 4), "unit": "tokens/s", "cores": cores,
+                                "kind": "oracle", "cpu_model": cpu_model(),
+                                "sample": "one full verify step (30 layers + lm_head + accept) on batch 0, "
+                                          f"1 + E[a] tokens; host weight copies untimed; accepted count {a}",
+                                "ms_per_step": round(secs * 1e3, 1),
+                                "single_thread": {"value": round((1 + ea) / secs1, 4), "unit": "tokens/s",
+                                                  "cores": 1, "ms_per_step": round(secs1 * 1e3, 1),
+                                                  "sample": sample1}}
     return line
 
 
@@ -541,6 +633,8 @@ def run_sweep(args):
             gbs = sum(nbytes[i % N_BATCHES] for i in range(K)) / (ms * 1e-3) / 1e9
             print(json.dumps({"case": "sweep", "M": m, "gamma": m - 1, "zipf_s": s_zipf,
                               "tokens_per_s": round(tokens / (ms * 1e-3), 1),
+                              "tokens_per_s_at_expected_accept": round(K * (1 + expected_accept(m - 1))
+                                                                       / (ms * 1e-3), 1),
                               "ms_per_step": round(ms / K, 4), "accepted_per_step": round((tokens - K) / K, 3),
                               "hbm_gbs": round(gbs, 1), "frac_of_peak": round(gbs / peak, 4),
                               "status": ws.status()}), flush=True)
@@ -602,6 +696,7 @@ def run_verify_fp8(args):
             "workload": "full verify step, M=5 (gamma=4), Zipf s=1.1, 30 layers, "
                         "262144x2816 E4M3 lm_head with fp32 row scales",
             "steps": K, "warmup": W, "tokens_per_s": round(tokens / (ms * 1e-3), 2),
+            "tokens_per_s_at_expected_accept": round(K * (1 + expected_accept(GAMMA)) / (ms * 1e-3), 2),
             "ms_per_step": round(ms / K, 4), "accepted_per_step": round((tokens - K) / K, 3),
             "algorithmic_bytes_per_step": int(statistics.mean(nbytes)),
             "hbm_gbs": round(gbs, 1), "frac_of_peak": round(gbs / peak, 4), "peak": peak, "peak_kind": kind,
@@ -657,7 +752,7 @@ def run_reference(args, rank, world):
         sample()
     times = [sample() for _ in range(args.steps)]
     ms = 1e3 * statistics.mean(times)
-    value = (a + 1) / (ms * 1e-3)
+    value = (1 + expected_accept(GAMMA)) / (ms * 1e-3)
     return {
         "impl": "reference", "metric": METRIC, "value": round(value, 4), "unit": "tokens/s",
         "n_gpus": 1, "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms, 2),
@@ -666,8 +761,10 @@ def run_reference(args, rank, world):
         "config": {"workload": WORKLOAD, "M": M, "gamma": GAMMA, "zipf_s": S_ZIPF, "layers": N_LAYERS,
                    "vocab": 262144, "parallelism": "single process, OpenMP"},
         "cpu_baseline": {"value": round(value, 4), "unit": "tokens/s", "cores": cores, "kind": "oracle",
+                         "cpu_model": cpu_model(),
                          "sample": f"per step: first {n_layers} of 30 layers + {v_rows} of 262144 lm_head rows "
-                                   f"on batch 0, scaled x{1 / frac:.2f}; accepted count {a} from one full step"},
+                                   f"on batch 0, scaled x{1 / frac:.2f}; 1 + E[a] tokens per step as in the "
+                                   f"CUDA arm (accepted count of the full step on batch 0: {a})"},
         "e2e": {"value": round(value, 4), "unit": "tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
     }
 
@@ -675,12 +772,16 @@ def run_reference(args, rank, world):
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--steps", type=int, default=64)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=("ours", "reference"), default="ours")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--path", choices=("fused", "staged"), default="fused",
                     help="persistent kernel (default) or one launch per stage")
+    ap.add_argument("--layers", type=int, default=N_LAYERS,
+                    help="verify case only: stack depth (a smaller case for ncu captures; default 30)")
+    ap.add_argument("--vocab", type=int, default=262144,
+                    help="verify case only: lm_head rows (a smaller case for ncu captures; default 262144)")
     ap.add_argument("--phase-trace", metavar="PATH", default=None,
                     help="after timing, run one traced step and write a per-phase summary to PATH")
     ap.add_argument("--case", choices=("verify", "layer", "lm_head", "lm_head_fp8", "verify_fp8", "sweep"),

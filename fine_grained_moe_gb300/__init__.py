@@ -69,6 +69,9 @@ def lib() -> ctypes.CDLL:
             "fgm_verify_step": (ci, [LP, ci, vp, i64, vp, vp, ci, vp, vp, vp, sz, vp]),
             "fgm_verify_step_host": (ci, [LP, ci, vp, i64, vp, vp, ci, vp, vp, sz, vp]),
             "fgm_verify_step_fp8_head": (ci, [LP, ci, vp, vp, i64, vp, vp, ci, vp, vp, vp, sz, vp]),
+            "fgm_lm_head_sample": (ci, [vp, i64, vp, ci, ctypes.c_float, vp, vp, vp, vp, vp, vp, vp, sz, vp]),
+            "fgm_verify_step_sample": (ci, [LP, ci, vp, i64, vp, vp, ci, ctypes.c_float, vp, vp, vp, vp, vp, vp,
+                                            sz, vp]),
             "fgm_read_status": (ci, [vp, sz, ci, vp, vp]),
             "fgm_select_path": (ci, [ci]),
             "fgm_set_phase_trace": (ci, [vp, sz]),
@@ -315,6 +318,53 @@ def lm_head_argmax_fp8(emb_q: torch.Tensor, emb_s: torch.Tensor, h: torch.Tensor
     _check(lib().fgm_lm_head_argmax_fp8(_ptr(emb_q), _ptr(emb_s), V, _ptr(h), M, _ptr(argmax),
                                         _ptr(maxlogit), ws.ptr, ws.nbytes, _stream(stream)))
     return argmax
+
+
+def _sample_args(M: int, V: int, device, draft, u_acc, u_next, z, out):
+    if u_next is None or u_next.dtype != torch.float32 or u_next.numel() != M:
+        raise FgmError(f"u_next must be fp32 [{M}]")
+    if M > 1 and (draft is None or u_acc is None or u_acc.dtype != torch.float32 or u_acc.numel() != M - 1
+                  or draft.dtype != torch.int32 or draft.numel() != M - 1):
+        raise FgmError(f"draft (int32) and u_acc (fp32) must have M - 1 = {M - 1} elements")
+    z = torch.empty((M, V), dtype=torch.float32, device=device) if z is None else z
+    if z.dtype != torch.float32 or tuple(z.shape) != (M, V) or not z.is_contiguous():
+        raise FgmError(f"z must be contiguous fp32 [{M}, {V}]")
+    out = torch.empty(2, dtype=torch.int32, device=device) if out is None else out
+    return z, out
+
+
+def lm_head_sample(emb: torch.Tensor, h: torch.Tensor, T: float, draft: torch.Tensor | None,
+                   u_acc: torch.Tensor | None, u_next: torch.Tensor, z: torch.Tensor | None = None,
+                   argmax: torch.Tensor | None = None, out: torch.Tensor | None = None,
+                   ws: Workspace | None = None, stream=None) -> tuple[torch.Tensor, torch.Tensor]:
+    """Speculative sampling verify at temperature T on the lm_head logits of the
+    M bf16 rows h; returns (out int32 [2] = {accepted drafts, emitted token},
+    z fp32 [M, V] logits)."""
+    M = _m(h)
+    V = int(emb.shape[0])
+    z, out = _sample_args(M, V, h.device, draft, u_acc, u_next, z, out)
+    ws = _ws(ws, h.device)
+    _check(lib().fgm_lm_head_sample(_ptr(emb), V, _ptr(h), M, float(T), _ptr(draft) if M > 1 else None,
+                                    _ptr(u_acc) if M > 1 else None, _ptr(u_next), _ptr(z), _ptr(argmax),
+                                    _ptr(out), ws.ptr, ws.nbytes, _stream(stream)))
+    return out, z
+
+
+def verify_step_sample(layers, emb: torch.Tensor, x: torch.Tensor, T: float, draft: torch.Tensor | None,
+                       u_acc: torch.Tensor | None, u_next: torch.Tensor, z: torch.Tensor | None = None,
+                       argmax: torch.Tensor | None = None, out: torch.Tensor | None = None,
+                       ws: Workspace | None = None, stream=None, _arr=None) -> tuple[torch.Tensor, torch.Tensor]:
+    """Stack + final RMSNorm + lm_head + speculative sampling at temperature T;
+    returns (out int32 [2] = {accepted drafts, emitted token}, z fp32 [M, V])."""
+    M = _m(x)
+    V = int(emb.shape[0])
+    z, out = _sample_args(M, V, x.device, draft, u_acc, u_next, z, out)
+    ws = _ws(ws, x.device)
+    arr = _layers_array(layers) if _arr is None else _arr
+    _check(lib().fgm_verify_step_sample(arr, len(arr), _ptr(emb), V, _ptr(x), _ptr(draft) if M > 1 else None, M,
+                                        float(T), _ptr(u_acc) if M > 1 else None, _ptr(u_next), _ptr(z),
+                                        _ptr(argmax), _ptr(out), ws.ptr, ws.nbytes, _stream(stream)))
+    return out, z
 
 
 def spec_verify(target: torch.Tensor, draft: torch.Tensor, out: torch.Tensor | None = None,

@@ -48,6 +48,7 @@ struct Ws {
                        // [kSyncLmHeadDone] CTAs done in the FP8 lm_head
     uint8_t *xterms;   // [8][3][2816] E4M3 terms of the gate/up input of the current layer
     float *xscale;     // [8][11] their power-of-two scale per token and 256-wide K-slice
+    float *part_sum;   // [kMaxParts][8] sampling: per-CTA sum of exp((z - part_val) / T)
 };
 
 __host__ __device__ inline size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
@@ -55,7 +56,7 @@ __host__ __device__ inline size_t align_up(size_t x, size_t a) { return (x + a -
 // Byte offsets of every region; the same function serves host and device.
 struct WsOffsets {
     size_t h, xn, acc, logits, meta, comb, act, ids, wts, part_val, part_idx, hb, argmax, io_x,
-        io_draft, io_out, status, sync, xterms, xscale, total;
+        io_draft, io_out, status, sync, xterms, xscale, part_sum, total;
 };
 
 inline WsOffsets ws_offsets()
@@ -87,6 +88,7 @@ inline WsOffsets ws_offsets()
     o.sync = take(sizeof(unsigned) * 128);
     o.xterms = take(static_cast<size_t>(kMaxM) * 3 * kH);
     o.xscale = take(sizeof(float) * kMaxM * 11);
+    o.part_sum = take(sizeof(float) * kMaxParts * kMaxM);
     o.total = p;
     return o;
 }
@@ -116,6 +118,7 @@ inline Ws ws_carve(void *base)
     w.sync = reinterpret_cast<unsigned *>(b + o.sync);
     w.xterms = reinterpret_cast<uint8_t *>(b + o.xterms);
     w.xscale = reinterpret_cast<float *>(b + o.xscale);
+    w.part_sum = reinterpret_cast<float *>(b + o.part_sum);
     return w;
 }
 

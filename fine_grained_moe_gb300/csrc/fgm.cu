@@ -1,6 +1,7 @@
 // C ABI of the library (declared in include/fgm.h): argument validation,
 // workspace carving and launch sequencing. Every stage of the step runs in
 // the CUDA kernels of basic_kernels.cuh / fused_step.cuh / lm_head_fp8.cuh.
+#include <cmath>
 #include <stdarg.h>
 #include <stdio.h>
 #include <string.h>
@@ -549,6 +550,82 @@ int fgm_verify_step(const fgm_layer *layers, int n_layers, const uint16_t *emb, 
     FGM_TRY(device_ready(&sms));
     return verify_step_impl(layers, n_layers, emb, V, x, draft, M, argmax, out, ws,
                             static_cast<cudaStream_t>(stream), sms);
+}
+
+namespace fgm {
+namespace {
+
+int check_sample_args(int M, float T, const int32_t *draft, const float *u_acc, const float *u_next, float *z,
+                      int32_t *out)
+{
+    if (!(T > 0.0f) || !std::isfinite(T) || !std::isfinite(1.0f / T))
+        return fail(FGM_ERR_INVALID_ARG, "temperature T = %g: needs a finite T > 0 with 1/T finite", (double)T);
+    if (!u_next || !z || !out || (M > 1 && (!draft || !u_acc)))
+        return fail(FGM_ERR_INVALID_ARG, "u_next/z/out NULL, or draft/u_acc NULL with M > 1");
+    if ((reinterpret_cast<uintptr_t>(z) | reinterpret_cast<uintptr_t>(u_next) |
+         reinterpret_cast<uintptr_t>(u_acc)) & 3u)
+        return fail(FGM_ERR_INVALID_ARG, "z/u_next/u_acc not 4-byte aligned");
+    return FGM_OK;
+}
+
+void set_sample(fused::Params &prm, float T, const int32_t *draft, const float *u_acc, const float *u_next,
+                float *z, int32_t *argmax, int32_t *out, const Ws &w)
+{
+    prm.z = z;
+    prm.inv_t = 1.0f / T;
+    prm.draft = draft;
+    prm.u_acc = u_acc;
+    prm.u_next = u_next;
+    prm.argmax = argmax ? argmax : w.argmax;
+    prm.out = out;
+}
+
+}  // namespace
+}  // namespace fgm
+
+int fgm_lm_head_sample(const uint16_t *emb, int64_t V, const uint16_t *h, int M, float T, const int32_t *draft,
+                       const float *u_acc, const float *u_next, float *z, int32_t *argmax, int32_t *out,
+                       void *ws, size_t ws_bytes, void *stream)
+{
+    FGM_TRY(check_m(M));
+    FGM_TRY(check_vocab(emb, V));
+    if (!h || !aligned16(h))
+        return fail(FGM_ERR_INVALID_ARG, "h NULL or not 16-byte aligned");
+    FGM_TRY(check_sample_args(M, T, draft, u_acc, u_next, z, out));
+    FGM_TRY(check_ws(ws, ws_bytes, M, V));
+    FGM_TRY(device_ready(nullptr));
+    Ws w = ws_carve(ws);
+    fused::Params prm = fused_params(fused::kModeLmHead, M, w);
+    prm.x = h;
+    prm.emb = emb;
+    prm.V = V;
+    set_sample(prm, T, draft, u_acc, u_next, z, argmax, out, w);
+    return launch_fused(prm, static_cast<cudaStream_t>(stream));
+}
+
+int fgm_verify_step_sample(const fgm_layer *layers, int n_layers, const uint16_t *emb, int64_t V,
+                           const uint16_t *x, const int32_t *draft, int M, float T, const float *u_acc,
+                           const float *u_next, float *z, int32_t *argmax, int32_t *out, void *ws,
+                           size_t ws_bytes, void *stream)
+{
+    FGM_TRY(check_m(M));
+    FGM_TRY(check_layers(layers, n_layers));
+    FGM_TRY(check_vocab(emb, V));
+    if (!x || !aligned16(x))
+        return fail(FGM_ERR_INVALID_ARG, "x NULL or not 16-byte aligned");
+    FGM_TRY(check_sample_args(M, T, draft, u_acc, u_next, z, out));
+    FGM_TRY(check_ws(ws, ws_bytes, M, V));
+    FGM_TRY(device_ready(nullptr));
+    Ws w = ws_carve(ws);
+    fused::Params prm = fused_params(fused::kModeVerify, M, w);
+    for (int l = 0; l < n_layers; ++l)
+        prm.layers[l] = layers[l];
+    prm.n_layers = n_layers;
+    prm.x = x;
+    prm.emb = emb;
+    prm.V = V;
+    set_sample(prm, T, draft, u_acc, u_next, z, argmax, out, w);
+    return launch_fused(prm, static_cast<cudaStream_t>(stream));
 }
 
 int fgm_verify_step_host(const fgm_layer *layers, int n_layers, const uint16_t *emb, int64_t V,

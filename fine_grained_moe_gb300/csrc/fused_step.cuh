@@ -87,6 +87,10 @@ struct Params {
     int32_t *argmax;        // [M] (verify, lm_head)
     float *maxlogit;        // [M] (lm_head, optional)
     int32_t *out;           // [2] (verify)
+    float *z;               // sampling at T > 0 (verify, lm_head): logits out [M][V]; null = greedy
+    float inv_t;            // sampling: 1 / T
+    const float *u_acc;     // sampling: [M-1] acceptance uniforms
+    const float *u_next;    // sampling: [M] uniforms of the emitted sample
     int32_t *ids;           // layer: [M][8]; stack/verify: [L][M][8] trace; optional
     float *wts;             // layer: [M][8]; optional
     Ws ws;
@@ -111,6 +115,7 @@ struct __align__(128) Smem {
     float part2[kRouterRows][kMW][8];
     float best_v[kMW][8];       // lm_head winners per reducing warp and token
     int32_t best_i[kMW][8];
+    float samp_s[kMW][8];       // sampling: sum of exp((z - best_v) / T) per reducing warp and token
     float comb[2][kMaxSlots][8];
     int32_t experts[2][kMaxSlots];
     int32_t n_unique[2];
@@ -744,6 +749,205 @@ __device__ __noinline__ DownCols<NB> down_columns(const float *act_slot, int M, 
     return r;
 }
 
+// Speculative sampling verify at temperature T = 1 / inv_t, run by the 352
+// consumer threads of the last CTA once every CTA's logits z [M][V] and its
+// per-token (max, sum of exp((z - max) / T)) over its contiguous vocabulary
+// range are in memory. With p_i = softmax(z_i / T): draft d_i is kept while
+// u_acc[i] < p_i(d_i); the first rejected position i emits an inverse-CDF
+// sample, in vocabulary order, of p_i with d_i removed at u_next[i]; if all
+// M - 1 drafts are kept, position M - 1 emits a sample of p_{M-1}.
+// out = {accepted drafts, emitted token}. The CDF walk picks the CTA range
+// from the per-CTA sums, then one of 11 sub-ranges from warp sums, then the
+// row by a warp scan. Where rounding leaves the target past the last weight,
+// the last row of positive weight is taken. A draft outside [0, V) has
+// probability 0: it is rejected and removes nothing.
+struct SampleShared {
+    float mx[kMaxM], tot[kMaxM];
+    float wsum[kMW];
+    int wlast[kMW];
+    float target, wx, base;
+    int emit, excl, g, wsel, resort;
+};
+
+__device__ __noinline__ void sample_finish(const float *z, int64_t V, int M, int G, float inv_t,
+                                           const float *part_max, const float *part_sum, const int32_t *draft,
+                                           const float *u_acc, const float *u_next, const int32_t *arg,
+                                           int32_t *out)
+{
+    __shared__ SampleShared sh;
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const unsigned full = 0xFFFFFFFFu;
+    // global max and total of every position
+    if (warp < M) {
+        float mx = -INFINITY;
+        for (int c = lane; c < G; c += 32)
+            mx = fmaxf(mx, __ldcg(part_max + c * kMaxM + warp));
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1)
+            mx = fmaxf(mx, __shfl_xor_sync(full, mx, o));
+        float tot = 0.0f;
+        for (int c = lane; c < G; c += 32) {
+            const float m = __ldcg(part_max + c * kMaxM + warp);
+            if (m > -INFINITY)
+                tot += __ldcg(part_sum + c * kMaxM + warp) * expf((m - mx) * inv_t);
+        }
+        tot = warp_sum(tot);
+        if (lane == 0) {
+            sh.mx[warp] = mx;
+            sh.tot[warp] = tot;
+        }
+    }
+    consumer_sync();
+    // acceptance, position by position
+    if (tid == 0) {
+        int i = 0, excl = -1;
+        for (; i < M - 1; ++i) {
+            const int d = draft[i];
+            if (d < 0 || d >= V)
+                break;
+            const float pd = expf((__ldcg(z + (size_t)i * V + d) - sh.mx[i]) * inv_t) / sh.tot[i];
+            if (!(u_acc[i] < pd)) {
+                excl = d;
+                break;
+            }
+        }
+        const float wx = excl >= 0 ? expf((__ldcg(z + (size_t)i * V + excl) - sh.mx[i]) * inv_t) : 0.0f;
+        sh.emit = i;
+        sh.excl = excl;
+        sh.wx = wx;
+        sh.target = u_next[i] * (sh.tot[i] - wx);
+    }
+    consumer_sync();
+    const int i = sh.emit, excl = sh.excl;
+    const float mx = sh.mx[i], target = sh.target, wx = sh.wx;
+    const float *zi = z + (size_t)i * V;
+    // the CTA range that holds the target: warp 0 scans the per-CTA sums in order
+    if (warp == 0) {
+        float base = 0.0f;
+        int gsel = -1, glast = -1;
+        float base_last = 0.0f;
+        for (int c0 = 0; c0 < G && gsel < 0; c0 += 32) {
+            const int c = c0 + lane;
+            float sc = 0.0f;
+            if (c < G) {
+                const float m = __ldcg(part_max + c * kMaxM + i);
+                if (m > -INFINITY)
+                    sc = __ldcg(part_sum + c * kMaxM + i) * expf((m - mx) * inv_t);
+                const Range r = split(V, c, G);
+                if (excl >= r.begin && excl < r.end)
+                    sc = fmaxf(sc - wx, 0.0f);
+            }
+            float inc = sc;
+#pragma unroll
+            for (int o = 1; o < 32; o <<= 1) {
+                const float n = __shfl_up_sync(full, inc, o);
+                if (lane >= o)
+                    inc += n;
+            }
+            const unsigned hit = __ballot_sync(full, sc > 0.0f && base + inc > target);
+            const unsigned pos = __ballot_sync(full, sc > 0.0f);
+            if (pos) {
+                const int l = 31 - __clz(pos);
+                glast = c0 + l;
+                base_last = base + __shfl_sync(full, inc - sc, l);
+            }
+            if (hit) {
+                const int l = __ffs(hit) - 1;
+                gsel = c0 + l;
+                base += __shfl_sync(full, inc - sc, l);
+            } else {
+                base += __shfl_sync(full, inc, 31);
+            }
+        }
+        if (lane == 0) {
+            sh.resort = gsel < 0;
+            sh.g = gsel >= 0 ? gsel : glast;
+            sh.base = gsel >= 0 ? base : base_last;
+        }
+    }
+    consumer_sync();
+    if (sh.g < 0) {   // no weight anywhere (every logit NaN, or all mass on the removed draft)
+        if (tid == 0) {
+            out[0] = i;
+            out[1] = arg[i];
+        }
+        return;
+    }
+    const Range r = split(V, sh.g, G);
+    const int per = (r.end - r.begin + kMW - 1) / kMW;
+    const int w0 = r.begin + warp * per, w1 = min(r.end, w0 + per);
+    auto weight = [&](int v) { return v == excl ? 0.0f : expf((__ldcg(zi + v) - mx) * inv_t); };
+    // the sub-range of each warp: its sum and its last row of positive weight
+    {
+        float sum = 0.0f;
+        int last = -1;
+        for (int v = w0 + lane; v < w1; v += 32) {
+            const float w = weight(v);
+            sum += w;
+            if (w > 0.0f)
+                last = v;
+        }
+        sum = warp_sum(sum);
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1)
+            last = max(last, __shfl_xor_sync(full, last, o));
+        if (lane == 0) {
+            sh.wsum[warp] = sum;
+            sh.wlast[warp] = last;
+        }
+    }
+    consumer_sync();
+    if (tid == 0) {
+        int wsel = -1;
+        float base = sh.base;
+        if (!sh.resort)
+            for (int w = 0; w < kMW; ++w) {
+                if (sh.wsum[w] > 0.0f && base + sh.wsum[w] > target) {
+                    wsel = w;
+                    break;
+                }
+                base += sh.wsum[w];
+            }
+        int last = -1;
+        for (int w = 0; w < kMW; ++w)
+            last = max(last, sh.wlast[w]);
+        sh.wsel = wsel;
+        sh.base = base;
+        if (wsel < 0) {   // rounding put the target past the range's weight
+            out[0] = i;
+            out[1] = last >= 0 ? last : arg[i];
+        }
+    }
+    consumer_sync();
+    if (warp != sh.wsel)
+        return;
+    float base = sh.base;
+    for (int v0 = w0; v0 < w1; v0 += 32) {
+        const int v = v0 + lane;
+        const float w = v < w1 ? weight(v) : 0.0f;
+        float inc = w;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+            const float n = __shfl_up_sync(full, inc, o);
+            if (lane >= o)
+                inc += n;
+        }
+        const unsigned hit = __ballot_sync(full, w > 0.0f && base + inc > target);
+        if (hit) {
+            if (lane == 0) {
+                out[0] = i;
+                out[1] = v0 + __ffs(hit) - 1;
+            }
+            return;
+        }
+        base += __shfl_sync(full, inc, 31);
+    }
+    if (lane == 0) {   // rounding between the warp's sum and its scan
+        out[0] = i;
+        out[1] = sh.wlast[warp];
+    }
+}
+
 // NB: packed column blocks (2: M <= 5, 3: M <= 8). TRACE: the phase-trace
 // profiling aid is compiled in (a separate instantiation, so that the
 // production kernels carry none of its code).
@@ -967,6 +1171,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_fused(const __grid_constant__ P
     // over the tiles this warp reduces
     float best_v[2] = {-INFINITY, -INFINITY};
     int best_i[2] = {0x7FFFFFFF, 0x7FFFFFFF};
+    float run_s[2] = {0.0f, 0.0f};   // sampling: sum of exp((z - best_v) / T) over the same tiles
 
     // Epilogue of one reduced tile. Expert tiles (packed columns): the lane
     // holds row r0 = lane / 4 in x, y and row r0 + 8 in z, w for its tokens
@@ -1021,6 +1226,27 @@ __global__ void __launch_bounds__(kThreads, 1) k_fused(const __grid_constant__ P
                         bz = oz;
                         bi = oi;
                     }
+                }
+                if (p.z) {
+                    // sampling: the logits go out, and the tile's sum of exp((z - bz) / T)
+                    // (bz = the column's tile maximum, the same in its 8 lanes) joins the
+                    // running sum kept relative to best_v
+                    const int t = n0 + c;
+                    if (t < M) {
+                        float *zr = p.z + (size_t)t * p.V + v0;
+                        if (r0 < nv)
+                            zr[r0] = za;
+                        if (r0 + 8 < nv)
+                            zr[r0 + 8] = zb;
+                    }
+                    float e = (ca ? expf((za - bz) * p.inv_t) : 0.0f) + (cb ? expf((zb - bz) * p.inv_t) : 0.0f);
+                    e += __shfl_xor_sync(0xFFFFFFFFu, e, 4);
+                    e += __shfl_xor_sync(0xFFFFFFFFu, e, 8);
+                    e += __shfl_xor_sync(0xFFFFFFFFu, e, 16);
+                    if (bz > best_v[c])
+                        run_s[c] = run_s[c] * expf((best_v[c] - bz) * p.inv_t) + e;
+                    else if (bz > -INFINITY)
+                        run_s[c] += e * expf((bz - best_v[c]) * p.inv_t);
                 }
                 if (better(bz, bi, best_v[c], best_i[c])) {
                     best_v[c] = bz;
@@ -1755,6 +1981,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_fused(const __grid_constant__ P
             for (int c = 0; c < 2; ++c) {
                 s.best_v[warp][2 * lane + c] = best_v[c];
                 s.best_i[warp][2 * lane + c] = best_i[c];
+                s.samp_s[warp][2 * lane + c] = run_s[c];
             }
         }
         consumer_sync();
@@ -1769,6 +1996,13 @@ __global__ void __launch_bounds__(kThreads, 1) k_fused(const __grid_constant__ P
                 }
             __stcg(ws.part_val + cta * kMaxM + tid, bv);
             __stcg(ws.part_idx + cta * kMaxM + tid, bi);
+            if (p.z) {
+                float sum = 0.0f;
+                for (int w = 0; w < kMW; ++w)
+                    if (s.best_v[w][tid] > -INFINITY)
+                        sum += s.samp_s[w][tid] * expf((s.best_v[w][tid] - bv) * p.inv_t);
+                __stcg(ws.part_sum + cta * kMaxM + tid, sum);
+            }
         }
     }
     if (TRACE && p.trace && tid == 0)
@@ -1823,7 +2057,11 @@ __global__ void __launch_bounds__(kThreads, 1) k_fused(const __grid_constant__ P
             }
         }
         consumer_sync();
-        if (tid == 0 && p.mode == kModeVerify) {
+        if (p.z) {
+            if (is_mma)
+                sample_finish(p.z, p.V, M, G, p.inv_t, ws.part_val, ws.part_sum, p.draft, p.u_acc, p.u_next, arg,
+                              p.out);
+        } else if (tid == 0 && p.mode == kModeVerify) {
             int a = 0;
             while (a < M - 1 && p.draft[a] == arg[a])
                 ++a;

@@ -228,6 +228,48 @@ int fgm_verify_step_host(const fgm_layer *layers, int n_layers, const uint16_t *
                          const uint16_t *x_host, const int32_t *draft_host, int M,
                          int32_t *out_host, void *ws, size_t ws_bytes, void *stream);
 
+/* Speculative sampling verify at temperature T > 0, on the tied lm_head
+ * logits z_{t,v} = sum_j emb[v][j] * h[t][j] (fp32 accumulation) of M
+ * positions and gamma = M - 1 drafted tokens. With p_t = softmax(z_t / T):
+ * for t = 0 .. M-2 draft d_t is accepted while u_acc[t] < p_t(d_t); at the
+ * first rejected position t the emitted token is the inverse-CDF sample, in
+ * vocabulary order, of p_t with d_t removed (renormalised) at u_next[t]; if
+ * every draft is accepted, position M-1 emits the sample of p_{M-1} at
+ * u_next[M-1]. out = {accepted drafts, emitted token}. The drafter proposes
+ * tokens only (its proposal is one-hot), so the emitted sequence has the
+ * distribution of ordinary sampling from p. Source: "llm-decoding" §"What we
+ * learned, and where this goes" (a kept token passes the full model's
+ * distribution, a rejected one falls back to a real model step, the output
+ * distribution is unchanged). Decisions within fp32 rounding of a boundary
+ * (|u_acc[t] - p_t(d_t)|, or u_next at a partial sum of the CDF) may go
+ * either way. As T -> 0 this is greedy acceptance (fgm_lm_head_argmax +
+ * fgm_spec_verify).
+ *  emb     bf16 [V][2816], 1 <= V < 2^31 (16-byte aligned)
+ *  h       bf16 [M][2816] final hidden states (16-byte aligned)
+ *  T       temperature: finite, > 0, and 1/T finite
+ *  draft   int32 [M-1] (device; may be NULL when M == 1); a draft outside
+ *          [0, V) has probability 0 (rejected, nothing removed)
+ *  u_acc   fp32 [M-1] uniforms in [0, 1) (device; may be NULL when M == 1)
+ *  u_next  fp32 [M] uniforms in [0, 1) (device)
+ *  z       fp32 [M][V] output: the logits (device, 4-byte aligned, caller-owned)
+ *  argmax  int32 [M] output or NULL: the greedy argmax of every position
+ *  out     int32 [2] output (device)
+ * Runs on the persistent kernel whatever fgm_select_path chose; its last CTA
+ * takes the decisions. */
+int fgm_lm_head_sample(const uint16_t *emb, int64_t V, const uint16_t *h, int M, float T, const int32_t *draft,
+                       const float *u_acc, const float *u_next, float *z, int32_t *argmax, int32_t *out,
+                       void *ws, size_t ws_bytes, void *stream);
+
+/* One full verify step with speculative sampling at temperature T: the
+ * n_layers stack from x, the final unit RMSNorm rounded to bf16, then
+ * fgm_lm_head_sample on those rows. One launch of the persistent kernel.
+ *  layers  HOST array of n_layers fgm_layer;  x  bf16 [M][2816]
+ *  other arguments as fgm_lm_head_sample */
+int fgm_verify_step_sample(const fgm_layer *layers, int n_layers, const uint16_t *emb, int64_t V,
+                           const uint16_t *x, const int32_t *draft, int M, float T, const float *u_acc,
+                           const float *u_next, float *z, int32_t *argmax, int32_t *out, void *ws,
+                           size_t ws_bytes, void *stream);
+
 /* Selects the execution path of subsequent calls in this process; returns the
  * previous one. An unknown value leaves the path unchanged. Both paths compute
  * the same step; they differ in kernel design only. */

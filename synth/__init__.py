@@ -160,6 +160,11 @@ def embedding_fp8(emb: torch.Tensor, *, chunk_rows: int = 1 << 14) -> tuple[torc
     return q, sc
 
 
+def uniforms(seed: int, n: int) -> torch.Tensor:
+    """n uniforms in [0, 1) (float32, CPU) for the sampling verify's decisions."""
+    return torch.rand(n, generator=_gen(seed, "cpu"), dtype=torch.float32)
+
+
 def drafts(seed: int, target, *, vocab: int = VOCAB, p: float = 0.7) -> torch.Tensor:
     """gamma = len(target) - 1 draft tokens (int32, CPU): d_i = target[i-1] with
     probability p, else uniform over [0, vocab)."""

@@ -49,6 +49,33 @@ def rowwise_rel_err(gpu_bf16: torch.Tensor, ref_f64: np.ndarray) -> np.ndarray:
     return np.abs(g - r).max(axis=1) / np.abs(r).max(axis=1)
 
 
+# Elementwise form of the same tolerance, reported beside the row form: each
+# element's error over max(|bf16(oracle)|, 1e-2 * rms of its row), so that small
+# elements are compared too without dividing by values near zero. Bound: the
+# two bf16 roundings alone may put the two sides one bf16 step apart (2^-8 of
+# the element); the library's arithmetic (activations as three E4M3 terms, each
+# within 2^-12 of its slice maximum, and fp32 sums over 704 or 2816 products)
+# adds an absolute error of order 1e-4 of the row's rms, which is 1e-2 of the
+# floor. ELEM_TOL = 2e-2 covers both with margin; the tests assert it.
+ELEM_TOL = 2e-2
+ELEM_FLOOR = 1e-2
+
+
+def elementwise_rel_err(gpu_bf16: torch.Tensor, ref_f64: np.ndarray) -> np.ndarray:
+    """Per row: max_k |gpu_k - bf16(oracle)_k| / max(|bf16(oracle)_k|, 1e-2 rms(bf16(oracle)))."""
+    g = gpu_bf16.detach().cpu().to(torch.float64).numpy()
+    r = oracle.bf16_to_f64(oracle.bf16_round(ref_f64))
+    rms = np.sqrt(np.mean(r * r, axis=1, keepdims=True))
+    den = np.maximum(np.abs(r), ELEM_FLOOR * rms)
+    return (np.abs(g - r) / den).max(axis=1)
+
+
+def to_bf16_tensor(values: np.ndarray, device="cuda") -> torch.Tensor:
+    """fp64 host values rounded to bf16 (the oracle's rounding) as a bf16 tensor."""
+    bits = oracle.bf16_round(values).astype(np.uint16).view(np.int16)
+    return torch.from_numpy(np.ascontiguousarray(bits)).view(torch.bfloat16).to(device)
+
+
 def id_sets_agree(gpu_ids: np.ndarray, ref_ids: np.ndarray) -> bool:
     return sorted(gpu_ids.tolist()) == sorted(ref_ids.tolist())
 

@@ -65,3 +65,25 @@ def test_traffic_figure_only_for_the_kernel_it_was_taken_on(tmp_path, monkeypatc
     assert bench.captured_traffic() == 5278000000
     prof.write_text("- kernel sources sha256: `0000`\n- traffic per launch (bytes): 5278000000\n")
     assert bench.captured_traffic() is None          # taken on other kernel sources
+
+
+def test_expected_accept_matches_enumeration():
+    """E[a] of the draft recipe (each draft copies the target's argmax with
+    probability 0.7) against an enumeration of all 2^gamma hit patterns pushed
+    through the oracle's greedy accept rule."""
+    import itertools
+
+    import numpy as np
+
+    sys.path.insert(0, ROOT)
+    import bench
+    import oracle
+    for gamma in range(0, 8):
+        target = np.arange(100, 101 + gamma, dtype=np.int32)
+        e = 0.0
+        for hits in itertools.product((0, 1), repeat=gamma):
+            d = np.array([target[i] if h else -1 - i for i, h in enumerate(hits)], dtype=np.int32)
+            a, _ = oracle.spec_verify(target, d)
+            e += a * np.prod([0.7 if h else 0.3 for h in hits])
+        assert abs(e - bench.expected_accept(gamma)) < 1e-12, (gamma, e)
+    assert abs(bench.expected_accept(4) - 1.7731) < 1e-12

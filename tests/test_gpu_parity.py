@@ -16,8 +16,8 @@ import torch
 
 import oracle
 import synth
-from helpers import (MARGIN, REL_TOL, bf16_bits, bf16_values, id_sets_agree, ids_valid_at_tie,
-                     rowwise_rel_err, to_oracle_layer)
+from helpers import (ELEM_TOL, MARGIN, REL_TOL, bf16_bits, bf16_values, elementwise_rel_err, id_sets_agree,
+                     ids_valid_at_tie, rowwise_rel_err, to_oracle_layer)
 
 pytestmark = pytest.mark.gpu
 
@@ -132,6 +132,62 @@ def test_moe_stack_matches_oracle(fgm, ws, n_layers, M, s):
     h_ref, traj = _stack_reference(host, bf16_values(x))
     full = _compare_stack(trace.cpu().numpy(), y, h_ref, traj, host, M)
     assert len(full) >= 1
+    assert ws.status() == 0
+
+
+def _edge_rows(m):
+    """Hidden rows that stress the per-slice power-of-two scales of the 3-term
+    E4M3 activation split (256-wide K slices): a spike 2^16 above its slice,
+    an all-zero slice, a slice of bf16 subnormals, a whole row scaled by 2^-40,
+    a 2^20 spike with a 2^-20 tail slice; for M = 8 also a negative 2^18 spike
+    in the last element, a zero last slice and a plain row."""
+    x = synth.hidden_states(X_SEED + 77, m).float()
+    x[0, 3 * 256 + 17] = 2.0 ** 16
+    x[1, 5 * 256:6 * 256] = 0.0
+    x[2, 7 * 256:8 * 256] *= 2.0 ** -130
+    x[3] *= 2.0 ** -40
+    x[4, 0] = 2.0 ** 20
+    x[4, 10 * 256:] *= 2.0 ** -20
+    if m > 5:
+        x[5, 2815] = -2.0 ** 18
+        x[6, 10 * 256:] = 0.0
+    return x.to(torch.bfloat16).cuda()
+
+
+def _check_rows(gid, y, ref, logits_of, m, what):
+    row, elem = rowwise_rel_err(y, ref.y), elementwise_rel_err(y, ref.y)
+    assert np.isfinite(y.float().cpu().numpy()).all(), what
+    for t in range(m):
+        if ref.margin[t] > MARGIN:
+            assert id_sets_agree(gid[t], ref.ids[t]), (what, t, gid[t], ref.ids[t])
+        else:
+            assert ids_valid_at_tie(gid[t], logits_of(t)), (what, t)
+            if not id_sets_agree(gid[t], ref.ids[t]):
+                continue
+        assert row[t] <= REL_TOL, (what, t, row[t])
+        assert elem[t] <= ELEM_TOL, (what, t, elem[t])
+    print(f"{what}: row errors {np.round(row, 6).tolist()}, elementwise {np.round(elem, 5).tolist()}")
+
+
+@pytest.mark.parametrize("M", [5, 8])
+def test_activation_split_edge_cases(fgm, ws, layer0, M):
+    """The layer (no norm) and a one-layer stack (RMSNorm + residual) on rows
+    whose K-slices span 2^-130 to 2^20: every routed token within the row and
+    elementwise tolerances of the oracle, nothing non-finite."""
+    p, L = _with_bias(*layer0, 1.1)
+    x = _edge_rows(M)
+    xv = bf16_values(x)
+    ids = torch.empty((M, 8), dtype=torch.int32, device="cuda")
+    y = fgm.moe_layer_fwd(p, x, topk_ids=ids, ws=ws)
+    torch.cuda.synchronize()
+    ref = oracle.moe_layer(L, xv)
+    _check_rows(ids.cpu().numpy(), y, ref, lambda t: ref.logits[t], M, "layer")
+    trace = torch.empty((1, M, 8), dtype=torch.int32, device="cuda")
+    y = fgm.moe_stack_fwd([p], x, ids_trace=trace, ws=ws)
+    torch.cuda.synchronize()
+    ref = oracle.stack_layer(L, xv)
+    _check_rows(trace.cpu().numpy()[0], y, ref,
+                lambda t: oracle.router_token(L, oracle.rmsnorm(xv[t:t + 1])[0])[3], M, "stack")
     assert ws.status() == 0
 
 

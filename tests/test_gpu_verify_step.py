@@ -5,6 +5,18 @@ about 23 GB of E4M3 expert weights), the final unit RMSNorm rounded to bf16,
 the 262,144-word tied lm_head and greedy acceptance of four drafts that copy
 the oracle's argmax with probability 0.7. The oracle runs layer by layer on
 host copies of the same weights.
+
+Two kinds of comparison:
+  * teacher-forced, layer by layer: each of the 30 layers gets the oracle's
+    own input to that layer (rounded to bf16) as a one-layer stack call, so
+    every token is compared at every layer (routing where the oracle's margin
+    exceeds 1e-2, outputs within the row and elementwise tolerances);
+  * end to end: the GPU's own 30-layer trajectory. A token's routing may first
+    differ from the oracle's only at a near tie (margin <= 1e-2, the GPU's
+    choice valid), after which that token follows another valid trajectory and
+    is not compared further; tokens that never diverge must match at the end.
+    How many stay comparable depends on the near ties of the seeded inputs, so
+    no count is asserted here: the teacher-forced test covers every token.
 """
 
 import numpy as np
@@ -13,7 +25,8 @@ import torch
 
 import oracle
 import synth
-from helpers import MARGIN, REL_TOL, bf16_bits, bf16_values, rowwise_rel_err, to_oracle_layer
+from helpers import (ELEM_TOL, MARGIN, REL_TOL, bf16_bits, bf16_values, elementwise_rel_err, id_sets_agree,
+                     ids_valid_at_tie, rowwise_rel_err, to_bf16_tensor, to_oracle_layer)
 from test_gpu_parity import _compare_stack
 
 pytestmark = pytest.mark.gpu
@@ -53,8 +66,44 @@ def test_stack_30_layers(setup):
     y = s["fgm"].moe_stack_fwd(s["layers"], s["x"], ids_trace=trace, ws=s["ws"])
     torch.cuda.synchronize()
     full = _compare_stack(trace.cpu().numpy(), y, s["h_ref"], s["traj"], s["host"], M)
-    assert len(full) >= 2, full
+    print(f"tokens compared to the end: {full}")
     assert s["ws"].status() == 0
+
+
+def _teacher_forced(fgm, ws, layers, host, traj, m):
+    """Every layer from the oracle's own (bf16-rounded) input: routing and output
+    of every token against the oracle's layer on the same input. Returns the
+    largest row and elementwise errors."""
+    worst_row, worst_elem, ties = 0.0, 0.0, 0
+    for l, (_, _, h_in) in enumerate(traj):
+        x = to_bf16_tensor(h_in)
+        trace = torch.empty((1, m, 8), dtype=torch.int32, device="cuda")
+        y = fgm.moe_stack_fwd([layers[l]], x, ids_trace=trace, ws=ws)
+        torch.cuda.synchronize()
+        ref = oracle.stack_layer(host[l], bf16_values(x))
+        gid = trace.cpu().numpy()[0]
+        row, elem = rowwise_rel_err(y, ref.y), elementwise_rel_err(y, ref.y)
+        for t in range(m):
+            if ref.margin[t] > MARGIN:
+                assert id_sets_agree(gid[t], ref.ids[t]), (l, t, gid[t], ref.ids[t])
+            else:
+                ties += 1
+                xn = oracle.rmsnorm(bf16_values(x)[t:t + 1])[0]
+                assert ids_valid_at_tie(gid[t], oracle.router_token(host[l], xn)[3]), (l, t)
+                if not id_sets_agree(gid[t], ref.ids[t]):
+                    continue
+            assert row[t] <= REL_TOL, (l, t, row[t])
+            assert elem[t] <= ELEM_TOL, (l, t, elem[t])
+            worst_row, worst_elem = max(worst_row, row[t]), max(worst_elem, elem[t])
+    assert ws.status() == 0
+    print(f"teacher-forced {len(traj)} layers x {m} tokens: worst row error {worst_row:.2e}, "
+          f"worst elementwise error {worst_elem:.2e}, near ties {ties}")
+    return worst_row, worst_elem
+
+
+def test_stack_teacher_forced_every_layer(setup):
+    s = setup
+    _teacher_forced(s["fgm"], s["ws"], s["layers"], s["host"], s["traj"], M)
 
 
 def _matched_positions(s):
@@ -73,24 +122,175 @@ def _comparable_prefix(s, margins=None):
     return [t in full and mg[t] > MARGIN for t in range(M)]
 
 
+def _oracle_batch(s, seed, draft_seed, m=M):
+    """Oracle trajectory, final argmax and drafts for one input batch."""
+    x = synth.hidden_states(seed, m, device="cuda")
+    h = bf16_values(x)
+    traj = []
+    for L in s["host"]:
+        out = oracle.stack_layer(L, h)
+        traj.append((out.ids.copy(), out.margin.copy(), h.copy()))
+        h = out.y
+    am, _, mg = oracle.lm_head(bf16_bits(s["emb"]), oracle.bf16_to_f64(oracle.bf16_round(oracle.rmsnorm(h))))
+    return x, h, traj, am, mg, synth.drafts(draft_seed, am)
+
+
 def test_verify_step_accept_and_next(setup):
+    """Accepted count and next token against the oracle's. The comparison needs
+    the oracle's trajectory to be the GPU's up to the accepted prefix (no near
+    tie taken the other way, argmax margins above 1e-2); batches are tried
+    until at least two have been compared, and that they were is asserted."""
     s = setup
     fgm = s["fgm"]
-    draft = s["draft"].cuda()
-    am = torch.empty(M, dtype=torch.int32, device="cuda")
-    out = fgm.verify_step(s["layers"], s["emb"], s["x"], draft, argmax=am, ws=s["ws"])
-    torch.cuda.synchronize()
-    a_ref, nxt_ref = oracle.spec_verify(s["am"], s["draft"].numpy())
-    ok = _comparable_prefix(s)
-    gam = am.cpu().numpy()
+    compared = 0
+    for b in range(6):
+        if b == 0:
+            x, h_ref, traj, am_ref, mg, draft = s["x"], s["h_ref"], s["traj"], s["am"], s["mg"], s["draft"]
+        else:
+            x, h_ref, traj, am_ref, mg, draft = _oracle_batch(s, 31 + b, 33 + b)
+        am = torch.empty(M, dtype=torch.int32, device="cuda")
+        out = fgm.verify_step(s["layers"], s["emb"], x, draft.cuda(), argmax=am, ws=s["ws"])
+        trace = torch.empty((N_LAYERS, M, 8), dtype=torch.int32, device="cuda")
+        y = fgm.moe_stack_fwd(s["layers"], x, ids_trace=trace, ws=s["ws"])
+        torch.cuda.synchronize()
+        full = set(_compare_stack(trace.cpu().numpy(), y, h_ref, traj, s["host"], M))
+        ok = [t in full and mg[t] > MARGIN for t in range(M)]
+        gam = am.cpu().numpy()
+        for t in range(M):
+            if ok[t]:
+                assert gam[t] == am_ref[t], (b, t, gam[t], am_ref[t])
+        a, nxt = out.cpu().tolist()
+        # the accept rule applied to the GPU's own argmax is always exact
+        assert (a, nxt) == oracle.spec_verify(gam, draft.numpy())
+        a_ref, nxt_ref = oracle.spec_verify(am_ref, draft.numpy())
+        if all(ok[:a_ref + 1]):
+            assert (a, nxt) == (a_ref, nxt_ref), (b, a, nxt, a_ref, nxt_ref)
+            compared += 1
+        if compared >= 2:
+            break
+    print(f"accepted count and next token compared on {compared} batches")
+    assert compared >= 2
+    assert s["ws"].status() == 0
+
+
+def _bf16_ulp(v: np.ndarray) -> np.ndarray:
+    """Spacing of bf16 values at |v| (8 significant bits)."""
+    e = np.floor(np.log2(np.maximum(np.abs(v), 2.0 ** -126)))
+    return 2.0 ** (e - 7)
+
+
+def test_verify_step_repeats_agree(setup):
+    """Determinism contract. The layer output is summed over CTAs with fp32
+    atomics, so the order of the additions, and the last bits of the fp32
+    residual stream, vary between runs. So:
+      * a token's routing may differ between repeats only at a near tie: the
+        first layer where repeats differ must have an oracle margin <= 1e-2
+        (checked while the token is still on the oracle's trajectory);
+      * tokens routed alike in every repeat end within 1 bf16 ulp plus 1e-3 of
+        the row rms of each other. An fp32 difference in the residual stream
+        moves the next layer's activation split (E4M3 terms whose resolution
+        is about 2^-16 of a slice's maximum) and so grows from layer to layer:
+        measured about 1.3e-4 of the rms after 30 layers, a tenth of the bound
+        and a tenth of the parity tolerance;
+      * the argmax of such a token, where the oracle's argmax margin exceeds
+        1e-2, is identical across repeats, and so are the accepted count and
+        next token when the accepted prefix is made of such tokens.
+    The verify calls are separate launches from the traced stack calls; a
+    routing flip in one of them needs a router margin below the run-to-run
+    difference (~1e-6), which the seeded inputs do not have."""
+    s = setup
+    fgm = s["fgm"]
+    outs, ams, ys, traces = [], [], [], []
+    for _ in range(4):
+        am = torch.empty(M, dtype=torch.int32, device="cuda")
+        outs.append(fgm.verify_step(s["layers"], s["emb"], s["x"], s["draft"].cuda(), argmax=am,
+                                    ws=s["ws"]).cpu().tolist())
+        ams.append(am.cpu().numpy())
+        trace = torch.empty((N_LAYERS, M, 8), dtype=torch.int32, device="cuda")
+        ys.append(fgm.moe_stack_fwd(s["layers"], s["x"], ids_trace=trace, ws=s["ws"]).cpu().double().numpy())
+        traces.append(trace.cpu().numpy())
+    same, flips = [], []
     for t in range(M):
-        if ok[t]:
-            assert gam[t] == s["am"][t], (t, gam[t], s["am"][t])
-    a, nxt = out.cpu().tolist()
-    # the accept rule applied to the GPU's own argmax is always exact
-    assert (a, nxt) == oracle.spec_verify(gam, s["draft"].numpy())
-    if all(ok[:a_ref + 1]):
-        assert (a, nxt) == (a_ref, nxt_ref)
+        diff = [l for l in range(N_LAYERS)
+                if not all(id_sets_agree(tr[l, t], traces[0][l, t]) for tr in traces)]
+        if not diff:
+            same.append(t)
+            continue
+        l0 = diff[0]
+        on_oracle = all(id_sets_agree(traces[0][l, t], s["traj"][l][0][t]) for l in range(l0))
+        flips.append((t, l0, float(s["traj"][l0][1][t]) if on_oracle else None))
+        if on_oracle:
+            assert s["traj"][l0][1][t] <= MARGIN, (t, l0, s["traj"][l0][1][t])
+    full = set(_compare_stack(traces[0], torch.from_numpy(ys[0]).to(torch.bfloat16), s["h_ref"], s["traj"],
+                              s["host"], M))
+    stable = [t in same and t in full and s["mg"][t] > MARGIN for t in range(M)]
+    for t in range(M):
+        if stable[t]:
+            assert len({int(a[t]) for a in ams}) == 1, (t, [int(a[t]) for a in ams])
+    a_ref, _ = oracle.spec_verify(s["am"], s["draft"].numpy())
+    if all(stable[:a_ref + 1]):
+        assert all(o == outs[0] for o in outs), outs
+    worst_ulps, worst_rms = 0.0, 0.0
+    for t in same:
+        y0 = ys[0][t]
+        rms = np.sqrt(np.mean(y0 * y0))
+        for y in ys[1:]:
+            d = np.abs(y[t] - y0)
+            ulp = _bf16_ulp(np.maximum(np.abs(y[t]), np.abs(y0)))
+            assert (d <= ulp + 1e-3 * rms).all(), (t, float((d / (ulp + 1e-3 * rms)).max()))
+            worst_ulps = max(worst_ulps, float((d / ulp).max()))
+            worst_rms = max(worst_rms, float(d.max() / rms))
+    print(f"repeats: routing alike for {same}; first differing layer (token, layer, oracle margin): {flips}; "
+          f"largest difference {worst_ulps:.2f} bf16 ulp, {worst_rms:.2e} of the row rms; stable argmax: {stable}")
+    assert s["ws"].status() == 0
+
+
+def test_verify_step_sample(setup):
+    """Speculative sampling at T = 0.1 through the full step (drafts copy the
+    oracle's argmax with probability 0.7):
+      * the logits of every token whose routing matched the oracle's in every
+        layer are within 1e-2 (row infinity norm) of the oracle's logits of its
+        own final normed row;
+      * on the GPU's own logits, the oracle's sampling rule gives the GPU's
+        {accepted, token} wherever its margins exceed 2e-4 / T (fp32 rounding
+        of the weights and sums);
+      * against the oracle's own logits, the same holds wherever the margins
+        exceed the weight change the logit difference can cause (4 x max
+        |dz| / T, dz over the matched tokens), and the positions up to the
+        decision matched the oracle's trajectory."""
+    s = setup
+    fgm = s["fgm"]
+    T = 0.1
+    z_ref = oracle.lm_head_logits(bf16_bits(s["emb"]), s["hn"])
+    draft = synth.drafts(35, s["am"])
+    full = _matched_positions(s)
+    own, vs_ref, dz = 0, 0, 0.0
+    for k in range(6):
+        u_acc, u_next = synth.uniforms(500 + 2 * k, M - 1), synth.uniforms(501 + 2 * k, M)
+        out, z = fgm.verify_step_sample(s["layers"], s["emb"], s["x"], T, draft.cuda(), u_acc.cuda(),
+                                        u_next.cuda(), ws=s["ws"])
+        torch.cuda.synchronize()
+        a, tok = out.cpu().tolist()
+        zg = z.cpu().double().numpy()
+        if k == 0:
+            err = rowwise_rel_err(z.to(torch.bfloat16), z_ref)
+            for t in full:
+                assert err[t] <= REL_TOL, (t, err[t])
+            dz = max([float(np.abs(zg[t] - z_ref[t]).max()) for t in full], default=0.0)
+        ua, un = u_acc.double().numpy(), u_next.double().numpy()
+        a_g, tok_g, mg_g, gap_g = oracle.spec_sample(zg, T, draft.numpy(), ua, un)
+        tol = 2e-4 / T
+        if mg_g > tol and gap_g > tol:
+            assert (a, tok) == (a_g, tok_g), (k, a, tok, a_g, tok_g)
+            own += 1
+        a_r, tok_r, mg_r, gap_r = oracle.spec_sample(z_ref, T, draft.numpy(), ua, un)
+        tol_r = tol + 4 * dz / T
+        if mg_r > tol_r and gap_r > tol_r and all(t in full for t in range(a_r + 1)):
+            assert (a, tok) == (a_r, tok_r), (k, a, tok, a_r, tok_r)
+            vs_ref += 1
+    print(f"sampling verify step: logit difference {dz:.2e}; {own} of 6 decisions compared on the GPU's logits, "
+          f"{vs_ref} on the oracle's")
+    assert own >= 2
     assert s["ws"].status() == 0
 
 
@@ -121,7 +321,8 @@ def test_verify_step_m1_no_drafts(setup):
 
 def test_stack_and_verify_m8(setup):
     """M = 8 (gamma = 7) runs the three-block packing of the persistent kernel;
-    full size, against the oracle trajectory of the same 30 layers."""
+    full size, teacher-forced layer by layer and end to end against the oracle
+    trajectory of the same 30 layers."""
     s = setup
     fgm = s["fgm"]
     m = 8
@@ -132,11 +333,12 @@ def test_stack_and_verify_m8(setup):
         out = oracle.stack_layer(L, h)
         traj.append((out.ids.copy(), out.margin.copy(), h.copy()))
         h = out.y
+    _teacher_forced(fgm, s["ws"], s["layers"], s["host"], traj, m)
     trace = torch.empty((N_LAYERS, m, 8), dtype=torch.int32, device="cuda")
     y = fgm.moe_stack_fwd(s["layers"], x, ids_trace=trace, ws=s["ws"])
     torch.cuda.synchronize()
     full = _compare_stack(trace.cpu().numpy(), y, h, traj, s["host"], m)
-    assert len(full) >= 2, full
+    print(f"M = 8 tokens compared to the end: {full}")
     hn_bits = oracle.bf16_round(oracle.rmsnorm(h))
     am_ref, _, mg = oracle.lm_head(bf16_bits(s["emb"]), oracle.bf16_to_f64(hn_bits))
     draft = synth.drafts(43, am_ref)
