@@ -190,8 +190,9 @@ def test_verify_step_repeats_agree(setup):
         the row rms of each other. An fp32 difference in the residual stream
         moves the next layer's activation split (E4M3 terms whose resolution
         is about 2^-16 of a slice's maximum) and so grows from layer to layer:
-        measured about 1.3e-4 of the rms after 30 layers, a tenth of the bound
-        and a tenth of the parity tolerance;
+        after 30 layers, elements far below the rms differ by up to about
+        1.3e-4 of the rms (a tenth of the bound, a hundredth of the parity
+        tolerance); large elements differ by at most their final rounding;
       * the argmax of such a token, where the oracle's argmax margin exceeds
         1e-2, is identical across repeats, and so are the accepted count and
         next token when the accepted prefix is made of such tokens.
