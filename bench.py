@@ -471,6 +471,7 @@ def run_ours(args, rank, world):
             "l2": "no flush: each step streams > 5 GB of weights (L2 is 129 MB)",
             "mean_unique_experts_per_layer": round(statistics.mean(sum(uniq, [])), 2),
             "draft_seeds": N_DRAFT_SEEDS,
+            "algorithmic_bytes_by_batch": [int(b) for b in step_bytes],
             "tokens_per_step": f"value counts 1 + E[a] = {1 + ea:.4f} (E[a] = sum of 0.7^j, j = 1..4)",
         },
         "hbm_gbs": round(achieved, 1),
@@ -549,6 +550,20 @@ def run_case(args):
         run = lambda i: fgm.moe_layer_fwd(calls[i][0], calls[i][1], ws=ws)
         unit_bytes = nbytes
         name = "one MoE layer, M=5, Zipf s=1.1 (4 weight copies rotate)"
+    elif args.case == "layer_dense":
+        copies = [synth.layer(1 + c, device=dev, s=S_ZIPF) for c in range(4)]
+        denses = [synth.dense_mlp(100 + c, device=dev) for c in range(4)]
+        ids = torch.empty((M, 8), dtype=torch.int32, device=dev)
+        calls, nbytes = [], []
+        for i in range(max(K, W)):
+            p, d, x = copies[i % 4], denses[i % 4], xs[i % N_BATCHES]
+            fgm.moe_layer_dense_fwd(p, d, x, topk_ids=ids, ws=ws)
+            nbytes.append(traffic.layer_dense_bytes(len(torch.unique(ids.cpu()))))
+            calls.append((p, d, x))
+        run = lambda i: fgm.moe_layer_dense_fwd(calls[i][0], calls[i][1], calls[i][2], ws=ws)
+        unit_bytes = nbytes
+        name = ("one MoE layer with the 2816x2112 dense MLP in place of the shared expert, M=5, Zipf s=1.1 "
+                "(per-stage kernels; 4 weight copies rotate)")
     elif args.case == "lm_head_fp8":
         emb_q, emb_s = synth.embedding_fp8(synth.embedding(EMB_SEED, device=dev))
         torch.cuda.empty_cache()
@@ -784,9 +799,10 @@ def main():
                     help="verify case only: lm_head rows (a smaller case for ncu captures; default 262144)")
     ap.add_argument("--phase-trace", metavar="PATH", default=None,
                     help="after timing, run one traced step and write a per-phase summary to PATH")
-    ap.add_argument("--case", choices=("verify", "layer", "lm_head", "lm_head_fp8", "verify_fp8", "sweep"),
+    ap.add_argument("--case", choices=("verify", "layer", "layer_dense", "lm_head", "lm_head_fp8", "verify_fp8",
+                                       "sweep"),
                     default="verify",
-                    help="verify: the headline step; layer / lm_head / lm_head_fp8: one stage alone "
+                    help="verify: the headline step; layer / layer_dense / lm_head / lm_head_fp8: one stage alone "
                          "(profiling); verify_fp8: the step with the FP8 lm_head; sweep: the verify step "
                          "over M = 1..8 and Zipf s in {0, 1.1, 2} (one line each)")
     args = ap.parse_args()

@@ -47,6 +47,11 @@ class fgm_layer(ctypes.Structure):
                 ("router_w", "router_b", "gate_q", "gate_s", "up_q", "up_s", "down_q", "down_s")]
 
 
+class fgm_mlp(ctypes.Structure):
+    _fields_ = [(n, ctypes.c_void_p) for n in ("gate_q", "gate_s", "up_q", "up_s", "down_q", "down_s")] + \
+               [("width", ctypes.c_int)]
+
+
 def lib() -> ctypes.CDLL:
     """The loaded CUDA library; raises if it has not been built."""
     global _lib
@@ -63,6 +68,7 @@ def lib() -> ctypes.CDLL:
             "fgm_moe_layer_fwd": (ci, [LP, vp, vp, ci, vp, vp, vp, sz, vp]),
             "fgm_moe_layer_fwd_noalloc": (ci, [LP, vp, vp, ci, vp, vp, vp]),
             "fgm_moe_stack_fwd": (ci, [LP, ci, vp, vp, ci, vp, vp, sz, vp]),
+            "fgm_moe_layer_dense_fwd": (ci, [LP, ctypes.POINTER(fgm_mlp), vp, vp, ci, vp, vp, vp, sz, vp]),
             "fgm_lm_head_argmax": (ci, [vp, i64, vp, ci, vp, vp, vp, sz, vp]),
             "fgm_lm_head_argmax_fp8": (ci, [vp, vp, i64, vp, ci, vp, vp, vp, sz, vp]),
             "fgm_spec_verify": (ci, [vp, vp, ci, vp, vp]),
@@ -248,6 +254,37 @@ def moe_layer_fwd(layer, x: torch.Tensor, y: torch.Tensor | None = None,
     L = (layer if isinstance(layer, Layer) else Layer.from_dict(layer)).struct()
     _check(lib().fgm_moe_layer_fwd(ctypes.byref(L), _ptr(x), _ptr(y), M, _ptr(topk_ids), _ptr(topk_w),
                                    ws.ptr, ws.nbytes, _stream(stream)))
+    return y
+
+
+def _mlp_struct(mlp: dict) -> fgm_mlp:
+    W = int(mlp["gate_q"].shape[0])
+    shapes = {"gate_q": ((W, HIDDEN), torch.uint8), "up_q": ((W, HIDDEN), torch.uint8),
+              "down_q": ((HIDDEN, W), torch.uint8), "gate_s": ((W,), torch.float32),
+              "up_s": ((W,), torch.float32), "down_s": ((HIDDEN,), torch.float32)}
+    for name, (shape, dt) in shapes.items():
+        t = mlp[name]
+        if tuple(t.shape) != shape or t.dtype != dt or not t.is_contiguous():
+            raise FgmError(f"dense {name}: expected contiguous {shape} {dt}, got {tuple(t.shape)} {t.dtype}")
+    return fgm_mlp(*[_ptr(mlp[n]).value for n in ("gate_q", "gate_s", "up_q", "up_s", "down_q", "down_s")],
+                   W)
+
+
+def moe_layer_dense_fwd(layer, dense: dict, x: torch.Tensor, y: torch.Tensor | None = None,
+                        topk_ids: torch.Tensor | None = None, topk_w: torch.Tensor | None = None,
+                        ws: Workspace | None = None, stream=None) -> torch.Tensor:
+    """One MoE layer with the always-on dense MLP `dense` (gate_q/up_q [W, 2816],
+    down_q [2816, W], fp32 row scales; W a multiple of 704 up to 2112) in place
+    of the shared expert; returns bf16 y."""
+    M = _m(x)
+    y = torch.empty_like(x) if y is None else y
+    _check_like("y", y, x)
+    _check_topk(M, x, topk_ids, topk_w)
+    ws = _ws(ws, x.device)
+    L = (layer if isinstance(layer, Layer) else Layer.from_dict(layer)).struct()
+    D = _mlp_struct(dense)
+    _check(lib().fgm_moe_layer_dense_fwd(ctypes.byref(L), ctypes.byref(D), _ptr(x), _ptr(y), M, _ptr(topk_ids),
+                                         _ptr(topk_w), ws.ptr, ws.nbytes, _stream(stream)))
     return y
 
 

@@ -164,11 +164,11 @@ __device__ __forceinline__ void warp_topk8(const float *__restrict__ lrow, int l
 }
 
 // Top-k for all tokens, then the distinct-expert list: slots 0..U-1 hold the
-// distinct routed experts in ascending id order, slot U the shared expert.
-// comb[s][t] is token t's routing weight for slot s (0 if not routed, 1 for
-// the shared slot), so every slot can be evaluated for all tokens and
-// weighted afterwards.
-__global__ void __launch_bounds__(256) k_topk_dedup(const float *__restrict__ logits, int M,
+// distinct routed experts in ascending id order, slots U..U+n_shared-1 the
+// shared part(s) (expert kE + p). comb[s][t] is token t's routing weight for
+// slot s (0 if not routed, 1 for a shared slot), so every slot can be
+// evaluated for all tokens and weighted afterwards.
+__global__ void __launch_bounds__(256) k_topk_dedup(const float *__restrict__ logits, int M, int n_shared,
                                                     int32_t *__restrict__ meta,
                                                     float *__restrict__ comb,
                                                     int32_t *__restrict__ ids_out,
@@ -204,12 +204,13 @@ __global__ void __launch_bounds__(256) k_topk_dedup(const float *__restrict__ lo
         }
         if (lane == 0) {
             meta[0] = base;
-            meta[1 + base] = kShared;
+            for (int p = 0; p < n_shared; ++p)
+                meta[1 + base + p] = kShared + p;
             s_nu = base;
         }
     }
     __syncthreads();
-    const int n_slots = s_nu + 1;
+    const int n_slots = s_nu + n_shared;
     for (int i = threadIdx.x; i < n_slots * kMaxM; i += blockDim.x)
         comb[i] = 0.0f;
     __syncthreads();
@@ -222,16 +223,17 @@ __global__ void __launch_bounds__(256) k_topk_dedup(const float *__restrict__ lo
                 w_out[t * kK + r] = s_w[t][r];
         }
     }
-    if (threadIdx.x < kMaxM)
-        comb[s_nu * kMaxM + threadIdx.x] = threadIdx.x < M ? 1.0f : 0.0f;
+    if (threadIdx.x < n_shared * kMaxM)
+        comb[(s_nu + threadIdx.x / kMaxM) * kMaxM + threadIdx.x % kMaxM] = threadIdx.x % kMaxM < M ? 1.0f : 0.0f;
 }
 
 // ---------------------------------------------------------------- experts
 
-// Gate/up + gated GELU. Grid (22, 65): blockIdx.y is the slot, each CTA covers
+// Gate/up + gated GELU. Grid (22, 67): blockIdx.y is the slot, each CTA covers
 // 32 rows of the 704 (8 warps x 4 rows). A warp streams gate row i and up row
 // i with 16-byte loads and keeps M dot products of each; the activation
-// act[s][t][i] = comb[s][t] * gelu_tanh(s_g g) * (s_u u).
+// act[s][t][i] = comb[s][t] * gelu_tanh(s_g g) * (s_u u). Slots of expert
+// kE + p read part p of the dense shared MLP when dn.parts > 0.
 template <int M>
 __global__ void __launch_bounds__(256) k_gateup_basic(const uint8_t *__restrict__ gq,
                                                       const float *__restrict__ gs,
@@ -240,14 +242,21 @@ __global__ void __launch_bounds__(256) k_gateup_basic(const uint8_t *__restrict_
                                                       const float *__restrict__ xn,
                                                       const int32_t *__restrict__ meta,
                                                       const float *__restrict__ comb,
-                                                      float *__restrict__ act)
+                                                      float *__restrict__ act, DenseArgs dn)
 {
     extern __shared__ float4 smem4[];
     float *sx = reinterpret_cast<float *>(smem4);
     const int slot = blockIdx.y;
-    if (slot > meta[0])
+    if (slot >= meta[0] + (dn.parts ? dn.parts : 1))
         return;
-    const int expert = meta[1 + slot];
+    int expert = meta[1 + slot];
+    if (expert >= kE && dn.parts) {   // part p of the dense MLP: the same layout as an expert
+        gq = dn.gq;
+        gs = dn.gs;
+        uq = dn.uq;
+        us = dn.us;
+        expert -= kE;
+    }
     for (int i = threadIdx.x; i < M * kH / 4; i += blockDim.x)
         smem4[i] = reinterpret_cast<const float4 *>(xn)[i];
     __syncthreads();
@@ -297,21 +306,28 @@ __global__ void __launch_bounds__(256) k_gateup_basic(const uint8_t *__restrict_
     }
 }
 
-// Down projection + combine. Grid (88, 65): slot blockIdx.y, 32 output rows per
+// Down projection + combine. Grid (88, 67): slot blockIdx.y, 32 output rows per
 // CTA (8 warps x 4 rows). out[t][j] += s_d[j] * (Q_d[j] . act[s][t]); several
-// slots add into the same output element with fp32 atomics.
+// slots add into the same output element with fp32 atomics. Part p of a dense
+// shared MLP reads columns p * 704 .. of its full-width down rows and their
+// scales.
 template <int M>
 __global__ void __launch_bounds__(256) k_down_basic(const uint8_t *__restrict__ dq,
                                                     const float *__restrict__ ds,
                                                     const float *__restrict__ act,
                                                     const int32_t *__restrict__ meta,
-                                                    float *__restrict__ out)
+                                                    float *__restrict__ out, DenseArgs dn)
 {
     __shared__ __align__(16) float sa[M * kF];
     const int slot = blockIdx.y;
-    if (slot > meta[0])
+    if (slot >= meta[0] + (dn.parts ? dn.parts : 1))
         return;
     const int expert = meta[1 + slot];
+    const bool dense = expert >= kE && dn.parts;
+    // row j of this slot's down matrix and its scale
+    const size_t row_stride = dense ? (size_t)dn.parts * kF : kF;
+    const uint8_t *dbase = dense ? dn.dq + (size_t)(expert - kE) * kF : dq + (size_t)expert * kH * kF;
+    const float *sbase = dense ? dn.ds : ds + (size_t)expert * kH;
     for (int i = threadIdx.x; i < M * kF; i += blockDim.x)
         sa[i] = act[((size_t)slot * kMaxM + i / kF) * kF + i % kF];
     __syncthreads();
@@ -320,7 +336,7 @@ __global__ void __launch_bounds__(256) k_down_basic(const uint8_t *__restrict__ 
         const int j = (blockIdx.x * 8 + warp) * 4 + r;
         if (j >= kH)
             break;
-        const uint8_t *drow = dq + ((size_t)expert * kH + j) * kF;
+        const uint8_t *drow = dbase + (size_t)j * row_stride;
         float a[M];
 #pragma unroll
         for (int t = 0; t < M; ++t)
@@ -345,7 +361,7 @@ __global__ void __launch_bounds__(256) k_down_basic(const uint8_t *__restrict__ 
         for (int t = 0; t < M; ++t)
             a[t] = warp_sum(a[t]);
         if (lane == 0) {
-            const float sd = ds[(size_t)expert * kH + j];
+            const float sd = sbase[j];
 #pragma unroll
             for (int t = 0; t < M; ++t)
                 atomicAdd(out + (size_t)t * kH + j, sd * a[t]);

@@ -20,6 +20,8 @@ constexpr int kK = FGM_TOPK;           // routed experts per token
 constexpr int kMaxM = FGM_MAX_M;       // tokens per call
 constexpr int kShared = kE;            // index of the shared expert
 constexpr int kMaxSlots = kMaxM * kK + 1;  // distinct routed experts + shared
+constexpr int kMaxDense = 3;               // 704-wide parts of a dense shared MLP (up to 2112 wide)
+constexpr int kMaxSlotsAll = kMaxM * kK + kMaxDense;   // routed + dense parts (per-stage kernels)
 constexpr int kMaxParts = 2048;        // lm_head per-CTA partials kept in the workspace
 constexpr float kEps = FGM_RMS_EPS;
 constexpr int kSyncLmHeadDone = 127;   // workspace sync word counting finished FP8 lm_head CTAs
@@ -30,10 +32,11 @@ struct Ws {
     float *xn;         // [8][2816] fp32 layer input (normed in the stack)
     float *acc;        // [8][2816] fp32 layer output accumulator
     float *logits;     // [8][128] router logits (bias included)
-    int32_t *meta;     // [0] = distinct routed experts U, [1 + s] = expert of slot s (slot U: shared)
-    float *comb;       // [65][8] routing weight of slot s for token t (0 when not routed)
-    float *act;        // [2][65][8][704] weighted gated activations per slot and token (the staged
-                       // path uses buffer 0; the persistent kernel alternates by layer)
+    int32_t *meta;     // [0] = distinct routed experts U, [1 + s] = expert of slot s (slots U..: the
+                       // shared expert, or the parts kE + p of a dense shared MLP)
+    float *comb;       // [67][8] routing weight of slot s for token t (0 when not routed)
+    float *act;        // [2][67][8][704] weighted gated activations per slot and token (the staged
+                       // path uses buffer 0; the persistent kernel alternates by layer over 65 slots)
     int32_t *ids;      // [8][8] chosen experts of the last routed layer
     float *wts;        // [8][8] their weights
     float *part_val;   // [kMaxParts][8] lm_head per-CTA best logit
@@ -72,9 +75,9 @@ inline WsOffsets ws_offsets()
     o.xn = take(sizeof(float) * kMaxM * kH);
     o.acc = take(sizeof(float) * kMaxM * kH);
     o.logits = take(sizeof(float) * kMaxM * kE);
-    o.meta = take(sizeof(int32_t) * (kMaxSlots + 8));
-    o.comb = take(sizeof(float) * kMaxSlots * kMaxM);
-    o.act = take(sizeof(float) * 2 * kMaxSlots * kMaxM * kF);
+    o.meta = take(sizeof(int32_t) * (kMaxSlotsAll + 8));
+    o.comb = take(sizeof(float) * kMaxSlotsAll * kMaxM);
+    o.act = take(sizeof(float) * 2 * kMaxSlotsAll * kMaxM * kF);
     o.ids = take(sizeof(int32_t) * kMaxM * kK);
     o.wts = take(sizeof(float) * kMaxM * kK);
     o.part_val = take(sizeof(float) * kMaxParts * kMaxM);
@@ -121,6 +124,21 @@ inline Ws ws_carve(void *base)
     w.part_sum = reinterpret_cast<float *>(b + o.part_sum);
     return w;
 }
+
+// Optional dense shared MLP of the per-stage layer kernels, in its natural
+// layout: gate/up [parts * 704][2816], down [2816][parts * 704] (row stride
+// parts * 704), fp32 row scales. Part p acts as expert kE + p: gate/up rows
+// p * 704 .. and down columns p * 704 .., with the down rows' full-width
+// scales. parts = 0: the layer's own shared expert.
+struct DenseArgs {
+    const uint8_t *gq;
+    const float *gs;
+    const uint8_t *uq;
+    const float *us;
+    const uint8_t *dq;
+    const float *ds;
+    int parts;
+};
 
 // ---------------------------------------------------------------- formats
 

@@ -205,39 +205,41 @@ int check_m(int M)
     } while (0)
 
 template <int M>
-int launch_layer_experts(const fgm_layer *L, const Ws &w, float *out, cudaStream_t st)
+int launch_layer_experts(const fgm_layer *L, const Ws &w, float *out, const DenseArgs &dn, cudaStream_t st)
 {
-    k_gateup_basic<M><<<dim3(kF / 32, kMaxSlots), 256, M * kH * 4, st>>>(
-        L->gate_q, L->gate_s, L->up_q, L->up_s, w.xn, w.meta, w.comb, w.act);
+    k_gateup_basic<M><<<dim3(kF / 32, kMaxSlotsAll), 256, M * kH * 4, st>>>(
+        L->gate_q, L->gate_s, L->up_q, L->up_s, w.xn, w.meta, w.comb, w.act, dn);
     FGM_CHECK_LAUNCH();
-    k_down_basic<M><<<dim3(kH / 32, kMaxSlots), 256, 0, st>>>(L->down_q, L->down_s, w.act, w.meta, out);
+    k_down_basic<M><<<dim3(kH / 32, kMaxSlotsAll), 256, 0, st>>>(L->down_q, L->down_s, w.act, w.meta, out, dn);
     FGM_CHECK_LAUNCH();
     return FGM_OK;
 }
 
-int launch_experts(int M, const fgm_layer *L, const Ws &w, float *out, cudaStream_t st)
+int launch_experts(int M, const fgm_layer *L, const Ws &w, float *out, const DenseArgs &dn, cudaStream_t st)
 {
     switch (M) {
-    case 1: return launch_layer_experts<1>(L, w, out, st);
-    case 2: return launch_layer_experts<2>(L, w, out, st);
-    case 3: return launch_layer_experts<3>(L, w, out, st);
-    case 4: return launch_layer_experts<4>(L, w, out, st);
-    case 5: return launch_layer_experts<5>(L, w, out, st);
-    case 6: return launch_layer_experts<6>(L, w, out, st);
-    case 7: return launch_layer_experts<7>(L, w, out, st);
-    default: return launch_layer_experts<8>(L, w, out, st);
+    case 1: return launch_layer_experts<1>(L, w, out, dn, st);
+    case 2: return launch_layer_experts<2>(L, w, out, dn, st);
+    case 3: return launch_layer_experts<3>(L, w, out, dn, st);
+    case 4: return launch_layer_experts<4>(L, w, out, dn, st);
+    case 5: return launch_layer_experts<5>(L, w, out, dn, st);
+    case 6: return launch_layer_experts<6>(L, w, out, dn, st);
+    case 7: return launch_layer_experts<7>(L, w, out, dn, st);
+    default: return launch_layer_experts<8>(L, w, out, dn, st);
     }
 }
 
-// Router + dedup + experts of one layer reading w.xn, adding into `out`.
+// Router + dedup + experts of one layer reading w.xn, adding into `out`; with
+// dn.parts > 0 the dense shared MLP takes the place of the shared expert.
 int run_layer(int M, const fgm_layer *L, const Ws &w, float *out, int32_t *ids_out, float *w_out,
-              cudaStream_t st)
+              cudaStream_t st, const DenseArgs &dn = DenseArgs{})
 {
     k_router_logits<<<kE, 256, 0, st>>>(w.xn, M, L->router_w, L->router_b, w.logits);
     FGM_CHECK_LAUNCH();
-    k_topk_dedup<<<1, 256, 0, st>>>(w.logits, M, w.meta, w.comb, ids_out, w_out, w.status);
+    k_topk_dedup<<<1, 256, 0, st>>>(w.logits, M, dn.parts ? dn.parts : 1, w.meta, w.comb, ids_out, w_out,
+                                     w.status);
     FGM_CHECK_LAUNCH();
-    return launch_experts(M, L, w, out, st);
+    return launch_experts(M, L, w, out, dn, st);
 }
 
 int lmhead_grid(int sms) { return sms * 4 < kMaxParts ? sms * 4 : kMaxParts; }
@@ -415,6 +417,44 @@ int fgm_moe_layer_fwd(const fgm_layer *layer, const uint16_t *x, uint16_t *y, in
     k_layer_prep<<<16, 256, 0, st>>>(x, M, w.xn, w.acc);
     FGM_CHECK_LAUNCH();
     FGM_TRY(run_layer(M, layer, w, w.acc, topk_ids, topk_w, st));
+    k_f32_to_bf16<<<16, 256, 0, st>>>(w.acc, M * kH, y);
+    FGM_CHECK_LAUNCH();
+    return FGM_OK;
+}
+
+int fgm_moe_layer_dense_fwd(const fgm_layer *layer, const fgm_mlp *dense, const uint16_t *x, uint16_t *y, int M,
+                            int32_t *topk_ids, float *topk_w, void *ws, size_t ws_bytes, void *stream)
+{
+    FGM_TRY(check_m(M));
+    FGM_TRY(check_layer(layer, 0));
+    if (!dense)
+        return fail(FGM_ERR_INVALID_ARG, "dense is NULL");
+    if (dense->width < kF || dense->width > kMaxDense * kF || dense->width % kF)
+        return fail(FGM_ERR_INVALID_ARG, "dense width %d: a multiple of %d up to %d", dense->width, kF,
+                    kMaxDense * kF);
+    {
+        const void *q[] = {dense->gate_q, dense->up_q, dense->down_q};
+        const void *sc[] = {dense->gate_s, dense->up_s, dense->down_s};
+        for (int i = 0; i < 3; ++i) {
+            if (!q[i] || !aligned16(q[i]))
+                return fail(FGM_ERR_INVALID_ARG, "dense weight %d NULL or not 16-byte aligned", i);
+            if (!sc[i] || (reinterpret_cast<uintptr_t>(sc[i]) & 3u))
+                return fail(FGM_ERR_INVALID_ARG, "dense scale %d NULL or not 4-byte aligned", i);
+        }
+    }
+    if (!x || !y || !aligned16(x) || !aligned16(y))
+        return fail(FGM_ERR_INVALID_ARG, "x/y NULL or not 16-byte aligned");
+    if (x == y)
+        return fail(FGM_ERR_INVALID_ARG, "y may not alias x");
+    FGM_TRY(check_ws(ws, ws_bytes, M, 0));
+    FGM_TRY(device_ready(nullptr));
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    Ws w = ws_carve(ws);
+    const DenseArgs dn{dense->gate_q, dense->gate_s, dense->up_q, dense->up_s, dense->down_q, dense->down_s,
+                       dense->width / kF};
+    k_layer_prep<<<16, 256, 0, st>>>(x, M, w.xn, w.acc);
+    FGM_CHECK_LAUNCH();
+    FGM_TRY(run_layer(M, layer, w, w.acc, topk_ids, topk_w, st, dn));
     k_f32_to_bf16<<<16, 256, 0, st>>>(w.acc, M * kH, y);
     FGM_CHECK_LAUNCH();
     return FGM_OK;

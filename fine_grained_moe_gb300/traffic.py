@@ -40,6 +40,18 @@ def lm_head_fp8_bytes(vocab: int = VOCAB, hidden: int = HIDDEN) -> int:
     return vocab * hidden + 4 * vocab
 
 
+def dense_mlp_bytes(width: int = 3 * FFN, hidden: int = HIDDEN) -> int:
+    """An always-on dense gated-GELU MLP of the given width: gate/up [W, H] and
+    down [H, W] in E4M3, plus fp32 row scales (2W + H)."""
+    return 3 * hidden * width + 4 * (2 * width + hidden)
+
+
+def layer_dense_bytes(unique: int, width: int = 3 * FFN, with_bias: bool = True) -> int:
+    """Unique bytes of one layer whose shared expert is the dense MLP: router,
+    the distinct routed experts, and the MLP."""
+    return int(unique) * expert_bytes() + dense_mlp_bytes(width) + router_bytes(with_bias=with_bias)
+
+
 def step_bytes(unique_per_layer, *, vocab: int = VOCAB, with_lm_head: bool = True,
                n_shared: int = 1, with_bias: bool = True, fp8_lm_head: bool = False) -> int:
     """Unique bytes of one step: for each layer the router and (unique routed +

@@ -94,6 +94,19 @@ typedef struct fgm_layer {
     const float *down_s;
 } fgm_layer;
 
+/* An always-on dense (shared) gated-GELU MLP of width W, E4M3 weights with
+ * one fp32 scale per output row (the experts' format):
+ *   mlp(x) = s_d (Q_d (gelu_tanh(s_g (Q_g x)) * s_u (Q_u x))). */
+typedef struct fgm_mlp {
+    const uint8_t *gate_q;  /* E4M3 [W][2816], 16-byte aligned */
+    const float *gate_s;    /* [W] */
+    const uint8_t *up_q;    /* E4M3 [W][2816] */
+    const float *up_s;      /* [W] */
+    const uint8_t *down_q;  /* E4M3 [2816][W] (row stride W bytes) */
+    const float *down_s;    /* [2816] */
+    int width;              /* W: a multiple of 704, at most 2112 */
+} fgm_mlp;
+
 /* Bytes of scratch an M-token call needs; V is the vocabulary size for the
  * lm_head entry points (0 if unused). Never fails; 0 for M out of range. */
 size_t fgm_workspace_bytes(int M, int64_t V);
@@ -145,6 +158,20 @@ int fgm_moe_layer_fwd(const fgm_layer *layer, const uint16_t *x, uint16_t *y, in
  *    use fgm_moe_layer_fwd when the status must be checked. */
 int fgm_moe_layer_fwd_noalloc(const fgm_layer *layer, const uint16_t *x, uint16_t *y, int M,
                               int32_t *topk_ids, float *topk_w, void *stream);
+
+/* fgm_moe_layer_fwd with an always-on dense MLP of width W in place of the
+ * shared expert (the layer's expert 128 is not read):
+ *   y_t = sum_{i<8} w_{t,i} * expert_{id_{t,i}}(x_t) + mlp(x_t).
+ * A GeGLU MLP splits exactly into W/704 column blocks of width 704 whose
+ * outputs add up (each down row keeps its full-width scale), so the kernels
+ * run it as W/704 always-on parts of weight 1 next to the routed experts.
+ * Source: "llm-decoding" §"Where the 7.36 GB goes" (an always-on dense MLP of
+ * 2816 x 2112 per layer). Runs on the per-stage kernels whatever
+ * fgm_select_path chose.
+ *  dense   HOST pointer to the MLP's device weights (see fgm_mlp)
+ *  other arguments as fgm_moe_layer_fwd */
+int fgm_moe_layer_dense_fwd(const fgm_layer *layer, const fgm_mlp *dense, const uint16_t *x, uint16_t *y, int M,
+                            int32_t *topk_ids, float *topk_w, void *ws, size_t ws_bytes, void *stream);
 
 /* n_layers stacked layers (attention omitted), each
  *   h <- h + moe_layer(RMSNorm(h)),  RMSNorm(h) = h / sqrt(mean(h^2) + 1e-6),
