@@ -364,7 +364,7 @@ def run_ours(args, rank, world):
     dev = torch.device("cuda", int(os.environ.get("LOCAL_RANK", 0)))
     torch.cuda.set_device(dev)
     fgm.lib()
-    fgm.select_path(fgm.PATH_FUSED if args.path == "fused" else fgm.PATH_STAGED)
+    fgm.select_path({"fused": fgm.PATH_FUSED, "staged": fgm.PATH_STAGED, "fused_tc": fgm.PATH_FUSED_TC}[args.path])
     nl, V = args.layers, args.vocab
     full_size = (nl, V) == (N_LAYERS, 262144)
     if args.phase_trace and not full_size:
@@ -484,7 +484,7 @@ def run_ours(args, rank, world):
         "p99_ms": round(sorted(per_step)[min(K - 1, int(0.99 * K))], 4),
         "path": args.path,
         "roofline": {
-            "kernel": ("k_fused (one persistent launch per step)" if args.path == "fused"
+            "kernel": ("k_fused (one persistent launch per step)" if args.path != "staged"
                        else "verify step (all launches of one step)"),
             "bound": "hbm",
             "achieved": round(achieved, 1),
@@ -492,13 +492,13 @@ def run_ours(args, rank, world):
             "peak_kind": f"{peak_kind} copy bandwidth",
             "unit": "GB/s",
             "frac": round(achieved / peak, 4),
-            "traffic": (captured_traffic() if args.path == "fused" and full_size else None),
+            "traffic": (captured_traffic() if args.path != "staged" and full_size else None),
             "algorithmic_bytes_per_launch": int(bytes_total / K),
         },
         "e2e": {"value": round(world * K * (1 + ea) / e2e_max, 2), "unit": "tokens/s",
                 "measured_accept_value": round(e2e_tok_all / e2e_max, 2),
                 "h2d_bytes_per_step": M * 2816 * 2 + GAMMA * 4, "d2h_bytes_per_step": 8},
-        "gpu_launches": K * (1 if args.path == "fused" else 1 + nl * 5 + 3),
+        "gpu_launches": K * (1 if args.path != "staged" else 1 + nl * 5 + 3),
         "clocks": {"sm_mhz": clocks["sm_mhz"], "sm_max_mhz": clocks["sm_max_mhz"],
                    "reasons": clocks["reasons"]},
         "status": status,
@@ -533,7 +533,7 @@ def run_case(args):
     dev = torch.device("cuda", 0)
     torch.cuda.set_device(dev)
     fgm.lib()
-    fgm.select_path(fgm.PATH_FUSED if args.path == "fused" else fgm.PATH_STAGED)
+    fgm.select_path({"fused": fgm.PATH_FUSED, "staged": fgm.PATH_STAGED, "fused_tc": fgm.PATH_FUSED_TC}[args.path])
     ws = fgm.Workspace(dev)
     xs = [synth.hidden_states(HIDDEN_SEED0 + b, M, device=dev) for b in range(N_BATCHES)]
     K, W = args.steps, args.warmup
@@ -610,7 +610,7 @@ def run_sweep(args):
     dev = torch.device("cuda", 0)
     torch.cuda.set_device(dev)
     fgm.lib()
-    fgm.select_path(fgm.PATH_FUSED if args.path == "fused" else fgm.PATH_STAGED)
+    fgm.select_path({"fused": fgm.PATH_FUSED, "staged": fgm.PATH_STAGED, "fused_tc": fgm.PATH_FUSED_TC}[args.path])
     layers, emb, _ = make_workload(dev)
     ws = fgm.Workspace(dev)
     peak, _ = measured_peaks()
@@ -670,7 +670,7 @@ def run_verify_fp8(args):
     dev = torch.device("cuda", 0)
     torch.cuda.set_device(dev)
     fgm.lib()
-    fgm.select_path(fgm.PATH_FUSED if args.path == "fused" else fgm.PATH_STAGED)
+    fgm.select_path({"fused": fgm.PATH_FUSED, "staged": fgm.PATH_STAGED, "fused_tc": fgm.PATH_FUSED_TC}[args.path])
     layers, emb, xs = make_workload(dev)
     emb_q, emb_s = synth.embedding_fp8(emb)
     del emb
@@ -715,7 +715,7 @@ def run_verify_fp8(args):
             "ms_per_step": round(ms / K, 4), "accepted_per_step": round((tokens - K) / K, 3),
             "algorithmic_bytes_per_step": int(statistics.mean(nbytes)),
             "hbm_gbs": round(gbs, 1), "frac_of_peak": round(gbs / peak, 4), "peak": peak, "peak_kind": kind,
-            "launches_per_step": 2 if args.path == "fused" else 1 + N_LAYERS * 5 + 1,
+            "launches_per_step": 2 if args.path != "staged" else 1 + N_LAYERS * 5 + 1,
             "clocks": {"sm_mhz": clocks["sm_mhz"], "sm_max_mhz": clocks["sm_max_mhz"],
                        "reasons": clocks["reasons"]},
             "status": ws.status()}
@@ -791,8 +791,9 @@ def main():
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=("ours", "reference"), default="ours")
     ap.add_argument("--no-cpu-baseline", action="store_true")
-    ap.add_argument("--path", choices=("fused", "staged"), default="fused",
-                    help="persistent kernel (default) or one launch per stage")
+    ap.add_argument("--path", choices=("fused", "staged", "fused_tc"), default="fused",
+                    help="persistent kernel (default), one launch per stage, or the persistent kernel with the "
+                         "tcgen05 FP8 lm_head")
     ap.add_argument("--layers", type=int, default=N_LAYERS,
                     help="verify case only: stack depth (a smaller case for ncu captures; default 30)")
     ap.add_argument("--vocab", type=int, default=262144,

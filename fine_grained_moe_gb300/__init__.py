@@ -32,6 +32,7 @@ STATUS_NONFINITE_LOGITS = 1
 STATUS_WAIT_TIMEOUT = 2
 PATH_FUSED = 0    # one persistent cooperative kernel per call (TMA ring + mma.sync tiles)
 PATH_STAGED = 1   # one launch per stage, fp32 CUDA-core arithmetic
+PATH_FUSED_TC = 2  # as PATH_FUSED, with the FP8 lm_head on tcgen05 tensor-memory tiles fed by TMA tensor copies
 
 _PKG = os.path.dirname(os.path.abspath(__file__))
 LIB_PATH = os.path.join(_PKG, "libfgm.so")

@@ -63,6 +63,8 @@ enum {
     FGM_PATH_FUSED = 0,  /* default: one persistent cooperative kernel per call; weight rows stream
                             through a TMA-bulk shared-memory ring into FP8/bf16 mma.sync tiles */
     FGM_PATH_STAGED = 1, /* one launch per stage with fp32 CUDA-core arithmetic (comparison path) */
+    FGM_PATH_FUSED_TC = 2, /* as FGM_PATH_FUSED, with the FP8 lm_head on the tensor-memory kernel
+                              (tcgen05.mma, TMA tensor copies) instead of the mma.sync one */
 };
 
 /* Status bits written by kernels into the workspace (fgm_read_status). */

@@ -3,7 +3,8 @@ against the oracle: argmax bit-exact where the oracle's top-1/top-2 margin
 exceeds 1e-2, otherwise the chosen row's oracle logit within 1e-2 of the top;
 the winning logit within 1e-4. Sizes from one ragged tile to the full
 262,144-word vocabulary; the edge cases are ties, NaN codes and hidden rows of
-extreme magnitude (the kernel's power-of-two f16 scaling)."""
+extreme magnitude (the power-of-two scaling of the hidden rows' E4M3 terms).
+Both kernels: the mma.sync one and the tensor-memory one (tcgen05)."""
 
 import numpy as np
 import pytest
@@ -16,11 +17,15 @@ from helpers import MARGIN, bf16_values, dequant_torch
 pytestmark = pytest.mark.gpu
 
 
-@pytest.fixture(scope="module")
-def fgm():
+@pytest.fixture(scope="module", params=[0, 1, 2], ids=["fused", "staged", "fused_tc"])
+def fgm(request):
+    """fused and staged: the mma.sync kernel; fused_tc: the tensor-memory kernel
+    (tcgen05.mma, TMA tensor copies)."""
     import fine_grained_moe_gb300 as m
     m.lib()
-    return m
+    prev = m.select_path(request.param)
+    yield m
+    m.select_path(prev)
 
 
 @pytest.fixture(scope="module")
