@@ -563,7 +563,7 @@ def run_case(args):
         run = lambda i: fgm.moe_layer_dense_fwd(calls[i][0], calls[i][1], calls[i][2], ws=ws)
         unit_bytes = nbytes
         name = ("one MoE layer with the 2816x2112 dense MLP in place of the shared expert, M=5, Zipf s=1.1 "
-                "(per-stage kernels; 4 weight copies rotate)")
+                "(4 weight copies rotate)")
     elif args.case == "lm_head_fp8":
         emb_q, emb_s = synth.embedding_fp8(synth.embedding(EMB_SEED, device=dev))
         torch.cuda.empty_cache()

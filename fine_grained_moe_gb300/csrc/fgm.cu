@@ -96,10 +96,12 @@ int device_ready(int *sms)
             FGM_SMEM(fp8tc::k_lmhead_fp8_tc<false>, fp8tc::kSmemBytes);
             FGM_SMEM(fp8tc::k_lmhead_fp8_tc<true>, fp8tc::kSmemBytes);
 #undef FGM_SMEM
-            const void *kerns[4] = {reinterpret_cast<const void *>(fused::k_fused<2, false>),
+            const void *kerns[6] = {reinterpret_cast<const void *>(fused::k_fused<2, false>),
                                     reinterpret_cast<const void *>(fused::k_fused<3, false>),
                                     reinterpret_cast<const void *>(fused::k_fused<2, true>),
-                                    reinterpret_cast<const void *>(fused::k_fused<3, true>)};
+                                    reinterpret_cast<const void *>(fused::k_fused<3, true>),
+                                    reinterpret_cast<const void *>(fused::k_fused<2, false, 3>),
+                                    reinterpret_cast<const void *>(fused::k_fused<3, false, 3>)};
             int per_sm = 1 << 30;
             for (const void *k : kerns) {
                 FGM_CUDA(cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)sizeof(fused::Smem)));
@@ -142,11 +144,16 @@ int launch_fused(fused::Params &prm, cudaStream_t st)
     g_debug_stall = 0;
     void *args[] = {&prm};
     // packed activation columns: 2 blocks of 8 hold M <= 5 tokens x 3 terms, 3 blocks M <= 8
-    const bool traced = prm.trace != nullptr;
-    const void *kern = prm.M <= 5 ? (traced ? reinterpret_cast<const void *>(fused::k_fused<2, true>)
-                                            : reinterpret_cast<const void *>(fused::k_fused<2, false>))
-                                  : (traced ? reinterpret_cast<const void *>(fused::k_fused<3, true>)
-                                            : reinterpret_cast<const void *>(fused::k_fused<3, false>));
+    const bool traced = prm.trace != nullptr && prm.dense.parts == 0;
+    const void *kern = prm.dense.parts == 3
+                           ? (prm.M <= 5 ? reinterpret_cast<const void *>(fused::k_fused<2, false, 3>)
+                                         : reinterpret_cast<const void *>(fused::k_fused<3, false, 3>))
+                       : prm.M <= 5 ? (traced ? reinterpret_cast<const void *>(fused::k_fused<2, true>)
+                                              : reinterpret_cast<const void *>(fused::k_fused<2, false>))
+                                    : (traced ? reinterpret_cast<const void *>(fused::k_fused<3, true>)
+                                              : reinterpret_cast<const void *>(fused::k_fused<3, false>));
+    if (!traced)
+        prm.trace = nullptr;
     FGM_CUDA(cudaLaunchCooperativeKernel(kern, dim3(G),
                                          dim3(fused::kThreads), args, sizeof(fused::Smem), st));
     return FGM_OK;
@@ -522,6 +529,18 @@ int fgm_moe_layer_dense_fwd(const fgm_layer *layer, const fgm_mlp *dense, const 
     Ws w = ws_carve(ws);
     const DenseArgs dn{dense->gate_q, dense->gate_s, dense->up_q, dense->up_s, dense->down_q, dense->down_s,
                        dense->width / kF};
+    if (g_path != FGM_PATH_STAGED && dn.parts == kMaxDense) {
+        // the persistent kernel with the MLP's three parts as its always-on slots
+        fused::Params prm = fused_params(fused::kModeLayer, M, w);
+        prm.layers[0] = *layer;
+        prm.n_layers = 1;
+        prm.x = x;
+        prm.y = y;
+        prm.ids = topk_ids;
+        prm.wts = topk_w;
+        prm.dense = dn;
+        return launch_fused(prm, st);
+    }
     k_layer_prep<<<16, 256, 0, st>>>(x, M, w.xn, w.acc);
     FGM_CHECK_LAUNCH();
     FGM_TRY(run_layer(M, layer, w, w.acc, topk_ids, topk_w, st, dn));

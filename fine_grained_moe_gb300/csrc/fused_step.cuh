@@ -59,11 +59,12 @@ constexpr int kDownTiles = 4;                 // 16-row down tiles per ring slot
 constexpr int kRouterCtas = 64;               // the last 64 CTAs compute the router logits,
 constexpr int kRouterRows = FGM_EXPERTS / kRouterCtas;   // 2 rows each (fewer CTAs read the residual)
 constexpr int kTerms = 3;                     // E4M3 terms per activation
-constexpr int kSharedSlot = kMaxSlots - 1;
+constexpr int kSharedSlot = kMaxM * kK;     // first always-on slot: the shared expert, or dense part p at + p
 constexpr uint32_t kActPending = 0x7FC0DEADu;   // NaN marker: activation row not written yet
 constexpr int kMinCtas = 128;                 // the persistent kernel needs at least this many SMs
-constexpr int kMaxGuRows = 8 * ((kMaxSlots * (kF / 8) + kMinCtas - 1) / kMinCtas);   // routed row pairs per CTA
-constexpr int kMaxDownRows = 16 * (kMaxSlots * (kH / 16) / kMinCtas + 5);   // down rows per CTA (see down_rows)
+constexpr int kMaxGuRows = 8 * ((kMaxSlotsAll * (kF / 8) + kMinCtas - 1) / kMinCtas);   // routed row pairs per CTA
+constexpr int kMaxDownRows = 16 * (kMaxSlotsAll * (kH / 16) / kMinCtas + 5);   // down rows per CTA (see down_rows)
+constexpr int kMaxShTiles = (kMaxDense * (kF / 8) + kMinCtas - 1) / kMinCtas;   // always-on gate/up tiles per CTA
 
 enum Mode { kModeLayer = 0, kModeStack = 1, kModeVerify = 2, kModeLmHead = 3 };
 enum TileKind { kTileGateUp = 0, kTileDown = 1, kTileLmHead = 2 };
@@ -93,6 +94,7 @@ struct Params {
     const float *u_next;    // sampling: [M] uniforms of the emitted sample
     int32_t *ids;           // layer: [M][8]; stack/verify: [L][M][8] trace; optional
     float *wts;             // layer: [M][8]; optional
+    DenseArgs dense;        // layer mode with NS = 3: the always-on dense MLP (its 3 parts)
     Ws ws;
     long long timeout_ns;
     long long *trace;       // optional: %globaltimer stamps (see kTracePoints)
@@ -116,15 +118,15 @@ struct __align__(128) Smem {
     float best_v[kMW][8];       // lm_head winners per reducing warp and token
     int32_t best_i[kMW][8];
     float samp_s[kMW][8];       // sampling: sum of exp((z - best_v) / T) per reducing warp and token
-    float comb[2][kMaxSlots][8];
-    int32_t experts[2][kMaxSlots];
+    float comb[2][kMaxSlotsAll][8];
+    int32_t experts[2][kMaxSlotsAll];
     int32_t n_unique[2];
     int32_t tk_ids[8][8];
     float tk_w[8][8];
     int32_t mark[kE];
     int32_t slot_of[kE];
-    float sc_g[kMaxGuRows + 8]; // gate/up row scales of this CTA's routed rows, then (from
-    float sc_u[kMaxGuRows + 8]; // kMaxGuRows) its shared-expert rows
+    float sc_g[kMaxGuRows + 8 * kMaxShTiles];   // gate/up row scales of this CTA's routed rows, then
+    float sc_u[kMaxGuRows + 8 * kMaxShTiles];   // (from kMaxGuRows) its always-on rows
     float sc_d[kMaxDownRows];   // down row scales of this CTA's down rows of the layer
     unsigned long long full[kStages];
     unsigned long long empty[kStages];
@@ -380,16 +382,17 @@ __device__ __forceinline__ Range split(long long total, int part, int parts)
 // not wait for the slowest CTA's last tiles.
 constexpr int kGuTiles = kF / 8;   // 88 tiles per expert
 
-__device__ __forceinline__ int gu_tile_count(int U, int cta, int G)
+// S = slots of the layer: U routed experts + the always-on parts.
+__device__ __forceinline__ int gu_tile_count(int S, int cta, int G)
 {
-    const int total = (U + 1) * kGuTiles;
+    const int total = S * kGuTiles;
     return cta < total ? (total - 1 - cta) / G + 1 : 0;
 }
 
 // Gate/up tiles of the CTAs before `cta` (the first total % G CTAs take one more).
-__device__ __forceinline__ unsigned gu_tiles_before(int U, int cta, int G)
+__device__ __forceinline__ unsigned gu_tiles_before(int S, int cta, int G)
 {
-    const unsigned total = static_cast<unsigned>(U + 1) * kGuTiles;
+    const unsigned total = static_cast<unsigned>(S) * kGuTiles;
     return static_cast<unsigned>(cta) * (total / G) + min(static_cast<unsigned>(cta), total % G);
 }
 
@@ -398,23 +401,23 @@ __device__ __forceinline__ unsigned gu_tiles_before(int U, int cta, int G)
 // down tiles (16 rows of 704 bytes; measured stage times are about 1 : 0.3),
 // and a CTA with one more gate/up tile than another gets 3 fewer down tiles.
 // Cumulative over CTAs: 16 (units(c) - 3 * gate/up tiles before c).
-__device__ __forceinline__ Range down_rows(int U, int cta, int G)
+__device__ __forceinline__ Range down_rows(int S, int cta, int G)
 {
-    // 32-bit arithmetic: (U + 1) * 440 * G < 2^32 for U < 65, G <= 152 * 1000
+    // 32-bit arithmetic: S * 440 * G < 2^32 for S <= 67, G <= 152 * 1000
     constexpr unsigned kW = 3;
-    const unsigned units = static_cast<unsigned>(U + 1) * (kW * kGuTiles + kH / 16);
+    const unsigned units = static_cast<unsigned>(S) * (kW * kGuTiles + kH / 16);
     const unsigned c0 = cta, c1 = cta + 1;
-    const int b = static_cast<int>(units * c0 / G - kW * gu_tiles_before(U, cta, G));
-    const int e = static_cast<int>(units * c1 / G - kW * gu_tiles_before(U, cta + 1, G));
+    const int b = static_cast<int>(units * c0 / G - kW * gu_tiles_before(S, cta, G));
+    const int e = static_cast<int>(units * c1 / G - kW * gu_tiles_before(S, cta + 1, G));
     return Range{16 * b, 16 * e};
 }
 
 struct DownStages {
     int begin, end;   // CTA range in the flattened (slot, row) space
     int k0, n, rot;   // first 64-row block, number of blocks, rotation
-    __device__ DownStages(int U, int cta, int G)
+    __device__ DownStages(int S, int cta, int G)
     {
-        const Range r = down_rows(U, cta, G);
+        const Range r = down_rows(S, cta, G);
         begin = r.begin;
         end = r.end;
         constexpr int kBlk = kDownTiles * 16;   // 64 rows
@@ -653,14 +656,14 @@ __device__ __forceinline__ float4 red_sum4(const Smem &s, int b, int t, int ln)
 // Writes the pending marker into an activation buffer (tokens < M): every
 // slot if n_used == 0, else the first n_used slots and the shared one. Thread
 // `first` of `stride` cooperating threads; out of line (cold code).
-__device__ __noinline__ void mark_act_pending(float *base, int n_used, int M, int first, int stride)
+__device__ __noinline__ void mark_act_pending(float *base, int n_used, int ns, int M, int first, int stride)
 {
     const float4 pend4 = make_float4(__uint_as_float(kActPending), __uint_as_float(kActPending),
                                      __uint_as_float(kActPending), __uint_as_float(kActPending));
-    const int rows = (n_used == 0 ? kMaxSlots : n_used + 1) * M;
+    const int rows = (n_used == 0 ? kMaxSlotsAll : n_used + ns) * M;
     for (int i = first; i < rows * (kF / 4); i += stride) {
         const int r = i / (kF / 4), c4 = i % (kF / 4);
-        const int slot = n_used == 0 ? r / M : (r / M < n_used ? r / M : kSharedSlot);
+        const int slot = n_used == 0 ? r / M : (r / M < n_used ? r / M : kSharedSlot + r / M - n_used);
         __stcg(reinterpret_cast<float4 *>(base + ((size_t)slot * kMaxM + r % M) * kF) + c4, pend4);
     }
 }
@@ -948,10 +951,44 @@ __device__ __noinline__ void sample_finish(const float *z, int64_t V, int M, int
     }
 }
 
+// Always-on part pp of a layer (its slot kSharedSlot + pp): with NS = 1 the
+// layer's shared expert (expert kShared), with NS = 3 part pp of the dense
+// MLP in Params::dense (gate/up rows pp * 704 .., down columns pp * 704 .. of
+// its 2112-wide rows, the down rows' full-width scales).
+template <int NS>
+struct Parts {
+    __device__ static const uint8_t *gate(const fgm_layer &L, const DenseArgs &d, int pp)
+    {
+        return NS > 1 ? d.gq + (size_t)pp * kF * kH : L.gate_q + (size_t)kShared * kF * kH;
+    }
+    __device__ static const uint8_t *up(const fgm_layer &L, const DenseArgs &d, int pp)
+    {
+        return NS > 1 ? d.uq + (size_t)pp * kF * kH : L.up_q + (size_t)kShared * kF * kH;
+    }
+    __device__ static const float *gate_s(const fgm_layer &L, const DenseArgs &d, int pp)
+    {
+        return NS > 1 ? d.gs + (size_t)pp * kF : L.gate_s + (size_t)kShared * kF;
+    }
+    __device__ static const float *up_s(const fgm_layer &L, const DenseArgs &d, int pp)
+    {
+        return NS > 1 ? d.us + (size_t)pp * kF : L.up_s + (size_t)kShared * kF;
+    }
+    // row j of the part's down matrix (kF bytes) and the row stride
+    __device__ static const uint8_t *down_row(const fgm_layer &L, const DenseArgs &d, int pp, int j)
+    {
+        return NS > 1 ? d.dq + (size_t)j * (NS * kF) + (size_t)pp * kF : L.down_q + ((size_t)kShared * kH + j) * kF;
+    }
+    __device__ static const float *down_s(const fgm_layer &L, const DenseArgs &d, int pp)
+    {
+        return NS > 1 ? d.ds : L.down_s + (size_t)kShared * kH;
+    }
+};
+
 // NB: packed column blocks (2: M <= 5, 3: M <= 8). TRACE: the phase-trace
 // profiling aid is compiled in (a separate instantiation, so that the
-// production kernels carry none of its code).
-template <int NB, bool TRACE>
+// production kernels carry none of its code). NS: always-on parts per layer
+// (1: the shared expert; 3: a 2112-wide dense MLP, layer mode).
+template <int NB, bool TRACE, int NS = 1>
 __global__ void __launch_bounds__(kThreads, 1) k_fused(const __grid_constant__ Params p)
 {
     extern __shared__ __align__(128) uint8_t smem_raw[];
@@ -999,12 +1036,13 @@ __global__ void __launch_bounds__(kThreads, 1) k_fused(const __grid_constant__ P
                     pdetail[((size_t)p_layer * kTraceStages + (stage - p_stage0)) * kTraceDetail] = clock64();
                 return s.ring[slot];
             };
-            auto gu_rows = [&](const fgm_layer &L, int e, int i, int nv) {
+            // rows i .. i + nv - 1 of one gate/up pair of matrices ([704][2816] each)
+            auto gu_rows = [&](const uint8_t *gbase, const uint8_t *ubase, int i, int nv) {
                 uint8_t *dst = claim(2u * nv * kH);
                 if (!dst)
                     return;
-                const uint8_t *gsrc = L.gate_q + ((size_t)e * kF + i) * kH;
-                const uint8_t *usrc = L.up_q + ((size_t)e * kF + i) * kH;
+                const uint8_t *gsrc = gbase + (size_t)i * kH;
+                const uint8_t *usrc = ubase + (size_t)i * kH;
                 for (int rr = 0; rr < nv; ++rr) {
                     bulk_g2s(dst + rr * kRowStride, gsrc + (size_t)rr * kH, kH, &s.full[stage % kStages]);
                     bulk_g2s(dst + (8 + rr) * kRowStride, usrc + (size_t)rr * kH, kH, &s.full[stage % kStages]);
@@ -1035,8 +1073,14 @@ __global__ void __launch_bounds__(kThreads, 1) k_fused(const __grid_constant__ P
                     if (l + 1 < n_layers)
                         prefetch_l2(p.layers[l + 1].router_w + (size_t)e0 * kH, kRowsBytes);
                 }
-                if (cta < kGuTiles)
-                    gu_rows(L, kShared, 8 * cta, 8);
+                // the always-on tiles (list indices below NS * kGuTiles) before the
+                // routing is known, then the routed ones
+                int k = 0;
+                for (; cta + k * G < NS * kGuTiles && ok; ++k) {
+                    const int x = cta + k * G;
+                    gu_rows(Parts<NS>::gate(L, p.dense, x / kGuTiles), Parts<NS>::up(L, p.dense, x / kGuTiles),
+                            8 * (x % kGuTiles), 8);
+                }
                 if (!ok)
                     break;
                 ok = mbar_wait(&s.route, l & 1, s, deadline, status, 2, l);
@@ -1044,27 +1088,36 @@ __global__ void __launch_bounds__(kThreads, 1) k_fused(const __grid_constant__ P
                     break;
                 const int pb = l & 1;
                 const int U = s.n_unique[pb];
-                const int n_gu = gu_tile_count(U, cta, G);
-                for (int k = cta < kGuTiles ? 1 : 0; k < n_gu && ok; ++k) {
-                    const int x = cta + k * G - kGuTiles;
-                    gu_rows(L, s.experts[pb][x / kGuTiles], 8 * (x % kGuTiles), 8);
+                const int n_gu = gu_tile_count(U + NS, cta, G);
+                for (; k < n_gu && ok; ++k) {
+                    const int x = cta + k * G - NS * kGuTiles;
+                    const size_t e = s.experts[pb][x / kGuTiles];
+                    gu_rows(L.gate_q + e * kF * kH, L.up_q + e * kF * kH, 8 * (x % kGuTiles), 8);
                 }
-                const DownStages dsp(U, cta, G);
+                const DownStages dsp(U + NS, cta, G);
                 for (int di = 0; di < dsp.n && ok; ++di) {
                     int pos, nv;
                     dsp.get(di, pos, nv);
                     const int slot = pos / kH, row = pos % kH;
                     {
-                        const int e = slot < U ? s.experts[pb][slot] : kShared;
                         uint8_t *dst = claim(static_cast<uint32_t>(nv) * kF);
                         if (!dst)
                             break;
-                        // 4-row (2816-byte) pieces: many mid-sized copies keep more
-                        // requests in flight than one 45 KB copy
-                        const uint8_t *src = L.down_q + ((size_t)e * kH + row) * kF;
-                        for (int r4 = 0; r4 < nv; r4 += 4)
-                            bulk_g2s(dst + r4 * kF, src + (size_t)r4 * kF,
-                                     static_cast<uint32_t>(min(4, nv - r4)) * kF, &s.full[stage % kStages]);
+                        if (NS == 1 || slot < U) {
+                            // 4-row (2816-byte) pieces: many mid-sized copies keep more
+                            // requests in flight than one 45 KB copy
+                            const uint8_t *src =
+                                slot < U ? L.down_q + ((size_t)s.experts[pb][slot] * kH + row) * kF
+                                         : Parts<NS>::down_row(L, p.dense, 0, row);
+                            for (int r4 = 0; r4 < nv; r4 += 4)
+                                bulk_g2s(dst + r4 * kF, src + (size_t)r4 * kF,
+                                         static_cast<uint32_t>(min(4, nv - r4)) * kF, &s.full[stage % kStages]);
+                        } else {
+                            // a dense part's rows are kF-byte pieces of wider rows
+                            for (int rr = 0; rr < nv; ++rr)
+                                bulk_g2s(dst + rr * kF, Parts<NS>::down_row(L, p.dense, slot - U, row + rr), kF,
+                                         &s.full[stage % kStages]);
+                        }
                         ++stage;
                     }
                 }
@@ -1164,7 +1217,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_fused(const __grid_constant__ P
     // previous contents is left and that its next writers come after a grid
     // barrier.
     auto mark_pending = [&](int buf, int n_used) {
-        mark_act_pending(ws.act + (size_t)buf * kMaxSlots * kMaxM * kF, n_used, M, cta * kConsumers + tid,
+        mark_act_pending(ws.act + (size_t)buf * kMaxSlotsAll * kMaxM * kF, n_used, NS, M, cta * kConsumers + tid,
                          G * kConsumers);
     };
     // lm_head: lanes 0..3 keep the running best of tokens 2 lane, 2 lane + 1
@@ -1323,7 +1376,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_fused(const __grid_constant__ P
         };
         cur_layer = l;
         cur_pb = pb;
-        act_cur = ws.act + (size_t)(l & 1) * kMaxSlots * kMaxM * kF;
+        act_cur = ws.act + (size_t)(l & 1) * kMaxSlotsAll * kMaxM * kF;
         layer_stage0 = stage;
         if (detail && tid == 0)
             detail[((size_t)l * kTraceStages) * kTraceDetail + 7] = clock64();
@@ -1333,8 +1386,8 @@ __global__ void __launch_bounds__(kThreads, 1) k_fused(const __grid_constant__ P
         if (l == 0 && p.debug_stall)
             grid_barrier();
         // -------------------------------------------------------- phase A
-        const int n_sh = cta < kGuTiles ? 1 : 0;
-        const Range rsh = n_sh ? Range{8 * cta, 8 * cta + 8} : Range{kF, kF};
+        // this CTA's always-on tiles: list indices cta, cta + G, ... below NS * kGuTiles
+        const int n_sh = cta < NS * kGuTiles ? (NS * kGuTiles - 1 - cta) / G + 1 : 0;
         {
             const bool from_x = (p.mode == kModeLayer) || l == 0;
             const bool norm = p.mode != kModeLayer;
@@ -1386,9 +1439,10 @@ __global__ void __launch_bounds__(kThreads, 1) k_fused(const __grid_constant__ P
             // scales of this CTA's shared-expert gate/up rows, copied asynchronously;
             // each thread waits for its copies before the first gate/up tile, and
             // the exchange barrier that follows makes them visible to the reducers
-            for (int i = tid; i < rsh.end - rsh.begin; i += kConsumers) {
-                cp_async4(&s.sc_g[kMaxGuRows + i], L.gate_s + (size_t)kShared * kF + rsh.begin + i);
-                cp_async4(&s.sc_u[kMaxGuRows + i], L.up_s + (size_t)kShared * kF + rsh.begin + i);
+            for (int i = tid; i < 8 * n_sh; i += kConsumers) {
+                const int x = cta + (i >> 3) * G, pp = x / kGuTiles, row = 8 * (x % kGuTiles) + (i & 7);
+                cp_async4(&s.sc_g[kMaxGuRows + i], Parts<NS>::gate_s(L, p.dense, pp) + row);
+                cp_async4(&s.sc_u[kMaxGuRows + i], Parts<NS>::up_s(L, p.dense, pp) + row);
             }
             cp_async_commit();
             if (l == 0) {
@@ -1676,7 +1730,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_fused(const __grid_constant__ P
                 if (lane == 0)
                     s.n_unique[pb] = base;
             }
-            for (int i = tid; i < kMaxSlots * 8; i += kConsumers)
+            for (int i = tid; i < kMaxSlotsAll * 8; i += kConsumers)
                 s.comb[pb][i >> 3][i & 7] = 0.0f;
             consumer_sync();
             stamp(11);
@@ -1695,24 +1749,25 @@ __global__ void __launch_bounds__(kThreads, 1) k_fused(const __grid_constant__ P
                 mbar_arrive(&s.route);
             stamp(6);
             const int U = s.n_unique[pb];
-            const int n_gu = gu_tile_count(U, cta, G);
+            const int n_gu = gu_tile_count(U + NS, cta, G);
             // row scales of this CTA's routed gate/up rows and of its down rows,
             // copied asynchronously (cp.async); each thread waits for its copies
             // before the first routed tile, and the next exchange barrier makes
             // them visible to the reducers
             for (int k = tid; k < 8 * (n_gu - n_sh); k += kConsumers) {
-                const int x = cta + (n_sh + k / 8) * G - kGuTiles;
+                const int x = cta + (n_sh + k / 8) * G - NS * kGuTiles;
                 const size_t row = (size_t)s.experts[pb][x / kGuTiles] * kF + 8 * (x % kGuTiles) + k % 8;
                 cp_async4(&s.sc_g[k], L.gate_s + row);
                 cp_async4(&s.sc_u[k], L.up_s + row);
             }
             {
-                const Range rd = down_rows(U, cta, G);
+                const Range rd = down_rows(U + NS, cta, G);
                 for (int k = tid; k < rd.end - rd.begin; k += kConsumers) {
                     const int pos = rd.begin + k;
                     const int si = pos / kH;
-                    const int e = si < U ? s.experts[pb][si] : kShared;
-                    cp_async4(&s.sc_d[k], L.down_s + (size_t)e * kH + pos % kH);
+                    const float *ds = si < U ? L.down_s + (size_t)s.experts[pb][si] * kH
+                                             : Parts<NS>::down_s(L, p.dense, si - U);
+                    cp_async4(&s.sc_d[k], ds + pos % kH);
                 }
             }
             cp_async_commit();
@@ -1737,12 +1792,13 @@ __global__ void __launch_bounds__(kThreads, 1) k_fused(const __grid_constant__ P
                 if (it >= n_gu)
                     break;
                 if (it < n_sh) {
-                    i = rsh.begin;
+                    const int x = cta + it * G;
+                    i = 8 * (x % kGuTiles);
                     nv = 8;
-                    aslot = kSharedSlot;
-                    k0 = kMaxGuRows;
+                    aslot = kSharedSlot + x / kGuTiles;
+                    k0 = kMaxGuRows + 8 * it;
                 } else {
-                    const int x = cta + it * G - kGuTiles;
+                    const int x = cta + it * G - NS * kGuTiles;
                     const int u = x / kGuTiles;
                     i = 8 * (x % kGuTiles);
                     nv = 8;
@@ -1776,7 +1832,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_fused(const __grid_constant__ P
         // -------------------------------------------------------- phase C
         {
             const int U = s.n_unique[pb];
-            const DownStages ds(U, cta, G);
+            const DownStages ds(U + NS, cta, G);
             // A CTA's rows span at most two slots (it owns fewer than 2816 rows):
             // their activation terms (this warp's 64-wide K-slice, token g) are
             // prepared once, up front.
@@ -1785,9 +1841,9 @@ __global__ void __launch_bounds__(kThreads, 1) k_fused(const __grid_constant__ P
 #pragma unroll
             for (int h2 = 0; h2 < 2; ++h2) {
                 const int si = si0 + h2;
-                const bool slot_ok = si <= U && (h2 == 0 || ds.end > (si0 + 1) * kH);   // same for the whole CTA
+                const bool slot_ok = si < U + NS && (h2 == 0 || ds.end > (si0 + 1) * kH);   // same for the whole CTA
                 if (slot_ok) {
-                    const int aslot = si < U ? si : kSharedSlot;
+                    const int aslot = si < U ? si : kSharedSlot + si - U;
                     dc[h2] = down_columns<NB>(act_cur + (size_t)aslot * kMaxM * kF, M, warp, lane, &s.abort, deadline,
                                               status, aslot);
                 } else {

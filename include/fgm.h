@@ -168,8 +168,10 @@ int fgm_moe_layer_fwd_noalloc(const fgm_layer *layer, const uint16_t *x, uint16_
  * outputs add up (each down row keeps its full-width scale), so the kernels
  * run it as W/704 always-on parts of weight 1 next to the routed experts.
  * Source: "llm-decoding" §"Where the 7.36 GB goes" (an always-on dense MLP of
- * 2816 x 2112 per layer). Runs on the per-stage kernels whatever
- * fgm_select_path chose.
+ * 2816 x 2112 per layer). On the fused paths a 2112-wide MLP runs in the
+ * persistent kernel, its three parts taking the shared expert's place in the
+ * always-on schedule; other widths, and the staged path, use the per-stage
+ * kernels.
  *  dense   HOST pointer to the MLP's device weights (see fgm_mlp)
  *  other arguments as fgm_moe_layer_fwd */
 int fgm_moe_layer_dense_fwd(const fgm_layer *layer, const fgm_mlp *dense, const uint16_t *x, uint16_t *y, int M,

@@ -5,7 +5,7 @@ benchmark layer (seed 0, Zipf bias) and a 2112-wide E4M3 MLP with fp32 row
 scales in its natural layout (down rows 2112 wide). Same rules as the layer
 test: router ids bit-exact where the oracle's margin exceeds 1e-2 (else a
 valid choice), rows within 1e-2 and elementwise within 2e-2 of the
-bf16-rounded oracle."""
+bf16-rounded oracle. Both the persistent kernel and the per-stage kernels."""
 
 import numpy as np
 import pytest
@@ -19,11 +19,15 @@ from helpers import (ELEM_TOL, MARGIN, REL_TOL, bf16_values, elementwise_rel_err
 pytestmark = pytest.mark.gpu
 
 
-@pytest.fixture(scope="module")
-def fgm():
+@pytest.fixture(scope="module", params=[0, 1], ids=["fused", "staged"])
+def fgm(request):
+    """fused: the persistent kernel with the MLP's three parts as its always-on
+    slots; staged: the per-stage kernels."""
     import fine_grained_moe_gb300 as m
     m.lib()
-    return m
+    prev = m.select_path(request.param)
+    yield m
+    m.select_path(prev)
 
 
 @pytest.fixture(scope="module")
