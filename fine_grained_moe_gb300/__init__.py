@@ -139,7 +139,7 @@ def _check_topk(M: int, x: torch.Tensor, topk_ids: torch.Tensor | None, topk_w: 
 
 
 def select_path(path: int) -> int:
-    """Selects the execution path (PATH_FUSED or PATH_STAGED); returns the previous one."""
+    """Selects the execution path (PATH_FUSED, PATH_STAGED or PATH_FUSED_TC); returns the previous one."""
     return int(lib().fgm_select_path(int(path)))
 
 

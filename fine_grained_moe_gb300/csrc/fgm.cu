@@ -53,6 +53,8 @@ struct DeviceInfo {
 
 int g_path = FGM_PATH_FUSED;
 long long g_timeout_ns = 2000000000LL;
+// the persistent kernel's shared memory: its block plus slack to align it to 1024 bytes
+constexpr size_t kFusedSmemBytes = sizeof(fused::Smem) + 1024;
 long long *g_trace = nullptr;
 int g_debug_stall = 0;
 size_t g_trace_n = 0;
@@ -96,17 +98,19 @@ int device_ready(int *sms)
             FGM_SMEM(fp8tc::k_lmhead_fp8_tc<false>, fp8tc::kSmemBytes);
             FGM_SMEM(fp8tc::k_lmhead_fp8_tc<true>, fp8tc::kSmemBytes);
 #undef FGM_SMEM
-            const void *kerns[6] = {reinterpret_cast<const void *>(fused::k_fused<2, false>),
+            const void *kerns[8] = {reinterpret_cast<const void *>(fused::k_fused<2, false>),
                                     reinterpret_cast<const void *>(fused::k_fused<3, false>),
                                     reinterpret_cast<const void *>(fused::k_fused<2, true>),
                                     reinterpret_cast<const void *>(fused::k_fused<3, true>),
                                     reinterpret_cast<const void *>(fused::k_fused<2, false, 3>),
-                                    reinterpret_cast<const void *>(fused::k_fused<3, false, 3>)};
+                                    reinterpret_cast<const void *>(fused::k_fused<3, false, 3>),
+                                    reinterpret_cast<const void *>(fused::k_fused<2, false, 1, true>),
+                                    reinterpret_cast<const void *>(fused::k_fused<2, true, 1, true>)};
             int per_sm = 1 << 30;
             for (const void *k : kerns) {
-                FGM_CUDA(cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)sizeof(fused::Smem)));
+                FGM_CUDA(cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kFusedSmemBytes));
                 int n = 0;
-                FGM_CUDA(cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, k, fused::kThreads, sizeof(fused::Smem)));
+                FGM_CUDA(cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, k, fused::kThreads, kFusedSmemBytes));
                 per_sm = n < per_sm ? n : per_sm;
             }
             d.fused_grid = (per_sm >= 1 && d.sms >= fused::kMinCtas) ? d.sms : 0;
@@ -131,11 +135,23 @@ int fused_grid()
 }
 
 // Launches the persistent kernel (cooperative: all CTAs co-resident).
+int tc_down_maps(const uint8_t *down_q, CUtensorMap *m128, CUtensorMap *m16);
+
 int launch_fused(fused::Params &prm, cudaStream_t st)
 {
     const int G = fused_grid();
     if (G < 0)
         return G;
+    // the tensor-memory path runs the down phase on tcgen05 (M <= 5, one shared expert)
+    const bool tcd = g_path == FGM_PATH_FUSED_TC && prm.M <= 5 && prm.dense.parts == 0 && prm.mode != fused::kModeLmHead;
+    if (tcd) {
+        const int n_l = prm.mode == fused::kModeLayer ? 1 : prm.n_layers;
+        for (int l = 0; l < n_l; ++l) {
+            const int rc = tc_down_maps(prm.layers[l].down_q, &prm.dmap[l], &prm.dmap16[l]);
+            if (rc != FGM_OK)
+                return rc;
+        }
+    }
     prm.timeout_ns = g_timeout_ns;
     const int n_l = prm.mode == fused::kModeLayer ? 1 : prm.mode == fused::kModeLmHead ? 0 : prm.n_layers;
     const size_t need = (size_t)(n_l * fused::kTracePoints + 2) * G + (size_t)n_l * fused::kTraceStages * fused::kTraceDetail;
@@ -148,6 +164,8 @@ int launch_fused(fused::Params &prm, cudaStream_t st)
     const void *kern = prm.dense.parts == 3
                            ? (prm.M <= 5 ? reinterpret_cast<const void *>(fused::k_fused<2, false, 3>)
                                          : reinterpret_cast<const void *>(fused::k_fused<3, false, 3>))
+                       : tcd ? (traced ? reinterpret_cast<const void *>(fused::k_fused<2, true, 1, true>)
+                                       : reinterpret_cast<const void *>(fused::k_fused<2, false, 1, true>))
                        : prm.M <= 5 ? (traced ? reinterpret_cast<const void *>(fused::k_fused<2, true>)
                                               : reinterpret_cast<const void *>(fused::k_fused<2, false>))
                                     : (traced ? reinterpret_cast<const void *>(fused::k_fused<3, true>)
@@ -155,7 +173,7 @@ int launch_fused(fused::Params &prm, cudaStream_t st)
     if (!traced)
         prm.trace = nullptr;
     FGM_CUDA(cudaLaunchCooperativeKernel(kern, dim3(G),
-                                         dim3(fused::kThreads), args, sizeof(fused::Smem), st));
+                                         dim3(fused::kThreads), args, kFusedSmemBytes, st));
     return FGM_OK;
 }
 
@@ -370,6 +388,47 @@ int run_lmhead_fp8_tc(const uint8_t *emb_q, const float *emb_s, int64_t V, const
     else
         fp8tc::k_lmhead_fp8_tc<false><<<G, fp8tc::kThreads, fp8tc::kSmemBytes, st>>>(tmap, a);
     FGM_CHECK_LAUNCH();
+    return FGM_OK;
+}
+
+// Tensor maps of one layer's down matrices ([129 * 2816 rows][704 bytes]):
+// 128 x 128-byte and 16 x 128-byte boxes in the 128-byte swizzle, zeros past
+// the 704 bytes of a row. Encoded once per weight address and kept.
+int tc_down_maps(const uint8_t *down_q, CUtensorMap *m128, CUtensorMap *m16)
+{
+    struct Entry {
+        const void *ptr;
+        CUtensorMap a, b;
+    };
+    static Entry cache[2 * FGM_MAX_LAYERS];
+    static int n = 0, next = 0;
+    static std::mutex mu;
+    std::lock_guard<std::mutex> lock(mu);
+    for (int i = 0; i < n; ++i)
+        if (cache[i].ptr == down_q) {
+            *m128 = cache[i].a;
+            *m16 = cache[i].b;
+            return FGM_OK;
+        }
+    EncodeTiledFn encode = nullptr;
+    FGM_TRY(encode_tiled_fn(&encode));
+    Entry e;
+    e.ptr = down_q;
+    const cuuint64_t dims[2] = {static_cast<cuuint64_t>(kF), static_cast<cuuint64_t>(kNE) * kH};
+    const cuuint64_t strides[1] = {static_cast<cuuint64_t>(kF)};
+    const cuuint32_t estr[2] = {1, 1};
+    for (int m = 0; m < 2; ++m) {
+        const cuuint32_t box[2] = {128, m == 0 ? 128u : 16u};
+        const CUresult r = encode(m == 0 ? &e.a : &e.b, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<uint8_t *>(down_q),
+                                  dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                                  CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+        if (r != CUDA_SUCCESS)
+            return fail(FGM_ERR_CUDA, "cuTensorMapEncodeTiled (down matrix) failed (%d)", static_cast<int>(r));
+    }
+    const int slot = n < 2 * FGM_MAX_LAYERS ? n++ : (next++ % (2 * FGM_MAX_LAYERS));
+    cache[slot] = e;
+    *m128 = e.a;
+    *m16 = e.b;
     return FGM_OK;
 }
 

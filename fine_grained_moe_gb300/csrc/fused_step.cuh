@@ -43,6 +43,8 @@
 // winners and applies the greedy accept rule (no waiting involved).
 #pragma once
 
+#include <cuda.h>
+
 #include "common.cuh"
 
 namespace fgm {
@@ -95,6 +97,10 @@ struct Params {
     int32_t *ids;           // layer: [M][8]; stack/verify: [L][M][8] trace; optional
     float *wts;             // layer: [M][8]; optional
     DenseArgs dense;        // layer mode with NS = 3: the always-on dense MLP (its 3 parts)
+    // tensor-memory down phase: each layer's down_q as [129 * 2816 rows][704 bytes],
+    // 128-byte boxes in the 128-byte swizzle, 128 rows (dmap) and 16 rows (dmap16)
+    CUtensorMap dmap[FGM_MAX_LAYERS];
+    CUtensorMap dmap16[FGM_MAX_LAYERS];
     Ws ws;
     long long timeout_ns;
     long long *trace;       // optional: %globaltimer stamps (see kTracePoints)
@@ -131,6 +137,10 @@ struct __align__(128) Smem {
     unsigned long long full[kStages];
     unsigned long long empty[kStages];
     unsigned long long route;
+    unsigned long long tfull[2], tempty[2];   // tensor-memory down phase: accumulators full / read
+    unsigned long long mdone[kStages];        // tensor-memory down phase: products of a ring slot done
+    uint32_t tmem_base;
+    float dscale[2][8];         // tensor-memory down phase: activation-term scale per (slot, token)
     int abort;
     int last;
 };
@@ -237,6 +247,92 @@ __device__ __forceinline__ void bulk_g2s(void *dst, const void *src, uint32_t by
         : "memory");
 }
 
+// ---------------------------------------------------------------- tcgen05
+// The tensor-memory down phase (TCD): weights by TMA tensor copies into the
+// ring, activations as E4M3 terms in shared memory, full-K accumulators in
+// tensor memory, products by tcgen05.mma issued from one thread.
+constexpr int kTcRows = 128;                 // rows per down tile (the MMA's M)
+constexpr int kTcN = 16;                     // MMA N: 5 tokens x 3 terms (+ 1 zero column)
+constexpr int kTcStagesPerTile = 3;          // K 0..255, 256..511, 512..767 (zeros past 704)
+constexpr int kTcBoxBytes = kTcRows * 128;   // one 128-row x 128-byte box
+constexpr int kTcBBytes = (kF / 16) * 256;   // B operand of one slot: 44 K-columns x 16 rows x 16 bytes
+constexpr uint32_t kTcTmemCols = 32;         // two 16-column accumulators
+// instruction descriptor, kind::f8f6f4: D fp32, A and B E4M3, both K-major, N >> 3, M >> 4
+constexpr uint32_t kTcIdesc = (1u << 4) | (static_cast<uint32_t>(kTcN >> 3) << 17) |
+                              (static_cast<uint32_t>(kTcRows >> 4) << 24);
+
+// A operand: K-major, 128-byte swizzle (8-row x 128-byte atoms 1024 bytes apart).
+__device__ __forceinline__ uint64_t tc_desc_sw128(uint32_t addr)
+{
+    return static_cast<uint64_t>((addr >> 4) & 0x3FFFu) | (1ull << 16) | (64ull << 32) | (1ull << 46) | (2ull << 61);
+}
+
+// B operand: K-major, no swizzle: core matrices of 8 rows x 16 bytes, 256 bytes
+// apart along K (leading byte offset) and 128 bytes apart along N (stride byte offset).
+__device__ __forceinline__ uint64_t tc_desc_nosw(uint32_t addr)
+{
+    return static_cast<uint64_t>((addr >> 4) & 0x3FFFu) | (16ull << 16) | (8ull << 32) | (1ull << 46);
+}
+
+// Byte offset of (column n, k) in a B operand (see tc_desc_nosw).
+__device__ __forceinline__ int tc_b_offset(int n, int k) { return (k >> 4) * 256 + (n >> 3) * 128 + (n & 7) * 16 + (k & 15); }
+
+__device__ __forceinline__ void tc_mma(uint32_t d, uint64_t a, uint64_t b, uint32_t accumulate)
+{
+    asm volatile(
+        "{\n\t.reg .pred p;\n\tsetp.ne.u32 p, %4, 0;\n\t"
+        "tcgen05.mma.cta_group::1.kind::f8f6f4 [%0], %1, %2, %3, p;\n\t}" ::"r"(d),
+        "l"(a), "l"(b), "r"(kTcIdesc), "r"(accumulate)
+        : "memory");
+}
+
+__device__ __forceinline__ void tc_commit(unsigned long long *bar)
+{
+    asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(su32(bar))
+                 : "memory");
+}
+
+__device__ __forceinline__ void tc_fence_after() { asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory"); }
+__device__ __forceinline__ void tc_fence_before() { asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory"); }
+
+// 16 consecutive fp32 columns of this thread's lane
+__device__ __forceinline__ void tc_ld16(uint32_t taddr, float (&v)[16])
+{
+    uint32_t r[16];
+    asm volatile(
+        "tcgen05.ld.sync.aligned.32x32b.x16.b32 {%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, "
+        "%15}, [%16];"
+        : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]), "=r"(r[8]),
+          "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15])
+        : "r"(taddr)
+        : "memory");
+    asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+#pragma unroll
+    for (int i = 0; i < 16; ++i)
+        v[i] = __uint_as_float(r[i]);
+}
+
+__device__ __forceinline__ void tma_2d(uint32_t dst, const CUtensorMap *map, int x, int y, unsigned long long *bar)
+{
+    asm volatile(
+        "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3}], [%4];" ::"r"(
+            dst),
+        "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(su32(bar))
+        : "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive_n(unsigned long long *b, uint32_t n)
+{
+    asm volatile("mbarrier.arrive.shared.b64 _, [%0], %1;" ::"r"(su32(b)), "r"(n) : "memory");
+}
+
+// A down tile of the tensor-memory phase: rows [pos, pos + nr) of the CTA's
+// flattened (slot, row) range, within one slot and at most 128 rows.
+__device__ __forceinline__ int tc_tile_rows(int pos, int end)
+{
+    return min(min(end, (pos / kH + 1) * kH), pos + kTcRows) - pos;
+}
+
 // Named barrier of the MMA warps (the producer never joins).
 __device__ __forceinline__ void consumer_sync() { asm volatile("bar.sync 1, %0;" ::"n"(kConsumers) : "memory"); }
 
@@ -252,6 +348,13 @@ __device__ __forceinline__ float4 ld_poll4(const float *p)
                  : "=f"(v.x), "=f"(v.y), "=f"(v.z), "=f"(v.w)
                  : "l"(p)
                  : "memory");
+    return v;
+}
+
+__device__ __forceinline__ float ld_poll1(const float *p)
+{
+    float v;
+    asm volatile("ld.relaxed.gpu.global.f32 %0, [%1];" : "=f"(v) : "l"(p) : "memory");
     return v;
 }
 
@@ -987,12 +1090,15 @@ struct Parts {
 // NB: packed column blocks (2: M <= 5, 3: M <= 8). TRACE: the phase-trace
 // profiling aid is compiled in (a separate instantiation, so that the
 // production kernels carry none of its code). NS: always-on parts per layer
-// (1: the shared expert; 3: a 2112-wide dense MLP, layer mode).
-template <int NB, bool TRACE, int NS = 1>
+// (1: the shared expert; 3: a 2112-wide dense MLP, layer mode). TCD: the down
+// phase on tcgen05 (NB = 2, NS = 1; tensor maps in Params::dmap).
+template <int NB, bool TRACE, int NS = 1, bool TCD = false>
 __global__ void __launch_bounds__(kThreads, 1) k_fused(const __grid_constant__ Params p)
 {
+    static_assert(!TCD || (NB == 2 && NS == 1), "the tensor-memory down phase covers M <= 5 with one shared expert");
+    // the shared-memory block starts 1024-byte aligned (swizzled TMA boxes in the ring)
     extern __shared__ __align__(128) uint8_t smem_raw[];
-    Smem &s = *reinterpret_cast<Smem *>(smem_raw);
+    Smem &s = *reinterpret_cast<Smem *>(smem_raw + ((1024u - (su32(smem_raw) & 1023u)) & 1023u));
     const int G = gridDim.x, cta = blockIdx.x;
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int g = lane >> 2, q = lane & 3;
@@ -1008,6 +1114,12 @@ __global__ void __launch_bounds__(kThreads, 1) k_fused(const __grid_constant__ P
             mbar_init(&s.empty[i], kMW);
         }
         mbar_init(&s.route, 1);
+        for (int i = 0; i < 2; ++i) {
+            mbar_init(&s.tfull[i], 1);
+            mbar_init(&s.tempty[i], 4);
+        }
+        for (int i = 0; i < kStages; ++i)
+            mbar_init(&s.mdone[i], 1);
         s.abort = 0;
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     }
@@ -1094,31 +1206,59 @@ __global__ void __launch_bounds__(kThreads, 1) k_fused(const __grid_constant__ P
                     const size_t e = s.experts[pb][x / kGuTiles];
                     gu_rows(L.gate_q + e * kF * kH, L.up_q + e * kF * kH, 8 * (x % kGuTiles), 8);
                 }
-                const DownStages dsp(U + NS, cta, G);
-                for (int di = 0; di < dsp.n && ok; ++di) {
-                    int pos, nv;
-                    dsp.get(di, pos, nv);
-                    const int slot = pos / kH, row = pos % kH;
-                    {
-                        uint8_t *dst = claim(static_cast<uint32_t>(nv) * kF);
-                        if (!dst)
-                            break;
-                        if (NS == 1 || slot < U) {
-                            // 4-row (2816-byte) pieces: many mid-sized copies keep more
-                            // requests in flight than one 45 KB copy
-                            const uint8_t *src =
-                                slot < U ? L.down_q + ((size_t)s.experts[pb][slot] * kH + row) * kF
-                                         : Parts<NS>::down_row(L, p.dense, 0, row);
-                            for (int r4 = 0; r4 < nv; r4 += 4)
-                                bulk_g2s(dst + r4 * kF, src + (size_t)r4 * kF,
-                                         static_cast<uint32_t>(min(4, nv - r4)) * kF, &s.full[stage % kStages]);
-                        } else {
-                            // a dense part's rows are kF-byte pieces of wider rows
-                            for (int rr = 0; rr < nv; ++rr)
-                                bulk_g2s(dst + rr * kF, Parts<NS>::down_row(L, p.dense, slot - U, row + rr), kF,
-                                         &s.full[stage % kStages]);
+                if constexpr (TCD) {
+                    // 128-row tiles within one slot, each in three K-stages of two
+                    // 128-byte boxes (K 640..767 reads zeros past 704); a ragged tile
+                    // in 16-row boxes
+                    const DownStages dsp(U + NS, cta, G);
+                    for (int pos = dsp.begin, nr = 0; pos < dsp.end && ok; pos += nr) {
+                        nr = tc_tile_rows(pos, dsp.end);
+                        const int si = pos / kH;
+                        const int y = (si < U ? s.experts[pb][si] : kShared) * kH + pos % kH;
+                        for (int ks = 0; ks < kTcStagesPerTile && ok; ++ks) {
+                            uint8_t *dst = claim(2u * static_cast<uint32_t>(nr) * 128u);
+                            if (!dst)
+                                break;
+                            const uint32_t d0 = su32(dst);
+                            for (int b = 0; b < 2; ++b) {
+                                const int x = 256 * ks + 128 * b;
+                                if (nr == kTcRows)
+                                    tma_2d(d0 + b * kTcBoxBytes, &p.dmap[l], x, y, &s.full[stage % kStages]);
+                                else
+                                    for (int r16 = 0; r16 < nr; r16 += 16)
+                                        tma_2d(d0 + b * kTcBoxBytes + r16 * 128, &p.dmap16[l], x, y + r16,
+                                               &s.full[stage % kStages]);
+                            }
+                            ++stage;
                         }
-                        ++stage;
+                    }
+                } else {
+                    const DownStages dsp(U + NS, cta, G);
+                    for (int di = 0; di < dsp.n && ok; ++di) {
+                        int pos, nv;
+                        dsp.get(di, pos, nv);
+                        const int slot = pos / kH, row = pos % kH;
+                        {
+                            uint8_t *dst = claim(static_cast<uint32_t>(nv) * kF);
+                            if (!dst)
+                                break;
+                            if (NS == 1 || slot < U) {
+                                // 4-row (2816-byte) pieces: many mid-sized copies keep more
+                                // requests in flight than one 45 KB copy
+                                const uint8_t *src =
+                                    slot < U ? L.down_q + ((size_t)s.experts[pb][slot] * kH + row) * kF
+                                             : Parts<NS>::down_row(L, p.dense, 0, row);
+                                for (int r4 = 0; r4 < nv; r4 += 4)
+                                    bulk_g2s(dst + r4 * kF, src + (size_t)r4 * kF,
+                                             static_cast<uint32_t>(min(4, nv - r4)) * kF, &s.full[stage % kStages]);
+                            } else {
+                                // a dense part's rows are kF-byte pieces of wider rows
+                                for (int rr = 0; rr < nv; ++rr)
+                                    bulk_g2s(dst + rr * kF, Parts<NS>::down_row(L, p.dense, slot - U, row + rr), kF,
+                                             &s.full[stage % kStages]);
+                            }
+                            ++stage;
+                        }
                     }
                 }
             }
@@ -1147,6 +1287,17 @@ __global__ void __launch_bounds__(kThreads, 1) k_fused(const __grid_constant__ P
     }
 
     // ============================================================ consumers
+    if constexpr (TCD) {
+        // tensor memory for the down phase's two accumulators (one CTA per SM)
+        if (warp == 0) {
+            asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(su32(&s.tmem_base)),
+                         "r"(kTcTmemCols)
+                         : "memory");
+            asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+        }
+    }
+    uint32_t tc_tiles = 0;    // tensor-memory down tiles finished by this CTA (barrier phases)
+    uint32_t mdone_phase = 0; // bit i: phase parity of s.mdone[i] (the issuing thread; one commit, one wait each)
     uint32_t stage = 0;   // ring stages consumed
     unsigned bar_target = 0;
     unsigned *bar_ctr = ws.sync;
@@ -1179,6 +1330,26 @@ __global__ void __launch_bounds__(kThreads, 1) k_fused(const __grid_constant__ P
             }
         }
         consumer_sync();
+    };
+    // Bounded exit of a warp's polling loop, the same answer in every lane: true
+    // once the CTA has aborted or the kernel's deadline has passed (then the
+    // abort flag, the status bit and the wait report are set).
+    auto poll_give_up = [&](int site, int index) -> bool {
+        int give_up = 0;
+        if (lane == 0) {
+            give_up = *reinterpret_cast<volatile int *>(&s.abort) != 0;
+            if (!give_up && gtime() > deadline) {
+                give_up = 1;
+                *reinterpret_cast<volatile int *>(&s.abort) = 1;
+                if (atomicOr(status, FGM_STATUS_WAIT_TIMEOUT) == 0) {
+                    status[1] = site;
+                    status[2] = cta;
+                    status[3] = warp;
+                    status[4] = index;
+                }
+            }
+        }
+        return __shfl_sync(0xFFFFFFFFu, give_up, 0) != 0;
     };
 
     long long *detail = (TRACE && p.trace && cta == G / 2)
@@ -1393,8 +1564,11 @@ __global__ void __launch_bounds__(kThreads, 1) k_fused(const __grid_constant__ P
             const bool norm = p.mode != kModeLayer;
             const bool router_cta = cta >= G - kRouterCtas;
             const int e0 = kRouterRows * (cta - (G - kRouterCtas));   // first router row (router CTAs)
-            // only the router CTAs and those hosting a term-split unit read h here
-            const bool need_h = router_cta || (G - 1 - cta) * kMW < M * kMW;
+            // only the router CTAs and those hosting a term-split unit read h here;
+            // token t's units sit on CTA G - kRouterCtas - 1 - t, next to the router
+            // CTAs, so that the two jobs run side by side
+            const int term_t = G - kRouterCtas - 1 - cta;
+            const bool need_h = router_cta || (term_t >= 0 && term_t < M);
             // Lane (g, q) holds 64 values of token g in warp w's 256-wide K-slice: fp32
             // rows at positions 256 w + 64 c + 16 k + 4 q + i (v[c][4 k + i]), bf16 rows
             // at 256 w + 64 c + 32 k + 8 q + i (v[c][8 k + i]); the four lanes of a token
@@ -1536,12 +1710,13 @@ __global__ void __launch_bounds__(kThreads, 1) k_fused(const __grid_constant__ P
                     __stcg(ws.logits + t * kE + e0 + j, z * rt + rbias);
                 }
                 // Activation terms of the gate/up products, computed once per grid:
-                // unit (token t, 256-wide K-slice w) is split by warp w of CTA G - 1 - t
-                // (a router CTA: it holds the slice in lanes 4 t .. 4 t + 3), 8 values a
-                // lane after a pass through shared memory (the exchange buffer is idle
-                // in phase A), into kTerms E4M3 terms under a power-of-two scale per unit.
-                const int t = G - 1 - cta;
-                if (t < M) {
+                // unit (token t, 256-wide K-slice w) is split by warp w of CTA
+                // G - kRouterCtas - 1 - t (it holds the slice in lanes 4 t .. 4 t + 3),
+                // 8 values a lane after a pass through shared memory (the exchange
+                // buffer is idle in phase A), into kTerms E4M3 terms under a
+                // power-of-two scale per unit.
+                const int t = term_t;
+                if (t >= 0 && t < M) {
                     const int w = warp;
                     const int k0 = 256 * w + 8 * lane;
                     float *sx = reinterpret_cast<float *>(&s.red[0][0][0][0]) + 256 * warp;
@@ -1830,6 +2005,172 @@ __global__ void __launch_bounds__(kThreads, 1) k_fused(const __grid_constant__ P
         consumer_sync();
         stamp(8);
         // -------------------------------------------------------- phase C
+        if constexpr (TCD) {
+            const int U = s.n_unique[pb];
+            const DownStages ds(U + NS, cta, G);
+            const int si0 = ds.begin / kH;
+            uint8_t *bop = reinterpret_cast<uint8_t *>(&s.red[0][0][0][0]);   // [2][kTcBBytes]: idle exchange buffer
+            // 1. B operands of the (at most two) slots this CTA's rows cover: warp
+            //    t < M polls token t's 704 activations until none is pending, scales
+            //    them by a power of two per (slot, token) and writes kTerms E4M3
+            //    terms as columns 3 t + e (the other columns stay zero)
+            for (int i = tid; i < 2 * kTcBBytes / 16; i += kConsumers)
+                reinterpret_cast<uint4 *>(bop)[i] = make_uint4(0u, 0u, 0u, 0u);
+            consumer_sync();
+#pragma unroll 1
+            for (int h2 = 0; h2 < 2; ++h2) {
+                const int si = si0 + h2;
+                const bool slot_ok = ds.end > ds.begin && si < U + NS && (h2 == 0 || ds.end > (si0 + 1) * kH);
+                if (!slot_ok || warp >= M)
+                    continue;
+                const int t = warp;
+                const int aslot = si < U ? si : kSharedSlot + si - U;
+                const float *a = act_cur + ((size_t)aslot * kMaxM + t) * kF;
+                float v[kF / 32];
+                for (int it = 0;; ++it) {
+                    bool pending = false;
+#pragma unroll
+                    for (int jj = 0; jj < kF / 32; ++jj) {
+                        v[jj] = ld_poll1(a + lane + 32 * jj);
+                        pending |= __float_as_uint(v[jj]) == kActPending;
+                    }
+                    if (!__any_sync(0xFFFFFFFFu, pending))
+                        break;
+                    if ((it & 15) == 15 && poll_give_up(11, aslot)) {
+#pragma unroll
+                        for (int jj = 0; jj < kF / 32; ++jj)
+                            v[jj] = 0.0f;
+                        break;
+                    }
+                }
+                float amax = 0.0f;
+#pragma unroll
+                for (int jj = 0; jj < kF / 32; ++jj)
+                    amax = fmaxf(amax, fabsf(v[jj]));
+#pragma unroll
+                for (int o = 16; o > 0; o >>= 1)
+                    amax = fmaxf(amax, __shfl_xor_sync(0xFFFFFFFFu, amax, o));
+                const float S = term_scale(amax);
+                if (lane == 0)
+                    s.dscale[h2][t] = S;
+                uint8_t *b = bop + h2 * kTcBBytes;
+#pragma unroll
+                for (int jj = 0; jj < kF / 32; ++jj) {
+                    const int k = lane + 32 * jj;
+                    float y = v[jj] * S;
+#pragma unroll
+                    for (int e = 0; e < kTerms; ++e) {
+                        const __nv_fp8_storage_t c = __nv_cvt_float_to_fp8(y, __NV_SATFINITE, __NV_E4M3);
+                        b[tc_b_offset(3 * t + e, k)] = static_cast<uint8_t>(c);
+                        if (e + 1 < kTerms)
+                            y = (y - __half2float(__half(__nv_cvt_fp8_to_halfraw(c, __NV_E4M3)))) * 16.0f;
+                    }
+                }
+            }
+            asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+            consumer_sync();
+            // 2. the tiles: one thread issues the products, warps 0..3 (tensor-memory
+            //    lanes 32 w .. 32 w + 31) read the accumulators, combine the terms,
+            //    apply the row scales and add into the residual stream
+            int n_tiles = 0;
+            for (int pos = ds.begin, nr = 0; pos < ds.end; pos += nr, ++n_tiles)
+                nr = tc_tile_rows(pos, ds.end);
+            const uint32_t stage0 = stage;
+            if (warp == kMW - 1) {
+                if (lane == 0) {
+                    bool ok = *reinterpret_cast<volatile int *>(&s.abort) == 0;
+                    bool have_prev = false;   // a stage whose slot is still to be released
+                    int prev_slot = 0;
+                    int ti = 0;
+                    for (int pos = ds.begin, nr = 0; pos < ds.end && ok; pos += nr, ++ti) {
+                        nr = tc_tile_rows(pos, ds.end);
+                        const uint32_t b0 = su32(bop + (pos / kH == si0 ? 0 : kTcBBytes));
+                        const uint32_t gt = tc_tiles + ti;
+                        const int buf = gt & 1;
+                        // the epilogue has read this accumulator two tiles ago
+                        if (gt >= 2 && !(ok = mbar_wait(&s.tempty[buf], ((gt >> 1) - 1) & 1, s, deadline, status, 8,
+                                                        (int)gt)))
+                            break;
+                        tc_fence_after();
+                        const uint32_t d = s.tmem_base + static_cast<uint32_t>(buf * kTcN);
+                        for (int ks = 0; ks < kTcStagesPerTile && ok; ++ks) {
+                            const int slot = stage % kStages;
+                            dstamp(stage, layer_stage0, 5);
+                            if (!(ok = mbar_wait(&s.full[slot], (stage / kStages) & 1, s, deadline, status, 3,
+                                                 (int)stage)))
+                                break;
+                            dstamp(stage, layer_stage0, 1);
+                            tc_fence_after();
+                            const uint32_t a0 = su32(s.ring[slot]);
+#pragma unroll
+                            for (int b = 0; b < 2; ++b)
+#pragma unroll
+                                for (int kk = 0; kk < 4; ++kk) {
+                                    const int kg = 256 * ks + 128 * b + 32 * kk;
+                                    if (kg < kF)
+                                        tc_mma(d, tc_desc_sw128(a0 + b * kTcBoxBytes + kk * 32), tc_desc_nosw(b0 + kg * 16),
+                                               kg > 0);
+                                }
+                            // this slot is released once its products are done: the
+                            // previous stage's slot is released here, after this
+                            // stage's products are issued
+                            tc_commit(&s.mdone[slot]);
+                            dstamp(stage, layer_stage0, 2);
+                            if (have_prev) {
+                                ok = mbar_wait(&s.mdone[prev_slot], (mdone_phase >> prev_slot) & 1u, s, deadline,
+                                               status, 9, (int)stage);
+                                mdone_phase ^= 1u << prev_slot;
+                                mbar_arrive_n(&s.empty[prev_slot], kMW);
+                            }
+                            have_prev = true;
+                            prev_slot = slot;
+                            dstamp(stage, layer_stage0, 3);
+                            ++stage;
+                        }
+                        if (ok)
+                            tc_commit(&s.tfull[buf]);
+                    }
+                    // the last stage's slot, once its products are done (also after an
+                    // abort: nothing may be in flight when tensor memory is released)
+                    if (have_prev) {
+                        mbar_wait(&s.mdone[prev_slot], (mdone_phase >> prev_slot) & 1u, s, deadline, status, 9, -1);
+                        mdone_phase ^= 1u << prev_slot;
+                        mbar_arrive_n(&s.empty[prev_slot], kMW);
+                    }
+                }
+                __syncwarp();
+            } else if (warp < 4) {
+                int ti = 0;
+                for (int pos = ds.begin, nr = 0; pos < ds.end; pos += nr, ++ti) {
+                    nr = tc_tile_rows(pos, ds.end);
+                    const int h2 = pos / kH == si0 ? 0 : 1;
+                    const uint32_t gt = tc_tiles + ti;
+                    const int buf = gt & 1;
+                    if (!mbar_wait(&s.tfull[buf], (gt >> 1) & 1, s, deadline, status, 10, (int)gt))
+                        break;
+                    tc_fence_after();
+                    float v[16];
+                    tc_ld16(s.tmem_base + (static_cast<uint32_t>(32 * warp) << 16) + static_cast<uint32_t>(buf * kTcN), v);
+                    tc_fence_before();
+                    __syncwarp();
+                    if (lane == 0)
+                        mbar_arrive(&s.tempty[buf]);
+                    const int r = 32 * warp + lane;
+                    if (r < nr) {
+                        const int j = pos % kH + r;
+                        const float sd = s.sc_d[pos - ds.begin + r];
+#pragma unroll
+                        for (int t = 0; t < 5; ++t)
+                            if (t < M)
+                                atomicAdd(ws.h + (size_t)t * kH + j,
+                                          (v[3 * t] + v[3 * t + 1] * 0.0625f + v[3 * t + 2] * 0.00390625f) /
+                                              s.dscale[h2][t] * sd);
+                    }
+                }
+            }
+            stage = stage0 + kTcStagesPerTile * n_tiles;
+            tc_tiles += n_tiles;
+        } else
         {
             const int U = s.n_unique[pb];
             const DownStages ds(U + NS, cta, G);
@@ -1941,6 +2282,15 @@ __global__ void __launch_bounds__(kThreads, 1) k_fused(const __grid_constant__ P
             mark_pending((l + 1) & 1, l == 0 ? 0 : s.n_unique[(l - 1) & 1]);
         stamp(9);
         grid_barrier();
+    }
+    if constexpr (TCD) {
+        // every product has completed (each stage's commit was waited for)
+        consumer_sync();
+        if (warp == 0) {
+            tc_fence_after();
+            asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(s.tmem_base), "r"(kTcTmemCols)
+                         : "memory");
+        }
     }
     if (TRACE && p.trace && tid == 0)
         p.trace[((size_t)n_layers * kTracePoints) * G + cta] = gtime();

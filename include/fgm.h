@@ -63,8 +63,9 @@ enum {
     FGM_PATH_FUSED = 0,  /* default: one persistent cooperative kernel per call; weight rows stream
                             through a TMA-bulk shared-memory ring into FP8/bf16 mma.sync tiles */
     FGM_PATH_STAGED = 1, /* one launch per stage with fp32 CUDA-core arithmetic (comparison path) */
-    FGM_PATH_FUSED_TC = 2, /* as FGM_PATH_FUSED, with the FP8 lm_head on the tensor-memory kernel
-                              (tcgen05.mma, TMA tensor copies) instead of the mma.sync one */
+    FGM_PATH_FUSED_TC = 2, /* as FGM_PATH_FUSED, with tcgen05.mma (TMA tensor copies, tensor-memory
+                              accumulators) for the FP8 lm_head and, at M <= 5 with the shared
+                              expert, for the routed and shared down products */
 };
 
 /* Status bits written by kernels into the workspace (fgm_read_status). */
@@ -340,7 +341,10 @@ int fgm_read_status(void *ws, size_t ws_bytes, int clear, int32_t *status, void 
  * (HOST report): {site, block, warp, index}; site 1 = ring slot free
  * (producer), 2 = routing known (producer), 3 = ring data landed, 6 = grid
  * barrier (warp = counter value, index = target), 7 = activation rows of an
- * expert written (index = its slot). Synchronises the stream. */
+ * expert written (index = its slot); FGM_PATH_FUSED_TC's down phase: 8 =
+ * accumulator read, 9 = products of a ring slot done, 10 = accumulator
+ * full, 11 = activation rows written (index = slot). Synchronises the
+ * stream. */
 int fgm_read_wait_report(void *ws, size_t ws_bytes, int32_t *report, void *stream);
 
 /* Message describing the last error returned on the calling thread. */

@@ -8,6 +8,7 @@ weights agree). The file is named to be collected last, so that it runs both
 after the whole suite and, alone, in a fresh process.
 """
 
+import gc
 import ctypes
 
 import numpy as np
@@ -56,13 +57,14 @@ def test_noalloc_matches_workspace_call_twice():
         # device) must not grow across the two calls that follow it
         fgm.moe_layer_fwd_noalloc(p, xs[0], ys[0])
         torch.cuda.synchronize()
+        gc.collect()   # tensors of earlier tests freed now, not between the two readings
         before = torch.cuda.memory_allocated()
         free_before, _ = torch.cuda.mem_get_info()
         for i in range(2):   # two calls in a row on the built-in scratch
             fgm.moe_layer_fwd_noalloc(p, xs[i], ys[i], topk_ids=ids[i], topk_w=wts[i])
         torch.cuda.synchronize()
         free_after, _ = torch.cuda.mem_get_info()
-        assert torch.cuda.memory_allocated() == before
+        assert torch.cuda.memory_allocated() <= before
         assert free_after >= free_before
         for i, x in enumerate(xs):
             M = x.shape[0]
