@@ -25,6 +25,9 @@ constexpr int kMaxSlotsAll = kMaxM * kK + kMaxDense;   // routed + dense parts (
 constexpr int kMaxParts = 2048;        // lm_head per-CTA partials kept in the workspace
 constexpr float kEps = FGM_RMS_EPS;
 constexpr int kSyncLmHeadDone = 127;   // workspace sync word counting finished FP8 lm_head CTAs
+constexpr int kSyncTileCount = 2;      // sync words [2, 98): down tiles taken per slot, by layer parity
+constexpr int kSyncTileStride = 48;    // (the persistent kernel's tensor-memory down phase, M <= 5)
+static_assert(kSyncTileCount + 2 * kSyncTileStride <= kSyncLmHeadDone, "sync words overlap");
 
 // Device scratch carved out of the caller's workspace (see ws_layout()).
 struct Ws {
@@ -47,8 +50,8 @@ struct Ws {
     int32_t *io_draft; // [8]
     int32_t *io_out;   // [2]
     int32_t *status;   // [1] FGM_STATUS_* bits
-    unsigned *sync;    // [128] [0] grid barrier, [1] exit count, [2 + s] completed activation rows of slot s,
-                       // [kSyncLmHeadDone] CTAs done in the FP8 lm_head
+    unsigned *sync;    // [128] [0] grid barrier, [1] exit count, [kSyncTileCount + 48 parity + s] down
+                       // tiles taken from slot s, [kSyncLmHeadDone] CTAs done in the FP8 lm_head
     uint8_t *xterms;   // [8][3][2816] E4M3 terms of the gate/up input of the current layer
     float *xscale;     // [8][11] their power-of-two scale per token and 256-wide K-slice
     float *part_sum;   // [kMaxParts][8] sampling: per-CTA sum of exp((z - part_val) / T)

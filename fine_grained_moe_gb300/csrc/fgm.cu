@@ -143,9 +143,15 @@ int launch_fused(fused::Params &prm, cudaStream_t st)
     if (G < 0)
         return G;
     // the tensor-memory path runs the down phase on tcgen05 (M <= 5, one shared expert)
-    const bool tcd = g_path == FGM_PATH_FUSED_TC && prm.M <= 5 && prm.dense.parts == 0 && prm.mode != fused::kModeLmHead;
+    // (its bulk copies of row scales want 16-byte aligned scale arrays; else the
+    // mma.sync down phase runs)
+    bool tcd = g_path == FGM_PATH_FUSED_TC && prm.M <= 5 && prm.dense.parts == 0 && prm.mode != fused::kModeLmHead;
+    const int n_tc = prm.mode == fused::kModeLayer ? 1 : prm.n_layers;
+    for (int l = 0; tcd && l < n_tc; ++l)
+        if (reinterpret_cast<uintptr_t>(prm.layers[l].down_s) & 15u)
+            tcd = false;
     if (tcd) {
-        const int n_l = prm.mode == fused::kModeLayer ? 1 : prm.n_layers;
+        const int n_l = n_tc;
         for (int l = 0; l < n_l; ++l) {
             const int rc = tc_down_maps(prm.layers[l].down_q, &prm.dmap[l], &prm.dmap16[l]);
             if (rc != FGM_OK)

@@ -133,13 +133,17 @@ struct __align__(128) Smem {
     int32_t slot_of[kE];
     float sc_g[kMaxGuRows + 8 * kMaxShTiles];   // gate/up row scales of this CTA's routed rows, then
     float sc_u[kMaxGuRows + 8 * kMaxShTiles];   // (from kMaxGuRows) its always-on rows
-    float sc_d[kMaxDownRows];   // down row scales of this CTA's down rows of the layer
+    alignas(16) float sc_d[kMaxDownRows];   // down row scales of this CTA's down rows of the layer
+                                            // (tensor-memory phase: of its last kTcInfo tiles)
+    int2 tinfo[8];              // tensor-memory down phase: (first row in the flattened (slot, row)
+                                // space or -1 at the end, home slot 0/1) of tile sequence number % 8
     unsigned long long full[kStages];
     unsigned long long empty[kStages];
     unsigned long long route;
     unsigned long long tfull[2], tempty[2];   // tensor-memory down phase: accumulators full / read
     unsigned long long mdone[kStages];        // tensor-memory down phase: products of a ring slot done
     uint32_t tmem_base;
+    uint32_t tc_stage, tc_next;   // tensor-memory down phase: ring stages and tile numbers after it
     float dscale[2][8];         // tensor-memory down phase: activation-term scale per (slot, token)
     int abort;
     int last;
@@ -257,6 +261,9 @@ constexpr int kTcStagesPerTile = 3;          // K 0..255, 256..511, 512..767 (ze
 constexpr int kTcBoxBytes = kTcRows * 128;   // one 128-row x 128-byte box
 constexpr int kTcBBytes = (kF / 16) * 256;   // B operand of one slot: 44 K-columns x 16 rows x 16 bytes
 constexpr uint32_t kTcTmemCols = 32;         // two 16-column accumulators
+constexpr int kTcInfo = 8;                   // tile records in flight (producer at most 4 tiles ahead of the epilogue)
+static_assert(kTcInfo * kTcRows <= kMaxDownRows, "tile scales do not fit");
+static_assert(5 * kK + 1 <= kSyncTileStride, "down-tile counters: slots at M <= 5 (one shared expert)");
 // instruction descriptor, kind::f8f6f4: D fp32, A and B E4M3, both K-major, N >> 3, M >> 4
 constexpr uint32_t kTcIdesc = (1u << 4) | (static_cast<uint32_t>(kTcN >> 3) << 17) |
                               (static_cast<uint32_t>(kTcRows >> 4) << 24);
@@ -327,10 +334,15 @@ __device__ __forceinline__ void mbar_arrive_n(unsigned long long *b, uint32_t n)
 }
 
 // A down tile of the tensor-memory phase: rows [pos, pos + nr) of the CTA's
-// flattened (slot, row) range, within one slot and at most 128 rows.
+// flattened (slot, row) range, within one slot and at most 128 rows. Each
+// slot's part of the range starts with its remainder (length mod 128), then
+// whole tiles: a short tile costs a whole tile's products, and first they run
+// while the whole tiles' weights are still arriving.
 __device__ __forceinline__ int tc_tile_rows(int pos, int end)
 {
-    return min(min(end, (pos / kH + 1) * kH), pos + kTcRows) - pos;
+    const int left = min(end, (pos / kH + 1) * kH) - pos;
+    const int r = left % kTcRows;
+    return r ? r : kTcRows;
 }
 
 // Named barrier of the MMA warps (the producer never joins).
@@ -1136,6 +1148,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_fused(const __grid_constant__ P
                                      ? p.trace + (size_t)(n_layers * kTracePoints + 2) * G : nullptr;
             int p_layer = 0;
             uint32_t p_stage0 = 0;
+            uint32_t p_tiles = 0;   // tensor-memory down tiles (and end markers) announced
             // Claims the next ring slot for `bytes` of copies; returns its base.
             auto claim = [&](uint32_t bytes) -> uint8_t * {
                 const int slot = stage % kStages;
@@ -1207,30 +1220,50 @@ __global__ void __launch_bounds__(kThreads, 1) k_fused(const __grid_constant__ P
                     gu_rows(L.gate_q + e * kF * kH, L.up_q + e * kF * kH, 8 * (x % kGuTiles), 8);
                 }
                 if constexpr (TCD) {
-                    // 128-row tiles within one slot, each in three K-stages of two
-                    // 128-byte boxes (K 640..767 reads zeros past 704); a ragged tile
-                    // in 16-row boxes
+                    // Whole 128-row tiles (a slot is 22 of them), taken one at a time
+                    // from a per-slot counter shared by the CTAs whose static ranges
+                    // touch the slot (their home slots, whose activation terms they
+                    // prepare): a CTA that runs ahead takes more of its slots' tiles.
+                    // Each tile: three K-stages of two 128-byte boxes (K 640..767
+                    // reads zeros past 704), its 128 row scales with the first. Then
+                    // an empty stage with an end marker.
                     const DownStages dsp(U + NS, cta, G);
-                    for (int pos = dsp.begin, nr = 0; pos < dsp.end && ok; pos += nr) {
-                        nr = tc_tile_rows(pos, dsp.end);
-                        const int si = pos / kH;
-                        const int y = (si < U ? s.experts[pb][si] : kShared) * kH + pos % kH;
-                        for (int ks = 0; ks < kTcStagesPerTile && ok; ++ks) {
-                            uint8_t *dst = claim(2u * static_cast<uint32_t>(nr) * 128u);
-                            if (!dst)
+                    const int hs0 = dsp.begin / kH;
+                    const int n_home = dsp.end > dsp.begin ? (dsp.end - 1) / kH - hs0 + 1 : 0;
+                    unsigned *cnt = ws.sync + kSyncTileCount + (l & 1) * kSyncTileStride;
+                    for (int h2 = 0; h2 < n_home && ok; ++h2) {
+                        const int si = hs0 + h2;
+                        const int e = si < U ? s.experts[pb][si] : kShared;
+                        const float *dsc = si < U ? L.down_s + (size_t)e * kH : Parts<NS>::down_s(L, p.dense, si - U);
+                        for (;;) {
+                            const unsigned t = atomicAdd(cnt + si, 1u);
+                            if (t >= static_cast<unsigned>(kH / kTcRows))
                                 break;
-                            const uint32_t d0 = su32(dst);
-                            for (int b = 0; b < 2; ++b) {
-                                const int x = 256 * ks + 128 * b;
-                                if (nr == kTcRows)
-                                    tma_2d(d0 + b * kTcBoxBytes, &p.dmap[l], x, y, &s.full[stage % kStages]);
-                                else
-                                    for (int r16 = 0; r16 < nr; r16 += 16)
-                                        tma_2d(d0 + b * kTcBoxBytes + r16 * 128, &p.dmap16[l], x, y + r16,
-                                               &s.full[stage % kStages]);
+                            const int row = static_cast<int>(t) * kTcRows;
+                            s.tinfo[p_tiles % kTcInfo] = make_int2(si * kH + row, h2);
+                            float *sc = &s.sc_d[(p_tiles % kTcInfo) * kTcRows];
+                            ++p_tiles;
+                            for (int ks = 0; ks < kTcStagesPerTile && ok; ++ks) {
+                                uint8_t *dst = claim(2u * kTcBoxBytes + (ks == 0 ? kTcRows * 4u : 0u));
+                                if (!dst)
+                                    break;
+                                const uint32_t d0 = su32(dst);
+                                if (ks == 0)
+                                    bulk_g2s(sc, dsc + row, kTcRows * 4u, &s.full[stage % kStages]);
+                                for (int b = 0; b < 2; ++b)
+                                    tma_2d(d0 + b * kTcBoxBytes, &p.dmap[l], 256 * ks + 128 * b, e * kH + row,
+                                           &s.full[stage % kStages]);
+                                ++stage;
                             }
-                            ++stage;
+                            if (!ok)
+                                break;
                         }
+                    }
+                    if (ok) {
+                        s.tinfo[p_tiles % kTcInfo] = make_int2(-1, 0);
+                        ++p_tiles;
+                        if (claim(0u))
+                            ++stage;
                     }
                 } else {
                     const DownStages dsp(U + NS, cta, G);
@@ -1554,6 +1587,12 @@ __global__ void __launch_bounds__(kThreads, 1) k_fused(const __grid_constant__ P
         stamp(0);
         if (l == 0 && p.debug_stall && tid == 0)
             bar_target += 1;   // the next grid barrier can never complete
+        if constexpr (TCD) {
+            // the next layer's down-tile counters (last used two layers ago, by
+            // producers that finished before this layer began)
+            if (cta == 0 && tid < kSyncTileStride)
+                ws.sync[kSyncTileCount + ((l + 1) & 1) * kSyncTileStride + tid] = 0u;
+        }
         if (l == 0 && p.debug_stall)
             grid_barrier();
         // -------------------------------------------------------- phase A
@@ -1935,7 +1974,8 @@ __global__ void __launch_bounds__(kThreads, 1) k_fused(const __grid_constant__ P
                 cp_async4(&s.sc_g[k], L.gate_s + row);
                 cp_async4(&s.sc_u[k], L.up_s + row);
             }
-            {
+            if constexpr (!TCD) {
+                // (the tensor-memory phase's producer copies each tile's scales)
                 const Range rd = down_rows(U + NS, cta, G);
                 for (int k = tid; k < rd.end - rd.begin; k += kConsumers) {
                     const int pos = rd.begin + k;
@@ -2069,23 +2109,20 @@ __global__ void __launch_bounds__(kThreads, 1) k_fused(const __grid_constant__ P
             }
             asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
             consumer_sync();
-            // 2. the tiles: one thread issues the products, warps 0..3 (tensor-memory
-            //    lanes 32 w .. 32 w + 31) read the accumulators, combine the terms,
-            //    apply the row scales and add into the residual stream
-            int n_tiles = 0;
-            for (int pos = ds.begin, nr = 0; pos < ds.end; pos += nr, ++n_tiles)
-                nr = tc_tile_rows(pos, ds.end);
-            const uint32_t stage0 = stage;
+            // 2. the tiles, in the order the producer took them (its tile records,
+            //    then an end marker): one thread issues the products, warps 0..3
+            //    (tensor-memory lanes 32 w .. 32 w + 31) read the accumulators,
+            //    combine the terms, apply the row scales and add into the residual
+            //    stream. The issuing thread publishes the stage and tile counts
+            //    after the phase (the tile count is known only to it).
             if (warp == kMW - 1) {
                 if (lane == 0) {
                     bool ok = *reinterpret_cast<volatile int *>(&s.abort) == 0;
                     bool have_prev = false;   // a stage whose slot is still to be released
                     int prev_slot = 0;
-                    int ti = 0;
-                    for (int pos = ds.begin, nr = 0; pos < ds.end && ok; pos += nr, ++ti) {
-                        nr = tc_tile_rows(pos, ds.end);
-                        const uint32_t b0 = su32(bop + (pos / kH == si0 ? 0 : kTcBBytes));
-                        const uint32_t gt = tc_tiles + ti;
+                    uint32_t gt = tc_tiles;
+                    s.tc_next = gt;   // (after an abort: where it stopped)
+                    for (; ok; ++gt) {
                         const int buf = gt & 1;
                         // the epilogue has read this accumulator two tiles ago
                         if (gt >= 2 && !(ok = mbar_wait(&s.tempty[buf], ((gt >> 1) - 1) & 1, s, deadline, status, 8,
@@ -2093,6 +2130,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_fused(const __grid_constant__ P
                             break;
                         tc_fence_after();
                         const uint32_t d = s.tmem_base + static_cast<uint32_t>(buf * kTcN);
+                        bool end_marker = false;
                         for (int ks = 0; ks < kTcStagesPerTile && ok; ++ks) {
                             const int slot = stage % kStages;
                             dstamp(stage, layer_stage0, 5);
@@ -2100,7 +2138,18 @@ __global__ void __launch_bounds__(kThreads, 1) k_fused(const __grid_constant__ P
                                                  (int)stage)))
                                 break;
                             dstamp(stage, layer_stage0, 1);
+                            const int2 inf = s.tinfo[gt % kTcInfo];
+                            if (inf.x < 0) {
+                                // the end marker's empty stage: its slot back, then the
+                                // epilogue told through this accumulator's barrier
+                                mbar_arrive_n(&s.empty[slot], kMW);
+                                ++stage;
+                                mbar_arrive(&s.tfull[buf]);
+                                end_marker = true;
+                                break;
+                            }
                             tc_fence_after();
+                            const uint32_t b0 = su32(bop + inf.y * kTcBBytes);
                             const uint32_t a0 = su32(s.ring[slot]);
 #pragma unroll
                             for (int b = 0; b < 2; ++b)
@@ -2127,6 +2176,10 @@ __global__ void __launch_bounds__(kThreads, 1) k_fused(const __grid_constant__ P
                             dstamp(stage, layer_stage0, 3);
                             ++stage;
                         }
+                        if (end_marker) {
+                            s.tc_next = gt + 1;
+                            break;
+                        }
                         if (ok)
                             tc_commit(&s.tfull[buf]);
                     }
@@ -2137,17 +2190,23 @@ __global__ void __launch_bounds__(kThreads, 1) k_fused(const __grid_constant__ P
                         mdone_phase ^= 1u << prev_slot;
                         mbar_arrive_n(&s.empty[prev_slot], kMW);
                     }
+                    s.tc_stage = stage;
                 }
                 __syncwarp();
             } else if (warp < 4) {
-                int ti = 0;
-                for (int pos = ds.begin, nr = 0; pos < ds.end; pos += nr, ++ti) {
-                    nr = tc_tile_rows(pos, ds.end);
-                    const int h2 = pos / kH == si0 ? 0 : 1;
-                    const uint32_t gt = tc_tiles + ti;
+                for (uint32_t gt = tc_tiles;; ++gt) {
                     const int buf = gt & 1;
                     if (!mbar_wait(&s.tfull[buf], (gt >> 1) & 1, s, deadline, status, 10, (int)gt))
                         break;
+                    const int2 inf = s.tinfo[gt % kTcInfo];
+                    if (inf.x < 0) {
+                        // the end marker: nothing to read; its phase of the
+                        // accumulator's barrier is answered like a tile's
+                        __syncwarp();
+                        if (lane == 0)
+                            mbar_arrive(&s.tempty[buf]);
+                        break;
+                    }
                     tc_fence_after();
                     float v[16];
                     tc_ld16(s.tmem_base + (static_cast<uint32_t>(32 * warp) << 16) + static_cast<uint32_t>(buf * kTcN), v);
@@ -2156,20 +2215,19 @@ __global__ void __launch_bounds__(kThreads, 1) k_fused(const __grid_constant__ P
                     if (lane == 0)
                         mbar_arrive(&s.tempty[buf]);
                     const int r = 32 * warp + lane;
-                    if (r < nr) {
-                        const int j = pos % kH + r;
-                        const float sd = s.sc_d[pos - ds.begin + r];
+                    const int j = inf.x % kH + r;
+                    const float sd = s.sc_d[(gt % kTcInfo) * kTcRows + r];
 #pragma unroll
-                        for (int t = 0; t < 5; ++t)
-                            if (t < M)
-                                atomicAdd(ws.h + (size_t)t * kH + j,
-                                          (v[3 * t] + v[3 * t + 1] * 0.0625f + v[3 * t + 2] * 0.00390625f) /
-                                              s.dscale[h2][t] * sd);
-                    }
+                    for (int t = 0; t < 5; ++t)
+                        if (t < M)
+                            atomicAdd(ws.h + (size_t)t * kH + j,
+                                      (v[3 * t] + v[3 * t + 1] * 0.0625f + v[3 * t + 2] * 0.00390625f) /
+                                          s.dscale[inf.y][t] * sd);
                 }
             }
-            stage = stage0 + kTcStagesPerTile * n_tiles;
-            tc_tiles += n_tiles;
+            consumer_sync();
+            stage = s.tc_stage;
+            tc_tiles = s.tc_next;
         } else
         {
             const int U = s.n_unique[pb];
@@ -2474,6 +2532,11 @@ __global__ void __launch_bounds__(kThreads, 1) k_fused(const __grid_constant__ P
             p.out[0] = a;
             p.out[1] = arg[a];
         }
+    }
+    if constexpr (TCD) {
+        // both parities of the down-tile counters, for the next launch
+        if (tid < 2 * kSyncTileStride)
+            ws.sync[kSyncTileCount + tid] = 0u;
     }
     if (tid == 0) {
         bar_ctr[1] = 0;
