@@ -45,6 +45,8 @@ DRAFT_SEED0 = 33
 N_DRAFT_SEEDS = 64
 P_COPY = 0.7   # probability that a draft copies the target's argmax
 EMB_SEED = 32
+# --path names and the library's path constants
+PATHS = {"fused": "PATH_FUSED", "staged": "PATH_STAGED", "fused_tc": "PATH_FUSED_TC", "fused_mma": "PATH_FUSED_MMA"}
 WORKLOAD = ("full verify step: 30-layer FP8 MoE stack (Gemma-4-26B-A4B shape, Zipf s=1.1) + "
             "final RMSNorm + 262144x2816 bf16 tied lm_head argmax + greedy accept, M=5 (gamma=4)")
 FALLBACK_HBM_GBS = 6800.0
@@ -364,7 +366,7 @@ def run_ours(args, rank, world):
     dev = torch.device("cuda", int(os.environ.get("LOCAL_RANK", 0)))
     torch.cuda.set_device(dev)
     fgm.lib()
-    fgm.select_path({"fused": fgm.PATH_FUSED, "staged": fgm.PATH_STAGED, "fused_tc": fgm.PATH_FUSED_TC}[args.path])
+    fgm.select_path(getattr(fgm, PATHS[args.path]))
     nl, V = args.layers, args.vocab
     full_size = (nl, V) == (N_LAYERS, 262144)
     if args.phase_trace and not full_size:
@@ -533,7 +535,7 @@ def run_case(args):
     dev = torch.device("cuda", 0)
     torch.cuda.set_device(dev)
     fgm.lib()
-    fgm.select_path({"fused": fgm.PATH_FUSED, "staged": fgm.PATH_STAGED, "fused_tc": fgm.PATH_FUSED_TC}[args.path])
+    fgm.select_path(getattr(fgm, PATHS[args.path]))
     ws = fgm.Workspace(dev)
     xs = [synth.hidden_states(HIDDEN_SEED0 + b, M, device=dev) for b in range(N_BATCHES)]
     K, W = args.steps, args.warmup
@@ -610,7 +612,7 @@ def run_sweep(args):
     dev = torch.device("cuda", 0)
     torch.cuda.set_device(dev)
     fgm.lib()
-    fgm.select_path({"fused": fgm.PATH_FUSED, "staged": fgm.PATH_STAGED, "fused_tc": fgm.PATH_FUSED_TC}[args.path])
+    fgm.select_path(getattr(fgm, PATHS[args.path]))
     layers, emb, _ = make_workload(dev)
     ws = fgm.Workspace(dev)
     peak, _ = measured_peaks()
@@ -670,7 +672,7 @@ def run_verify_fp8(args):
     dev = torch.device("cuda", 0)
     torch.cuda.set_device(dev)
     fgm.lib()
-    fgm.select_path({"fused": fgm.PATH_FUSED, "staged": fgm.PATH_STAGED, "fused_tc": fgm.PATH_FUSED_TC}[args.path])
+    fgm.select_path(getattr(fgm, PATHS[args.path]))
     layers, emb, xs = make_workload(dev)
     emb_q, emb_s = synth.embedding_fp8(emb)
     del emb
@@ -791,9 +793,9 @@ def main():
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=("ours", "reference"), default="ours")
     ap.add_argument("--no-cpu-baseline", action="store_true")
-    ap.add_argument("--path", choices=("fused", "staged", "fused_tc"), default="fused",
-                    help="persistent kernel (default), one launch per stage, or the persistent kernel with the "
-                         "tcgen05 FP8 lm_head")
+    ap.add_argument("--path", choices=tuple(PATHS), default="fused",
+                    help="persistent kernel (default), one launch per stage, the persistent kernel with the "
+                         "tcgen05 FP8 lm_head, or the persistent kernel with mma.sync down products")
     ap.add_argument("--layers", type=int, default=N_LAYERS,
                     help="verify case only: stack depth (a smaller case for ncu captures; default 30)")
     ap.add_argument("--vocab", type=int, default=262144,

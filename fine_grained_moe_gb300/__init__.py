@@ -30,9 +30,10 @@ MAX_LAYERS = 48
 
 STATUS_NONFINITE_LOGITS = 1
 STATUS_WAIT_TIMEOUT = 2
-PATH_FUSED = 0    # one persistent cooperative kernel per call (TMA ring + mma.sync tiles)
+PATH_FUSED = 0    # one persistent cooperative kernel per call (TMA ring + mma.sync tiles; tcgen05 down products at M <= 5)
 PATH_STAGED = 1   # one launch per stage, fp32 CUDA-core arithmetic
 PATH_FUSED_TC = 2  # as PATH_FUSED, with the FP8 lm_head on tcgen05 tensor-memory tiles fed by TMA tensor copies
+PATH_FUSED_MMA = 3  # as PATH_FUSED, with the down products on mma.sync at every M (comparison path)
 
 _PKG = os.path.dirname(os.path.abspath(__file__))
 LIB_PATH = os.path.join(_PKG, "libfgm.so")
@@ -139,7 +140,7 @@ def _check_topk(M: int, x: torch.Tensor, topk_ids: torch.Tensor | None, topk_w: 
 
 
 def select_path(path: int) -> int:
-    """Selects the execution path (PATH_FUSED, PATH_STAGED or PATH_FUSED_TC); returns the previous one."""
+    """Selects the execution path (PATH_FUSED, PATH_STAGED, PATH_FUSED_TC or PATH_FUSED_MMA); returns the previous one."""
     return int(lib().fgm_select_path(int(path)))
 
 

@@ -145,7 +145,8 @@ int launch_fused(fused::Params &prm, cudaStream_t st)
     // the tensor-memory path runs the down phase on tcgen05 (M <= 5, one shared expert)
     // (its bulk copies of row scales want 16-byte aligned scale arrays; else the
     // mma.sync down phase runs)
-    bool tcd = g_path == FGM_PATH_FUSED_TC && prm.M <= 5 && prm.dense.parts == 0 && prm.mode != fused::kModeLmHead;
+    bool tcd = (g_path == FGM_PATH_FUSED || g_path == FGM_PATH_FUSED_TC) && prm.M <= 5 && prm.dense.parts == 0 &&
+               prm.mode != fused::kModeLmHead;
     const int n_tc = prm.mode == fused::kModeLayer ? 1 : prm.n_layers;
     for (int l = 0; tcd && l < n_tc; ++l)
         if (reinterpret_cast<uintptr_t>(prm.layers[l].down_s) & 15u)
@@ -848,7 +849,7 @@ int fgm_verify_step_host(const fgm_layer *layers, int n_layers, const uint16_t *
 int fgm_select_path(int path)
 {
     const int prev = g_path;
-    if (path == FGM_PATH_FUSED || path == FGM_PATH_STAGED || path == FGM_PATH_FUSED_TC)
+    if (path == FGM_PATH_FUSED || path == FGM_PATH_STAGED || path == FGM_PATH_FUSED_TC || path == FGM_PATH_FUSED_MMA)
         g_path = path;
     return prev;
 }

@@ -141,6 +141,7 @@ struct __align__(128) Smem {
     unsigned long long empty[kStages];
     unsigned long long route;
     unsigned long long tfull[2], tempty[2];   // tensor-memory down phase: accumulators full / read
+    unsigned long long bready;                // tensor-memory down phase: second home slot's operand built
     unsigned long long mdone[kStages];        // tensor-memory down phase: products of a ring slot done
     uint32_t tmem_base;
     uint32_t tc_stage, tc_next;   // tensor-memory down phase: ring stages and tile numbers after it
@@ -347,6 +348,10 @@ __device__ __forceinline__ int tc_tile_rows(int pos, int end)
 
 // Named barrier of the MMA warps (the producer never joins).
 __device__ __forceinline__ void consumer_sync() { asm volatile("bar.sync 1, %0;" ::"n"(kConsumers) : "memory"); }
+
+// Named barrier of warps 0..4 and the last MMA warp (the tensor-memory down
+// phase: its first home slot's operand built, warps 5..9 still on the second).
+__device__ __forceinline__ void first_slot_sync() { asm volatile("bar.sync 2, 192;" ::: "memory"); }
 
 __device__ __forceinline__ float4 ldcg4(const float *p) { return __ldcg(reinterpret_cast<const float4 *>(p)); }
 
@@ -1132,6 +1137,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_fused(const __grid_constant__ P
         }
         for (int i = 0; i < kStages; ++i)
             mbar_init(&s.mdone[i], 1);
+        mbar_init(&s.bready, 5);
         s.abort = 0;
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     }
@@ -1330,6 +1336,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_fused(const __grid_constant__ P
         }
     }
     uint32_t tc_tiles = 0;    // tensor-memory down tiles finished by this CTA (barrier phases)
+    uint32_t tc_layers = 0;   // tensor-memory down phases run (phases of s.bready)
     uint32_t mdone_phase = 0; // bit i: phase parity of s.mdone[i] (the issuing thread; one commit, one wait each)
     uint32_t stage = 0;   // ring stages consumed
     unsigned bar_target = 0;
@@ -1588,10 +1595,16 @@ __global__ void __launch_bounds__(kThreads, 1) k_fused(const __grid_constant__ P
         if (l == 0 && p.debug_stall && tid == 0)
             bar_target += 1;   // the next grid barrier can never complete
         if constexpr (TCD) {
-            // the next layer's down-tile counters (last used two layers ago, by
-            // producers that finished before this layer began)
-            if (cta == 0 && tid < kSyncTileStride)
+            // The down-tile counters: at layer 0 this layer's (whatever an earlier
+            // launch left, even one that gave up), and at every layer the next
+            // layer's (last used two layers ago, by producers that finished before
+            // this layer began). The grid barrier after phase A orders these
+            // stores before any tile is taken.
+            if (cta == 0 && tid < kSyncTileStride) {
                 ws.sync[kSyncTileCount + ((l + 1) & 1) * kSyncTileStride + tid] = 0u;
+                if (l == 0)
+                    ws.sync[kSyncTileCount + tid] = 0u;
+            }
         }
         if (l == 0 && p.debug_stall)
             grid_barrier();
@@ -2050,65 +2063,87 @@ __global__ void __launch_bounds__(kThreads, 1) k_fused(const __grid_constant__ P
             const DownStages ds(U + NS, cta, G);
             const int si0 = ds.begin / kH;
             uint8_t *bop = reinterpret_cast<uint8_t *>(&s.red[0][0][0][0]);   // [2][kTcBBytes]: idle exchange buffer
-            // 1. B operands of the (at most two) slots this CTA's rows cover: warp
-            //    t < M polls token t's 704 activations until none is pending, scales
-            //    them by a power of two per (slot, token) and writes kTerms E4M3
-            //    terms as columns 3 t + e (the other columns stay zero)
+            // 1. B operands of the (at most two) home slots this CTA's static range
+            //    touches: warp 5 h2 + t (t < M) polls token t's 704 activations of
+            //    home slot h2 (16-byte loads) until none is pending, scales them by
+            //    a power of two per (slot, token) and writes kTerms E4M3 terms as
+            //    columns 3 t + e (the other columns stay zero). Warps 0..4 and the
+            //    issuing warp meet once the first is built; the second, later
+            //    ready, is announced on s.bready, which the issuing thread waits
+            //    for before the slot's first tile.
             for (int i = tid; i < 2 * kTcBBytes / 16; i += kConsumers)
                 reinterpret_cast<uint4 *>(bop)[i] = make_uint4(0u, 0u, 0u, 0u);
             consumer_sync();
-#pragma unroll 1
-            for (int h2 = 0; h2 < 2; ++h2) {
+            if (warp < 10) {
+                const int h2 = warp < 5 ? 0 : 1;
+                const int t = warp - 5 * h2;
                 const int si = si0 + h2;
                 const bool slot_ok = ds.end > ds.begin && si < U + NS && (h2 == 0 || ds.end > (si0 + 1) * kH);
-                if (!slot_ok || warp >= M)
-                    continue;
-                const int t = warp;
-                const int aslot = si < U ? si : kSharedSlot + si - U;
-                const float *a = act_cur + ((size_t)aslot * kMaxM + t) * kF;
-                float v[kF / 32];
-                for (int it = 0;; ++it) {
-                    bool pending = false;
+                if (slot_ok && t < M) {
+                    const int aslot = si < U ? si : kSharedSlot + si - U;
+                    const float *a = act_cur + ((size_t)aslot * kMaxM + t) * kF;
+                    constexpr int kQ = kF / 4;   // 176 float4 of a row
+                    float4 v[(kQ + 31) / 32];
+                    for (int it = 0;; ++it) {
+                        bool pending = false;
 #pragma unroll
-                    for (int jj = 0; jj < kF / 32; ++jj) {
-                        v[jj] = ld_poll1(a + lane + 32 * jj);
-                        pending |= __float_as_uint(v[jj]) == kActPending;
+                        for (int jj = 0; jj < (kQ + 31) / 32; ++jj) {
+                            const int m = lane + 32 * jj;
+                            v[jj] = m < kQ ? ld_poll4(a + 4 * m) : make_float4(0.0f, 0.0f, 0.0f, 0.0f);
+                            pending |= __float_as_uint(v[jj].x) == kActPending || __float_as_uint(v[jj].y) == kActPending ||
+                                       __float_as_uint(v[jj].z) == kActPending || __float_as_uint(v[jj].w) == kActPending;
+                        }
+                        if (!__any_sync(0xFFFFFFFFu, pending))
+                            break;
+                        if ((it & 15) == 15 && poll_give_up(11, aslot)) {
+#pragma unroll
+                            for (int jj = 0; jj < (kQ + 31) / 32; ++jj)
+                                v[jj] = make_float4(0.0f, 0.0f, 0.0f, 0.0f);
+                            break;
+                        }
                     }
-                    if (!__any_sync(0xFFFFFFFFu, pending))
-                        break;
-                    if ((it & 15) == 15 && poll_give_up(11, aslot)) {
+                    float amax = 0.0f;
 #pragma unroll
-                        for (int jj = 0; jj < kF / 32; ++jj)
-                            v[jj] = 0.0f;
-                        break;
+                    for (int jj = 0; jj < (kQ + 31) / 32; ++jj)
+                        amax = fmaxf(fmaxf(amax, fmaxf(fabsf(v[jj].x), fabsf(v[jj].y))),
+                                     fmaxf(fabsf(v[jj].z), fabsf(v[jj].w)));
+#pragma unroll
+                    for (int o = 16; o > 0; o >>= 1)
+                        amax = fmaxf(amax, __shfl_xor_sync(0xFFFFFFFFu, amax, o));
+                    const float S = term_scale(amax);
+                    if (lane == 0)
+                        s.dscale[h2][t] = S;
+                    uint8_t *b = bop + h2 * kTcBBytes;
+#pragma unroll
+                    for (int jj = 0; jj < (kQ + 31) / 32; ++jj) {
+                        const int m = lane + 32 * jj;
+                        if (m < kQ) {
+                            // four consecutive k: four consecutive bytes of each term column
+                            float y[4] = {v[jj].x * S, v[jj].y * S, v[jj].z * S, v[jj].w * S};
+#pragma unroll
+                            for (int e = 0; e < kTerms; ++e) {
+                                uint32_t packed = 0u;
+#pragma unroll
+                                for (int c = 0; c < 4; ++c) {
+                                    const __nv_fp8_storage_t q8 = __nv_cvt_float_to_fp8(y[c], __NV_SATFINITE, __NV_E4M3);
+                                    packed |= static_cast<uint32_t>(q8) << (8 * c);
+                                    if (e + 1 < kTerms)
+                                        y[c] = (y[c] - __half2float(__half(__nv_cvt_fp8_to_halfraw(q8, __NV_E4M3)))) * 16.0f;
+                                }
+                                *reinterpret_cast<uint32_t *>(b + tc_b_offset(3 * t + e, 4 * m)) = packed;
+                            }
+                        }
                     }
                 }
-                float amax = 0.0f;
-#pragma unroll
-                for (int jj = 0; jj < kF / 32; ++jj)
-                    amax = fmaxf(amax, fabsf(v[jj]));
-#pragma unroll
-                for (int o = 16; o > 0; o >>= 1)
-                    amax = fmaxf(amax, __shfl_xor_sync(0xFFFFFFFFu, amax, o));
-                const float S = term_scale(amax);
-                if (lane == 0)
-                    s.dscale[h2][t] = S;
-                uint8_t *b = bop + h2 * kTcBBytes;
-#pragma unroll
-                for (int jj = 0; jj < kF / 32; ++jj) {
-                    const int k = lane + 32 * jj;
-                    float y = v[jj] * S;
-#pragma unroll
-                    for (int e = 0; e < kTerms; ++e) {
-                        const __nv_fp8_storage_t c = __nv_cvt_float_to_fp8(y, __NV_SATFINITE, __NV_E4M3);
-                        b[tc_b_offset(3 * t + e, k)] = static_cast<uint8_t>(c);
-                        if (e + 1 < kTerms)
-                            y = (y - __half2float(__half(__nv_cvt_fp8_to_halfraw(c, __NV_E4M3)))) * 16.0f;
-                    }
+                asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+                if (h2 == 1) {
+                    __syncwarp();
+                    if (lane == 0)
+                        mbar_arrive(&s.bready);
                 }
             }
-            asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
-            consumer_sync();
+            if (warp < 5 || warp == kMW - 1)
+                first_slot_sync();
             // 2. the tiles, in the order the producer took them (its tile records,
             //    then an end marker): one thread issues the products, warps 0..3
             //    (tensor-memory lanes 32 w .. 32 w + 31) read the accumulators,
@@ -2119,6 +2154,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_fused(const __grid_constant__ P
                 if (lane == 0) {
                     bool ok = *reinterpret_cast<volatile int *>(&s.abort) == 0;
                     bool have_prev = false;   // a stage whose slot is still to be released
+                    bool b1_ready = false;    // the second home slot's operand seen built
                     int prev_slot = 0;
                     uint32_t gt = tc_tiles;
                     s.tc_next = gt;   // (after an abort: where it stopped)
@@ -2139,6 +2175,11 @@ __global__ void __launch_bounds__(kThreads, 1) k_fused(const __grid_constant__ P
                                 break;
                             dstamp(stage, layer_stage0, 1);
                             const int2 inf = s.tinfo[gt % kTcInfo];
+                            if (inf.y == 1 && !b1_ready) {
+                                if (!(ok = mbar_wait(&s.bready, tc_layers & 1, s, deadline, status, 12, (int)gt)))
+                                    break;
+                                b1_ready = true;
+                            }
                             if (inf.x < 0) {
                                 // the end marker's empty stage: its slot back, then the
                                 // epilogue told through this accumulator's barrier
@@ -2228,6 +2269,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_fused(const __grid_constant__ P
             consumer_sync();
             stage = s.tc_stage;
             tc_tiles = s.tc_next;
+            ++tc_layers;
         } else
         {
             const int U = s.n_unique[pb];
@@ -2532,11 +2574,6 @@ __global__ void __launch_bounds__(kThreads, 1) k_fused(const __grid_constant__ P
             p.out[0] = a;
             p.out[1] = arg[a];
         }
-    }
-    if constexpr (TCD) {
-        // both parities of the down-tile counters, for the next launch
-        if (tid < 2 * kSyncTileStride)
-            ws.sync[kSyncTileCount + tid] = 0u;
     }
     if (tid == 0) {
         bar_ctr[1] = 0;

@@ -61,11 +61,13 @@ enum {
 /* Execution paths (fgm_select_path). */
 enum {
     FGM_PATH_FUSED = 0,  /* default: one persistent cooperative kernel per call; weight rows stream
-                            through a TMA-bulk shared-memory ring into FP8/bf16 mma.sync tiles */
+                            through a TMA-bulk shared-memory ring into FP8/bf16 mma.sync tiles, and
+                            at M <= 5 with the shared expert the down products run on tcgen05.mma
+                            (TMA tensor copies, tensor-memory accumulators) */
     FGM_PATH_STAGED = 1, /* one launch per stage with fp32 CUDA-core arithmetic (comparison path) */
-    FGM_PATH_FUSED_TC = 2, /* as FGM_PATH_FUSED, with tcgen05.mma (TMA tensor copies, tensor-memory
-                              accumulators) for the FP8 lm_head and, at M <= 5 with the shared
-                              expert, for the routed and shared down products */
+    FGM_PATH_FUSED_TC = 2, /* as FGM_PATH_FUSED, with the FP8 lm_head on tcgen05.mma as well */
+    FGM_PATH_FUSED_MMA = 3, /* as FGM_PATH_FUSED, with the down products on mma.sync at every M
+                               (comparison path) */
 };
 
 /* Status bits written by kernels into the workspace (fgm_read_status). */
@@ -341,10 +343,10 @@ int fgm_read_status(void *ws, size_t ws_bytes, int clear, int32_t *status, void 
  * (HOST report): {site, block, warp, index}; site 1 = ring slot free
  * (producer), 2 = routing known (producer), 3 = ring data landed, 6 = grid
  * barrier (warp = counter value, index = target), 7 = activation rows of an
- * expert written (index = its slot); FGM_PATH_FUSED_TC's down phase: 8 =
+ * expert written (index = its slot); the tcgen05 down phase: 8 =
  * accumulator read, 9 = products of a ring slot done, 10 = accumulator
- * full, 11 = activation rows written (index = slot). Synchronises the
- * stream. */
+ * full, 11 = activation rows written (index = slot), 12 = second home
+ * slot's operand built. Synchronises the stream. */
 int fgm_read_wait_report(void *ws, size_t ws_bytes, int32_t *report, void *stream);
 
 /* Message describing the last error returned on the calling thread. */

@@ -24,7 +24,7 @@ pytestmark = pytest.mark.gpu
 X_SEED = 1000
 
 
-@pytest.fixture(scope="module", params=[0, 1, 2], ids=["fused", "staged", "fused_tc"])
+@pytest.fixture(scope="module", params=[0, 1, 2, 3], ids=["fused", "staged", "fused_tc", "fused_mma"])
 def fgm(request):
     import fine_grained_moe_gb300 as m
     m.lib()

@@ -35,7 +35,7 @@ M = 5
 N_LAYERS = 30
 
 
-@pytest.fixture(scope="module", params=[0, 1, 2], ids=["fused", "staged", "fused_tc"])
+@pytest.fixture(scope="module", params=[0, 1, 2, 3], ids=["fused", "staged", "fused_tc", "fused_mma"])
 def setup(request):
     import fine_grained_moe_gb300 as fgm
     fgm.lib()
