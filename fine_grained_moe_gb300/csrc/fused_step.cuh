@@ -45,6 +45,8 @@
 
 #include <cuda.h>
 
+#include <type_traits>
+
 #include "common.cuh"
 
 namespace fgm {
@@ -146,6 +148,7 @@ struct __align__(128) Smem {
     uint32_t tmem_base;
     uint32_t tc_stage, tc_next;   // tensor-memory down phase: ring stages and tile numbers after it
     float dscale[2][8];         // tensor-memory down phase: activation-term scale per (slot, token)
+    float tc_amax[8][2];        // tensor-memory down phase: half-row maxima of the first slot per token
     int abort;
     int last;
 };
@@ -348,10 +351,6 @@ __device__ __forceinline__ int tc_tile_rows(int pos, int end)
 
 // Named barrier of the MMA warps (the producer never joins).
 __device__ __forceinline__ void consumer_sync() { asm volatile("bar.sync 1, %0;" ::"n"(kConsumers) : "memory"); }
-
-// Named barrier of warps 0..4 and the last MMA warp (the tensor-memory down
-// phase: its first home slot's operand built, warps 5..9 still on the second).
-__device__ __forceinline__ void first_slot_sync() { asm volatile("bar.sync 2, 192;" ::: "memory"); }
 
 __device__ __forceinline__ float4 ldcg4(const float *p) { return __ldcg(reinterpret_cast<const float4 *>(p)); }
 
@@ -2064,86 +2063,93 @@ __global__ void __launch_bounds__(kThreads, 1) k_fused(const __grid_constant__ P
             const int si0 = ds.begin / kH;
             uint8_t *bop = reinterpret_cast<uint8_t *>(&s.red[0][0][0][0]);   // [2][kTcBBytes]: idle exchange buffer
             // 1. B operands of the (at most two) home slots this CTA's static range
-            //    touches: warp 5 h2 + t (t < M) polls token t's 704 activations of
-            //    home slot h2 (16-byte loads) until none is pending, scales them by
-            //    a power of two per (slot, token) and writes kTerms E4M3 terms as
-            //    columns 3 t + e (the other columns stay zero). Warps 0..4 and the
-            //    issuing warp meet once the first is built; the second, later
-            //    ready, is announced on s.bready, which the issuing thread waits
-            //    for before the slot's first tile.
+            //    touches: token t's 704 activations of a slot are polled (16-byte
+            //    loads) until none is pending, scaled by a power of two per (slot,
+            //    token) and written as kTerms E4M3 terms in columns 3 t + e (the
+            //    other columns stay zero). The first slot's, on which the first
+            //    tile waits, by warps 2 t and 2 t + 1 (half a row each, the scale
+            //    from both halves through shared memory); the second's by warp
+            //    4 + t after all consumers meet, announced on s.bready, which the
+            //    issuing thread waits for before that slot's first tile.
             for (int i = tid; i < 2 * kTcBBytes / 16; i += kConsumers)
                 reinterpret_cast<uint4 *>(bop)[i] = make_uint4(0u, 0u, 0u, 0u);
             consumer_sync();
-            if (warp < 10) {
-                const int h2 = warp < 5 ? 0 : 1;
-                const int t = warp - 5 * h2;
+            constexpr int kQ = kF / 4;   // 176 float4 of a row
+            // polls float4 m0 + lane + 32 jj (jj < NJ, below m1) of token t's row of home
+            // slot h2, then builds those terms under the slot-token scale S
+            auto tc_operand = [&](int h2, int t, int m0, int m1, auto nj, float *half_amax, int pair_bar) {
+                constexpr int NJ = decltype(nj)::value;
                 const int si = si0 + h2;
-                const bool slot_ok = ds.end > ds.begin && si < U + NS && (h2 == 0 || ds.end > (si0 + 1) * kH);
-                if (slot_ok && t < M) {
-                    const int aslot = si < U ? si : kSharedSlot + si - U;
-                    const float *a = act_cur + ((size_t)aslot * kMaxM + t) * kF;
-                    constexpr int kQ = kF / 4;   // 176 float4 of a row
-                    float4 v[(kQ + 31) / 32];
-                    for (int it = 0;; ++it) {
-                        bool pending = false;
+                const int aslot = si < U ? si : kSharedSlot + si - U;
+                const float *a = act_cur + ((size_t)aslot * kMaxM + t) * kF;
+                float4 v[NJ];
+                for (int it = 0;; ++it) {
+                    bool pending = false;
 #pragma unroll
-                        for (int jj = 0; jj < (kQ + 31) / 32; ++jj) {
-                            const int m = lane + 32 * jj;
-                            v[jj] = m < kQ ? ld_poll4(a + 4 * m) : make_float4(0.0f, 0.0f, 0.0f, 0.0f);
-                            pending |= __float_as_uint(v[jj].x) == kActPending || __float_as_uint(v[jj].y) == kActPending ||
-                                       __float_as_uint(v[jj].z) == kActPending || __float_as_uint(v[jj].w) == kActPending;
-                        }
-                        if (!__any_sync(0xFFFFFFFFu, pending))
-                            break;
-                        if ((it & 15) == 15 && poll_give_up(11, aslot)) {
-#pragma unroll
-                            for (int jj = 0; jj < (kQ + 31) / 32; ++jj)
-                                v[jj] = make_float4(0.0f, 0.0f, 0.0f, 0.0f);
-                            break;
-                        }
+                    for (int jj = 0; jj < NJ; ++jj) {
+                        const int m = m0 + lane + 32 * jj;
+                        v[jj] = m < m1 ? ld_poll4(a + 4 * m) : make_float4(0.0f, 0.0f, 0.0f, 0.0f);
+                        pending |= __float_as_uint(v[jj].x) == kActPending || __float_as_uint(v[jj].y) == kActPending ||
+                                   __float_as_uint(v[jj].z) == kActPending || __float_as_uint(v[jj].w) == kActPending;
                     }
-                    float amax = 0.0f;
+                    if (!__any_sync(0xFFFFFFFFu, pending))
+                        break;
+                    if ((it & 15) == 15 && poll_give_up(11, aslot)) {
 #pragma unroll
-                    for (int jj = 0; jj < (kQ + 31) / 32; ++jj)
-                        amax = fmaxf(fmaxf(amax, fmaxf(fabsf(v[jj].x), fabsf(v[jj].y))),
-                                     fmaxf(fabsf(v[jj].z), fabsf(v[jj].w)));
+                        for (int jj = 0; jj < NJ; ++jj)
+                            v[jj] = make_float4(0.0f, 0.0f, 0.0f, 0.0f);
+                        break;
+                    }
+                }
+                float amax = 0.0f;
 #pragma unroll
-                    for (int o = 16; o > 0; o >>= 1)
-                        amax = fmaxf(amax, __shfl_xor_sync(0xFFFFFFFFu, amax, o));
-                    const float S = term_scale(amax);
+                for (int jj = 0; jj < NJ; ++jj)
+                    amax = fmaxf(fmaxf(amax, fmaxf(fabsf(v[jj].x), fabsf(v[jj].y))), fmaxf(fabsf(v[jj].z), fabsf(v[jj].w)));
+#pragma unroll
+                for (int o = 16; o > 0; o >>= 1)
+                    amax = fmaxf(amax, __shfl_xor_sync(0xFFFFFFFFu, amax, o));
+                if (half_amax) {
+                    // the other half's maximum: both warps of the pair meet on their barrier
                     if (lane == 0)
-                        s.dscale[h2][t] = S;
-                    uint8_t *b = bop + h2 * kTcBBytes;
+                        half_amax[m0 == 0 ? 0 : 1] = amax;
+                    asm volatile("bar.sync %0, 64;" ::"r"(pair_bar) : "memory");
+                    amax = fmaxf(half_amax[0], half_amax[1]);
+                }
+                const float S = term_scale(amax);
+                if (lane == 0 && m0 == 0)
+                    s.dscale[h2][t] = S;
+                uint8_t *b = bop + h2 * kTcBBytes;
 #pragma unroll
-                    for (int jj = 0; jj < (kQ + 31) / 32; ++jj) {
-                        const int m = lane + 32 * jj;
-                        if (m < kQ) {
-                            // four consecutive k: four consecutive bytes of each term column
-                            float y[4] = {v[jj].x * S, v[jj].y * S, v[jj].z * S, v[jj].w * S};
+                for (int jj = 0; jj < NJ; ++jj) {
+                    const int m = m0 + lane + 32 * jj;
+                    if (m < m1) {
+                        // four consecutive k: four consecutive bytes of each term column
+                        float y[4] = {v[jj].x * S, v[jj].y * S, v[jj].z * S, v[jj].w * S};
+                        uint32_t w[kTerms];
+                        split_terms4(y, w);
 #pragma unroll
-                            for (int e = 0; e < kTerms; ++e) {
-                                uint32_t packed = 0u;
-#pragma unroll
-                                for (int c = 0; c < 4; ++c) {
-                                    const __nv_fp8_storage_t q8 = __nv_cvt_float_to_fp8(y[c], __NV_SATFINITE, __NV_E4M3);
-                                    packed |= static_cast<uint32_t>(q8) << (8 * c);
-                                    if (e + 1 < kTerms)
-                                        y[c] = (y[c] - __half2float(__half(__nv_cvt_fp8_to_halfraw(q8, __NV_E4M3)))) * 16.0f;
-                                }
-                                *reinterpret_cast<uint32_t *>(b + tc_b_offset(3 * t + e, 4 * m)) = packed;
-                            }
-                        }
+                        for (int e = 0; e < kTerms; ++e)
+                            *reinterpret_cast<uint32_t *>(b + tc_b_offset(3 * t + e, 4 * m)) = w[e];
                     }
                 }
                 asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
-                if (h2 == 1) {
-                    __syncwarp();
-                    if (lane == 0)
-                        mbar_arrive(&s.bready);
-                }
+            };
+            const bool has0 = ds.end > ds.begin;
+            const bool has1 = has0 && ds.end > (si0 + 1) * kH;
+            if (warp < 10 && has0 && (warp >> 1) < M) {
+                const int t = warp >> 1, hf = warp & 1;
+                tc_operand(0, t, hf * (kQ / 2), (hf + 1) * (kQ / 2), std::integral_constant<int, (kQ / 2 + 31) / 32>{},
+                           s.tc_amax[t], 3 + t);
             }
-            if (warp < 5 || warp == kMW - 1)
-                first_slot_sync();
+            consumer_sync();
+            if (warp >= 4 && warp < 9) {
+                const int t = warp - 4;
+                if (has1 && t < M)
+                    tc_operand(1, t, 0, kQ, std::integral_constant<int, (kQ + 31) / 32>{}, nullptr, 0);
+                __syncwarp();
+                if (lane == 0)
+                    mbar_arrive(&s.bready);
+            }
             // 2. the tiles, in the order the producer took them (its tile records,
             //    then an end marker): one thread issues the products, warps 0..3
             //    (tensor-memory lanes 32 w .. 32 w + 31) read the accumulators,
