@@ -1615,11 +1615,14 @@ __global__ void __launch_bounds__(kThreads, 1) k_fused(const __grid_constant__ P
             const bool norm = p.mode != kModeLayer;
             const bool router_cta = cta >= G - kRouterCtas;
             const int e0 = kRouterRows * (cta - (G - kRouterCtas));   // first router row (router CTAs)
-            // only the router CTAs and those hosting a term-split unit read h here;
-            // token t's units sit on CTA G - kRouterCtas - 1 - t, next to the router
-            // CTAs, so that the two jobs run side by side
-            const int term_t = G - kRouterCtas - 1 - cta;
-            const bool need_h = router_cta || (term_t >= 0 && term_t < M);
+            // only the router CTAs and those hosting term-split units read h here;
+            // token t's units sit on CTAs G - kRouterCtas - 1 - 2 t (K-slices 0..5)
+            // and G - kRouterCtas - 2 - 2 t (slices 6..10), next to the router CTAs,
+            // so that the two jobs run side by side and each SM converts about half
+            // a row
+            const int term_c = G - kRouterCtas - 1 - cta;
+            const int term_t = term_c >> 1;
+            const bool need_h = router_cta || (term_c >= 0 && term_t < M);
             // Lane (g, q) holds 64 values of token g in warp w's 256-wide K-slice: fp32
             // rows at positions 256 w + 64 c + 16 k + 4 q + i (v[c][4 k + i]), bf16 rows
             // at 256 w + 64 c + 32 k + 8 q + i (v[c][8 k + i]); the four lanes of a token
@@ -1761,13 +1764,13 @@ __global__ void __launch_bounds__(kThreads, 1) k_fused(const __grid_constant__ P
                     __stcg(ws.logits + t * kE + e0 + j, z * rt + rbias);
                 }
                 // Activation terms of the gate/up products, computed once per grid:
-                // unit (token t, 256-wide K-slice w) is split by warp w of CTA
-                // G - kRouterCtas - 1 - t (it holds the slice in lanes 4 t .. 4 t + 3),
+                // unit (token t, 256-wide K-slice w) is split by warp w of one of
+                // token t's two term CTAs (it holds the slice in lanes 4 t .. 4 t + 3),
                 // 8 values a lane after a pass through shared memory (the exchange
                 // buffer is idle in phase A), into kTerms E4M3 terms under a
                 // power-of-two scale per unit.
                 const int t = term_t;
-                if (t >= 0 && t < M) {
+                if (term_c >= 0 && t < M && (warp < 6) == ((term_c & 1) == 0)) {
                     const int w = warp;
                     const int k0 = 256 * w + 8 * lane;
                     float *sx = reinterpret_cast<float *>(&s.red[0][0][0][0]) + 256 * warp;
