@@ -658,6 +658,70 @@ def run_sweep(args):
     return None
 
 
+def run_verify_dense(args):
+    """The verify step of the model variant whose every layer carries a 2816 x
+    2112 dense MLP in place of the 704-wide shared expert: same 30 routed
+    stacks, inputs and draft recipe (drafts copy this step's own argmax with
+    probability 0.7), MLP seeds 40..69. Returns one JSON line (tokens/s
+    counting accepted drafts + 1 per step, algorithmic HBM GB/s)."""
+    import torch
+
+    import fine_grained_moe_gb300 as fgm
+    import synth
+    from fine_grained_moe_gb300 import traffic
+
+    dev = torch.device("cuda", 0)
+    torch.cuda.set_device(dev)
+    fgm.lib()
+    fgm.select_path(getattr(fgm, PATHS[args.path]))
+    layers, emb, xs = make_workload(dev)
+    mlps = [synth.dense_mlp(40 + l, device=dev) for l in range(N_LAYERS)]
+    arr, mlp_arr = fgm.layers_array(layers), fgm.mlps_array(mlps)
+    ws = fgm.Workspace(dev)
+    uniq, drafts = [], []
+    trace = torch.empty((N_LAYERS, M, 8), dtype=torch.int32, device=dev)
+    for b, x in enumerate(xs):
+        fgm.moe_stack_dense_fwd(layers, mlps, x, ids_trace=trace, ws=ws)
+        tr = trace.cpu()
+        uniq.append([len(torch.unique(tr[l])) for l in range(N_LAYERS)])
+        am = torch.empty(M, dtype=torch.int32, device=dev)
+        fgm.verify_step_dense(layers, mlps, emb, x, torch.zeros(GAMMA, dtype=torch.int32, device=dev), argmax=am,
+                              ws=ws, _arr=arr, _mlp_arr=mlp_arr)
+        drafts.append(synth.drafts(DRAFT_SEED0 + b, am.cpu()).to(dev))
+    nbytes = [traffic.step_bytes(u, dense_width=3 * 704) for u in uniq]
+    K, W = args.steps, args.warmup
+    outs = torch.zeros((K, 2), dtype=torch.int32, device=dev)
+    for i in range(W):
+        b = i % N_BATCHES
+        fgm.verify_step_dense(layers, mlps, emb, xs[b], drafts[b], ws=ws, _arr=arr, _mlp_arr=mlp_arr)
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    with ClockSampler(dev.index) as clk:
+        e0.record()
+        for i in range(K):
+            b = i % N_BATCHES
+            fgm.verify_step_dense(layers, mlps, emb, xs[b], drafts[b], out=outs[i], ws=ws, _arr=arr,
+                                  _mlp_arr=mlp_arr)
+        e1.record()
+        torch.cuda.synchronize()
+    ms = e0.elapsed_time(e1)
+    tokens = int(outs[:, 0].sum().cpu()) + K
+    gbs = sum(nbytes[i % N_BATCHES] for i in range(K)) / (ms * 1e-3) / 1e9
+    peak, kind = measured_peaks()
+    clocks = clk.summary()
+    return {"case": "verify_dense", "path": args.path,
+            "workload": "full verify step, M=5 (gamma=4), Zipf s=1.1, 30 layers each with a 2816x2112 dense "
+                        "MLP in place of the shared expert, 262144x2816 bf16 lm_head",
+            "steps": K, "warmup": W, "tokens_per_s": round(tokens / (ms * 1e-3), 2),
+            "tokens_per_s_at_expected_accept": round(K * (1 + expected_accept(GAMMA)) / (ms * 1e-3), 2),
+            "ms_per_step": round(ms / K, 4), "accepted_per_step": round((tokens - K) / K, 3),
+            "algorithmic_bytes_per_step": int(statistics.mean(nbytes)),
+            "hbm_gbs": round(gbs, 1), "frac_of_peak": round(gbs / peak, 4), "peak": peak, "peak_kind": kind,
+            "clocks": {"sm_mhz": clocks["sm_mhz"], "sm_max_mhz": clocks["sm_max_mhz"],
+                       "reasons": clocks["reasons"]},
+            "status": ws.status()}
+
+
 def run_verify_fp8(args):
     """The headline verify step with the FP8 lm_head in place of the bf16 one:
     same 30-layer stack, inputs and draft recipe (drafts copy the FP8 head's
@@ -803,10 +867,11 @@ def main():
     ap.add_argument("--phase-trace", metavar="PATH", default=None,
                     help="after timing, run one traced step and write a per-phase summary to PATH")
     ap.add_argument("--case", choices=("verify", "layer", "layer_dense", "lm_head", "lm_head_fp8", "verify_fp8",
-                                       "sweep"),
+                                       "verify_dense", "sweep"),
                     default="verify",
                     help="verify: the headline step; layer / layer_dense / lm_head / lm_head_fp8: one stage alone "
-                         "(profiling); verify_fp8: the step with the FP8 lm_head; sweep: the verify step "
+                         "(profiling); verify_fp8: the step with the FP8 lm_head; verify_dense: the step with a "
+                         "2112-wide dense MLP per layer; sweep: the verify step "
                          "over M = 1..8 and Zipf s in {0, 1.1, 2} (one line each)")
     args = ap.parse_args()
     if args.warmup < 3:
@@ -824,6 +889,8 @@ def main():
             line = run_sweep(args)
         elif args.case == "verify_fp8":
             line = run_verify_fp8(args)
+        elif args.case == "verify_dense":
+            line = run_verify_dense(args)
         elif args.case != "verify":
             line = run_case(args)
         else:

@@ -71,6 +71,9 @@ def lib() -> ctypes.CDLL:
             "fgm_moe_layer_fwd_noalloc": (ci, [LP, vp, vp, ci, vp, vp, vp]),
             "fgm_moe_stack_fwd": (ci, [LP, ci, vp, vp, ci, vp, vp, sz, vp]),
             "fgm_moe_layer_dense_fwd": (ci, [LP, ctypes.POINTER(fgm_mlp), vp, vp, ci, vp, vp, vp, sz, vp]),
+            "fgm_moe_stack_dense_fwd": (ci, [LP, ctypes.POINTER(fgm_mlp), ci, vp, vp, ci, vp, vp, sz, vp]),
+            "fgm_verify_step_dense": (ci, [LP, ctypes.POINTER(fgm_mlp), ci, vp, i64, vp, vp, ci, vp, vp, vp, sz,
+                                           vp]),
             "fgm_lm_head_argmax": (ci, [vp, i64, vp, ci, vp, vp, vp, sz, vp]),
             "fgm_lm_head_argmax_fp8": (ci, [vp, vp, i64, vp, ci, vp, vp, vp, sz, vp]),
             "fgm_spec_verify": (ci, [vp, vp, ci, vp, vp]),
@@ -324,6 +327,31 @@ def moe_stack_fwd(layers, x: torch.Tensor, y: torch.Tensor | None = None,
     return y
 
 
+def _mlps_array(mlps, n_layers: int) -> ctypes.Array:
+    if len(mlps) != n_layers:
+        raise FgmError(f"mlps: expected one dense MLP per layer ({n_layers}), got {len(mlps)}")
+    return (fgm_mlp * n_layers)(*[_mlp_struct(m) for m in mlps])
+
+
+def moe_stack_dense_fwd(layers, mlps, x: torch.Tensor, y: torch.Tensor | None = None,
+                        ids_trace: torch.Tensor | None = None, ws: Workspace | None = None,
+                        stream=None) -> torch.Tensor:
+    """The stack with the dense MLP ``mlps[l]`` (dicts as for moe_layer_dense_fwd)
+    in place of layer l's shared expert; returns bf16 h."""
+    M = _m(x)
+    y = torch.empty_like(x) if y is None else y
+    _check_like("y", y, x)
+    if ids_trace is not None and (tuple(ids_trace.shape) != (len(layers), M, TOPK)
+                                  or ids_trace.dtype != torch.int32 or ids_trace.device != x.device):
+        raise FgmError(f"ids_trace: expected int32 [{len(layers)}, {M}, {TOPK}] on {x.device}")
+    ws = _ws(ws, x.device)
+    arr = _layers_array(layers)
+    mlp_arr = _mlps_array(mlps, len(arr))
+    _check(lib().fgm_moe_stack_dense_fwd(arr, mlp_arr, len(arr), _ptr(x), _ptr(y), M, _ptr(ids_trace), ws.ptr,
+                                         ws.nbytes, _stream(stream)))
+    return y
+
+
 def lm_head_argmax(emb: torch.Tensor, h: torch.Tensor, argmax: torch.Tensor | None = None,
                    maxlogit: torch.Tensor | None = None, ws: Workspace | None = None,
                    stream=None) -> torch.Tensor:
@@ -429,6 +457,27 @@ def verify_step(layers, emb: torch.Tensor, x: torch.Tensor, draft: torch.Tensor 
                                  _ptr(draft) if M > 1 else None, M, _ptr(argmax), _ptr(out), ws.ptr,
                                  ws.nbytes, _stream(stream)))
     return out
+
+
+def verify_step_dense(layers, mlps, emb: torch.Tensor, x: torch.Tensor, draft: torch.Tensor | None,
+                      out: torch.Tensor | None = None, argmax: torch.Tensor | None = None,
+                      ws: Workspace | None = None, stream=None, _arr=None, _mlp_arr=None) -> torch.Tensor:
+    """verify_step on the stack with a dense MLP per layer (see moe_stack_dense_fwd);
+    returns int32 [2] = {accepted drafts, next token} on the device."""
+    M = _m(x)
+    out = torch.empty(2, dtype=torch.int32, device=x.device) if out is None else out
+    ws = _ws(ws, x.device)
+    arr = _layers_array(layers) if _arr is None else _arr
+    mlp_arr = _mlps_array(mlps, len(arr)) if _mlp_arr is None else _mlp_arr
+    _check(lib().fgm_verify_step_dense(arr, mlp_arr, len(arr), _ptr(emb), int(emb.shape[0]), _ptr(x),
+                                       _ptr(draft) if M > 1 else None, M, _ptr(argmax), _ptr(out), ws.ptr,
+                                       ws.nbytes, _stream(stream)))
+    return out
+
+
+def mlps_array(mlps):
+    """Pre-marshalled dense MLP table, reusable across calls (pass as ``_mlp_arr``)."""
+    return _mlps_array(mlps, len(mlps))
 
 
 def verify_step_fp8_head(layers, emb_q: torch.Tensor, emb_s: torch.Tensor, x: torch.Tensor,

@@ -135,7 +135,7 @@ int fused_grid()
 }
 
 // Launches the persistent kernel (cooperative: all CTAs co-resident).
-int tc_down_maps(const uint8_t *down_q, CUtensorMap *m128, CUtensorMap *m16);
+int tc_down_map(const uint8_t *down_q, CUtensorMap *map);
 
 int launch_fused(fused::Params &prm, cudaStream_t st)
 {
@@ -145,7 +145,7 @@ int launch_fused(fused::Params &prm, cudaStream_t st)
     // the tensor-memory path runs the down phase on tcgen05 (M <= 5, one shared expert)
     // (its bulk copies of row scales want 16-byte aligned scale arrays; else the
     // mma.sync down phase runs)
-    bool tcd = (g_path == FGM_PATH_FUSED || g_path == FGM_PATH_FUSED_TC) && prm.M <= 5 && prm.dense.parts == 0 &&
+    bool tcd = (g_path == FGM_PATH_FUSED || g_path == FGM_PATH_FUSED_TC) && prm.M <= 5 && prm.dense_parts == 0 &&
                prm.mode != fused::kModeLmHead;
     const int n_tc = prm.mode == fused::kModeLayer ? 1 : prm.n_layers;
     for (int l = 0; tcd && l < n_tc; ++l)
@@ -154,7 +154,7 @@ int launch_fused(fused::Params &prm, cudaStream_t st)
     if (tcd) {
         const int n_l = n_tc;
         for (int l = 0; l < n_l; ++l) {
-            const int rc = tc_down_maps(prm.layers[l].down_q, &prm.dmap[l], &prm.dmap16[l]);
+            const int rc = tc_down_map(prm.layers[l].down_q, &prm.dmap[l]);
             if (rc != FGM_OK)
                 return rc;
         }
@@ -167,8 +167,8 @@ int launch_fused(fused::Params &prm, cudaStream_t st)
     g_debug_stall = 0;
     void *args[] = {&prm};
     // packed activation columns: 2 blocks of 8 hold M <= 5 tokens x 3 terms, 3 blocks M <= 8
-    const bool traced = prm.trace != nullptr && prm.dense.parts == 0;
-    const void *kern = prm.dense.parts == 3
+    const bool traced = prm.trace != nullptr && prm.dense_parts == 0;
+    const void *kern = prm.dense_parts == 3
                            ? (prm.M <= 5 ? reinterpret_cast<const void *>(fused::k_fused<2, false, 3>)
                                          : reinterpret_cast<const void *>(fused::k_fused<3, false, 3>))
                        : tcd ? (traced ? reinterpret_cast<const void *>(fused::k_fused<2, true, 1, true>)
@@ -195,6 +195,26 @@ fused::Params fused_params(int mode, int M, const Ws &w)
 }
 
 bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+// A dense MLP's pointers and width (index: its layer, for the message).
+int check_mlp(const fgm_mlp *m, int index, DenseArgs *out)
+{
+    if (!m)
+        return fail(FGM_ERR_INVALID_ARG, "dense MLP %d is NULL", index);
+    if (m->width < kF || m->width > kMaxDense * kF || m->width % kF)
+        return fail(FGM_ERR_INVALID_ARG, "dense MLP %d width %d: a multiple of %d up to %d", index, m->width, kF,
+                    kMaxDense * kF);
+    const void *q[] = {m->gate_q, m->up_q, m->down_q};
+    const void *sc[] = {m->gate_s, m->up_s, m->down_s};
+    for (int i = 0; i < 3; ++i) {
+        if (!q[i] || !aligned16(q[i]))
+            return fail(FGM_ERR_INVALID_ARG, "dense MLP %d: weight %d NULL or not 16-byte aligned", index, i);
+        if (!sc[i] || (reinterpret_cast<uintptr_t>(sc[i]) & 3u))
+            return fail(FGM_ERR_INVALID_ARG, "dense MLP %d: scale %d NULL or not 4-byte aligned", index, i);
+    }
+    *out = DenseArgs{m->gate_q, m->gate_s, m->up_q, m->up_s, m->down_q, m->down_s, m->width / kF};
+    return FGM_OK;
+}
 
 int check_layer(const fgm_layer *L, int index)
 {
@@ -401,11 +421,11 @@ int run_lmhead_fp8_tc(const uint8_t *emb_q, const float *emb_s, int64_t V, const
 // Tensor maps of one layer's down matrices ([129 * 2816 rows][704 bytes]):
 // 128 x 128-byte and 16 x 128-byte boxes in the 128-byte swizzle, zeros past
 // the 704 bytes of a row. Encoded once per weight address and kept.
-int tc_down_maps(const uint8_t *down_q, CUtensorMap *m128, CUtensorMap *m16)
+int tc_down_map(const uint8_t *down_q, CUtensorMap *map)
 {
     struct Entry {
         const void *ptr;
-        CUtensorMap a, b;
+        CUtensorMap map;
     };
     static Entry cache[2 * FGM_MAX_LAYERS];
     static int n = 0, next = 0;
@@ -413,8 +433,7 @@ int tc_down_maps(const uint8_t *down_q, CUtensorMap *m128, CUtensorMap *m16)
     std::lock_guard<std::mutex> lock(mu);
     for (int i = 0; i < n; ++i)
         if (cache[i].ptr == down_q) {
-            *m128 = cache[i].a;
-            *m16 = cache[i].b;
+            *map = cache[i].map;
             return FGM_OK;
         }
     EncodeTiledFn encode = nullptr;
@@ -424,18 +443,15 @@ int tc_down_maps(const uint8_t *down_q, CUtensorMap *m128, CUtensorMap *m16)
     const cuuint64_t dims[2] = {static_cast<cuuint64_t>(kF), static_cast<cuuint64_t>(kNE) * kH};
     const cuuint64_t strides[1] = {static_cast<cuuint64_t>(kF)};
     const cuuint32_t estr[2] = {1, 1};
-    for (int m = 0; m < 2; ++m) {
-        const cuuint32_t box[2] = {128, m == 0 ? 128u : 16u};
-        const CUresult r = encode(m == 0 ? &e.a : &e.b, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<uint8_t *>(down_q),
-                                  dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
-                                  CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
-        if (r != CUDA_SUCCESS)
-            return fail(FGM_ERR_CUDA, "cuTensorMapEncodeTiled (down matrix) failed (%d)", static_cast<int>(r));
-    }
+    const cuuint32_t box[2] = {128, 128};
+    const CUresult r = encode(&e.map, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<uint8_t *>(down_q), dims, strides,
+                              box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                              CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    if (r != CUDA_SUCCESS)
+        return fail(FGM_ERR_CUDA, "cuTensorMapEncodeTiled (down matrix) failed (%d)", static_cast<int>(r));
     const int slot = n < 2 * FGM_MAX_LAYERS ? n++ : (next++ % (2 * FGM_MAX_LAYERS));
     cache[slot] = e;
-    *m128 = e.a;
-    *m16 = e.b;
+    *map = e.map;
     return FGM_OK;
 }
 
@@ -472,26 +488,47 @@ int run_lmhead_fp8(const uint8_t *emb_q, const float *emb_s, int64_t V, const vo
 
 // The stack on w.h (already holding the input), layer by layer.
 int run_stack(const fgm_layer *layers, int n_layers, int M, const Ws &w, int32_t *ids_trace,
-              cudaStream_t st)
+              cudaStream_t st, const DenseArgs *dns = nullptr)
 {
     for (int l = 0; l < n_layers; ++l) {
         k_rmsnorm<<<M, 256, 0, st>>>(w.h, w.xn, nullptr);
         FGM_CHECK_LAUNCH();
         FGM_TRY(run_layer(M, &layers[l], w, w.h, ids_trace ? ids_trace + (size_t)l * M * kK : nullptr,
-                          nullptr, st));
+                          nullptr, st, dns ? dns[l] : DenseArgs{}));
     }
     return FGM_OK;
 }
 
+// The persistent kernel takes per-layer dense MLPs when all are 2112 wide.
+bool dense_fused(const DenseArgs *dns, int n_layers)
+{
+    if (!dns)
+        return true;
+    for (int l = 0; l < n_layers; ++l)
+        if (dns[l].parts != kMaxDense)
+            return false;
+    return true;
+}
+
+void set_dense(fused::Params &prm, const DenseArgs *dns, int n_layers)
+{
+    if (!dns)
+        return;
+    for (int l = 0; l < n_layers; ++l)
+        prm.dense[l] = dns[l];
+    prm.dense_parts = kMaxDense;
+}
+
 int verify_step_impl(const fgm_layer *layers, int n_layers, const uint16_t *emb, int64_t V,
                      const uint16_t *x, const int32_t *draft, int M, int32_t *argmax, int32_t *out,
-                     void *ws, cudaStream_t st, int sms)
+                     void *ws, cudaStream_t st, int sms, const DenseArgs *dns = nullptr)
 {
     Ws w = ws_carve(ws);
-    if (g_path != FGM_PATH_STAGED) {
+    if (g_path != FGM_PATH_STAGED && dense_fused(dns, n_layers)) {
         fused::Params prm = fused_params(fused::kModeVerify, M, w);
         for (int l = 0; l < n_layers; ++l)
             prm.layers[l] = layers[l];
+        set_dense(prm, dns, n_layers);
         prm.n_layers = n_layers;
         prm.x = x;
         prm.emb = emb;
@@ -503,7 +540,7 @@ int verify_step_impl(const fgm_layer *layers, int n_layers, const uint16_t *emb,
     }
     k_bf16_to_f32<<<8, 256, 0, st>>>(x, M * kH, w.h);
     FGM_CHECK_LAUNCH();
-    FGM_TRY(run_stack(layers, n_layers, M, w, nullptr, st));
+    FGM_TRY(run_stack(layers, n_layers, M, w, nullptr, st, dns));
     k_rmsnorm<<<M, 256, 0, st>>>(w.h, nullptr, w.hb);
     FGM_CHECK_LAUNCH();
     const int G = lmhead_grid(sms);
@@ -570,21 +607,8 @@ int fgm_moe_layer_dense_fwd(const fgm_layer *layer, const fgm_mlp *dense, const 
 {
     FGM_TRY(check_m(M));
     FGM_TRY(check_layer(layer, 0));
-    if (!dense)
-        return fail(FGM_ERR_INVALID_ARG, "dense is NULL");
-    if (dense->width < kF || dense->width > kMaxDense * kF || dense->width % kF)
-        return fail(FGM_ERR_INVALID_ARG, "dense width %d: a multiple of %d up to %d", dense->width, kF,
-                    kMaxDense * kF);
-    {
-        const void *q[] = {dense->gate_q, dense->up_q, dense->down_q};
-        const void *sc[] = {dense->gate_s, dense->up_s, dense->down_s};
-        for (int i = 0; i < 3; ++i) {
-            if (!q[i] || !aligned16(q[i]))
-                return fail(FGM_ERR_INVALID_ARG, "dense weight %d NULL or not 16-byte aligned", i);
-            if (!sc[i] || (reinterpret_cast<uintptr_t>(sc[i]) & 3u))
-                return fail(FGM_ERR_INVALID_ARG, "dense scale %d NULL or not 4-byte aligned", i);
-        }
-    }
+    DenseArgs dn;
+    FGM_TRY(check_mlp(dense, 0, &dn));
     if (!x || !y || !aligned16(x) || !aligned16(y))
         return fail(FGM_ERR_INVALID_ARG, "x/y NULL or not 16-byte aligned");
     if (x == y)
@@ -593,8 +617,6 @@ int fgm_moe_layer_dense_fwd(const fgm_layer *layer, const fgm_mlp *dense, const 
     FGM_TRY(device_ready(nullptr));
     cudaStream_t st = static_cast<cudaStream_t>(stream);
     Ws w = ws_carve(ws);
-    const DenseArgs dn{dense->gate_q, dense->gate_s, dense->up_q, dense->up_s, dense->down_q, dense->down_s,
-                       dense->width / kF};
     if (g_path != FGM_PATH_STAGED && dn.parts == kMaxDense) {
         // the persistent kernel with the MLP's three parts as its always-on slots
         fused::Params prm = fused_params(fused::kModeLayer, M, w);
@@ -604,7 +626,8 @@ int fgm_moe_layer_dense_fwd(const fgm_layer *layer, const fgm_mlp *dense, const 
         prm.y = y;
         prm.ids = topk_ids;
         prm.wts = topk_w;
-        prm.dense = dn;
+        prm.dense[0] = dn;
+        prm.dense_parts = kMaxDense;
         return launch_fused(prm, st);
     }
     k_layer_prep<<<16, 256, 0, st>>>(x, M, w.xn, w.acc);
@@ -615,22 +638,24 @@ int fgm_moe_layer_dense_fwd(const fgm_layer *layer, const fgm_mlp *dense, const 
     return FGM_OK;
 }
 
-int fgm_moe_stack_fwd(const fgm_layer *layers, int n_layers, const uint16_t *x, uint16_t *y, int M,
-                      int32_t *ids_trace, void *ws, size_t ws_bytes, void *stream)
+namespace fgm {
+namespace {
+
+int stack_impl(const fgm_layer *layers, int n_layers, const uint16_t *x, uint16_t *y, int M, int32_t *ids_trace,
+               void *ws, size_t ws_bytes, void *stream, const DenseArgs *dns)
 {
     int sms = 0;
-    FGM_TRY(check_m(M));
-    FGM_TRY(check_layers(layers, n_layers));
     if (!x || !y || !aligned16(x) || !aligned16(y))
         return fail(FGM_ERR_INVALID_ARG, "x/y NULL or not 16-byte aligned");
     FGM_TRY(check_ws(ws, ws_bytes, M, 0));
     FGM_TRY(device_ready(&sms));
     cudaStream_t st = static_cast<cudaStream_t>(stream);
     Ws w = ws_carve(ws);
-    if (g_path != FGM_PATH_STAGED) {
+    if (g_path != FGM_PATH_STAGED && dense_fused(dns, n_layers)) {
         fused::Params prm = fused_params(fused::kModeStack, M, w);
         for (int l = 0; l < n_layers; ++l)
             prm.layers[l] = layers[l];
+        set_dense(prm, dns, n_layers);
         prm.n_layers = n_layers;
         prm.x = x;
         prm.y = y;
@@ -639,10 +664,40 @@ int fgm_moe_stack_fwd(const fgm_layer *layers, int n_layers, const uint16_t *x, 
     }
     k_bf16_to_f32<<<8, 256, 0, st>>>(x, M * kH, w.h);
     FGM_CHECK_LAUNCH();
-    FGM_TRY(run_stack(layers, n_layers, M, w, ids_trace, st));
+    FGM_TRY(run_stack(layers, n_layers, M, w, ids_trace, st, dns));
     k_f32_to_bf16<<<16, 256, 0, st>>>(w.h, M * kH, y);
     FGM_CHECK_LAUNCH();
     return FGM_OK;
+}
+
+int check_mlps(const fgm_mlp *mlps, int n_layers, DenseArgs *out)
+{
+    if (!mlps)
+        return fail(FGM_ERR_INVALID_ARG, "mlps is NULL");
+    for (int l = 0; l < n_layers; ++l)
+        FGM_TRY(check_mlp(&mlps[l], l, &out[l]));
+    return FGM_OK;
+}
+
+}  // namespace
+}  // namespace fgm
+
+int fgm_moe_stack_fwd(const fgm_layer *layers, int n_layers, const uint16_t *x, uint16_t *y, int M,
+                      int32_t *ids_trace, void *ws, size_t ws_bytes, void *stream)
+{
+    FGM_TRY(check_m(M));
+    FGM_TRY(check_layers(layers, n_layers));
+    return stack_impl(layers, n_layers, x, y, M, ids_trace, ws, ws_bytes, stream, nullptr);
+}
+
+int fgm_moe_stack_dense_fwd(const fgm_layer *layers, const fgm_mlp *mlps, int n_layers, const uint16_t *x,
+                            uint16_t *y, int M, int32_t *ids_trace, void *ws, size_t ws_bytes, void *stream)
+{
+    FGM_TRY(check_m(M));
+    FGM_TRY(check_layers(layers, n_layers));
+    DenseArgs dns[FGM_MAX_LAYERS];
+    FGM_TRY(check_mlps(mlps, n_layers, dns));
+    return stack_impl(layers, n_layers, x, y, M, ids_trace, ws, ws_bytes, stream, dns);
 }
 
 int fgm_lm_head_argmax(const uint16_t *emb, int64_t V, const uint16_t *h, int M, int32_t *argmax,
@@ -745,6 +800,24 @@ int fgm_verify_step(const fgm_layer *layers, int n_layers, const uint16_t *emb, 
     FGM_TRY(device_ready(&sms));
     return verify_step_impl(layers, n_layers, emb, V, x, draft, M, argmax, out, ws,
                             static_cast<cudaStream_t>(stream), sms);
+}
+
+int fgm_verify_step_dense(const fgm_layer *layers, const fgm_mlp *mlps, int n_layers, const uint16_t *emb,
+                          int64_t V, const uint16_t *x, const int32_t *draft, int M, int32_t *argmax, int32_t *out,
+                          void *ws, size_t ws_bytes, void *stream)
+{
+    int sms = 0;
+    FGM_TRY(check_m(M));
+    FGM_TRY(check_layers(layers, n_layers));
+    DenseArgs dns[FGM_MAX_LAYERS];
+    FGM_TRY(check_mlps(mlps, n_layers, dns));
+    FGM_TRY(check_vocab(emb, V));
+    if (!x || !aligned16(x) || !out || (M > 1 && !draft))
+        return fail(FGM_ERR_INVALID_ARG, "x/out NULL, x misaligned, or draft NULL with M > 1");
+    FGM_TRY(check_ws(ws, ws_bytes, M, V));
+    FGM_TRY(device_ready(&sms));
+    return verify_step_impl(layers, n_layers, emb, V, x, draft, M, argmax, out, ws,
+                            static_cast<cudaStream_t>(stream), sms, dns);
 }
 
 namespace fgm {

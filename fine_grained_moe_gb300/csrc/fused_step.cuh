@@ -98,11 +98,11 @@ struct Params {
     const float *u_next;    // sampling: [M] uniforms of the emitted sample
     int32_t *ids;           // layer: [M][8]; stack/verify: [L][M][8] trace; optional
     float *wts;             // layer: [M][8]; optional
-    DenseArgs dense;        // layer mode with NS = 3: the always-on dense MLP (its 3 parts)
+    DenseArgs dense[FGM_MAX_LAYERS];   // NS = 3: each layer's always-on dense MLP (its 3 parts)
+    int dense_parts;                   // 3 when the layers carry dense MLPs (NS = 3), else 0
     // tensor-memory down phase: each layer's down_q as [129 * 2816 rows][704 bytes],
-    // 128-byte boxes in the 128-byte swizzle, 128 rows (dmap) and 16 rows (dmap16)
+    // 128 x 128-byte boxes in the 128-byte swizzle
     CUtensorMap dmap[FGM_MAX_LAYERS];
-    CUtensorMap dmap16[FGM_MAX_LAYERS];
     Ws ws;
     long long timeout_ns;
     long long *trace;       // optional: %globaltimer stamps (see kTracePoints)
@@ -1106,7 +1106,7 @@ struct Parts {
 // NB: packed column blocks (2: M <= 5, 3: M <= 8). TRACE: the phase-trace
 // profiling aid is compiled in (a separate instantiation, so that the
 // production kernels carry none of its code). NS: always-on parts per layer
-// (1: the shared expert; 3: a 2112-wide dense MLP, layer mode). TCD: the down
+// (1: the shared expert; 3: a 2112-wide dense MLP in every layer). TCD: the down
 // phase on tcgen05 (NB = 2, NS = 1; tensor maps in Params::dmap).
 template <int NB, bool TRACE, int NS = 1, bool TCD = false>
 __global__ void __launch_bounds__(kThreads, 1) k_fused(const __grid_constant__ Params p)
@@ -1208,7 +1208,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_fused(const __grid_constant__ P
                 int k = 0;
                 for (; cta + k * G < NS * kGuTiles && ok; ++k) {
                     const int x = cta + k * G;
-                    gu_rows(Parts<NS>::gate(L, p.dense, x / kGuTiles), Parts<NS>::up(L, p.dense, x / kGuTiles),
+                    gu_rows(Parts<NS>::gate(L, p.dense[l], x / kGuTiles), Parts<NS>::up(L, p.dense[l], x / kGuTiles),
                             8 * (x % kGuTiles), 8);
                 }
                 if (!ok)
@@ -1239,7 +1239,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_fused(const __grid_constant__ P
                     for (int h2 = 0; h2 < n_home && ok; ++h2) {
                         const int si = hs0 + h2;
                         const int e = si < U ? s.experts[pb][si] : kShared;
-                        const float *dsc = si < U ? L.down_s + (size_t)e * kH : Parts<NS>::down_s(L, p.dense, si - U);
+                        const float *dsc = si < U ? L.down_s + (size_t)e * kH : Parts<NS>::down_s(L, p.dense[l], si - U);
                         for (;;) {
                             const unsigned t = atomicAdd(cnt + si, 1u);
                             if (t >= static_cast<unsigned>(kH / kTcRows))
@@ -1285,14 +1285,14 @@ __global__ void __launch_bounds__(kThreads, 1) k_fused(const __grid_constant__ P
                                 // requests in flight than one 45 KB copy
                                 const uint8_t *src =
                                     slot < U ? L.down_q + ((size_t)s.experts[pb][slot] * kH + row) * kF
-                                             : Parts<NS>::down_row(L, p.dense, 0, row);
+                                             : Parts<NS>::down_row(L, p.dense[l], 0, row);
                                 for (int r4 = 0; r4 < nv; r4 += 4)
                                     bulk_g2s(dst + r4 * kF, src + (size_t)r4 * kF,
                                              static_cast<uint32_t>(min(4, nv - r4)) * kF, &s.full[stage % kStages]);
                             } else {
                                 // a dense part's rows are kF-byte pieces of wider rows
                                 for (int rr = 0; rr < nv; ++rr)
-                                    bulk_g2s(dst + rr * kF, Parts<NS>::down_row(L, p.dense, slot - U, row + rr), kF,
+                                    bulk_g2s(dst + rr * kF, Parts<NS>::down_row(L, p.dense[l], slot - U, row + rr), kF,
                                              &s.full[stage % kStages]);
                             }
                             ++stage;
@@ -1669,8 +1669,8 @@ __global__ void __launch_bounds__(kThreads, 1) k_fused(const __grid_constant__ P
             // the exchange barrier that follows makes them visible to the reducers
             for (int i = tid; i < 8 * n_sh; i += kConsumers) {
                 const int x = cta + (i >> 3) * G, pp = x / kGuTiles, row = 8 * (x % kGuTiles) + (i & 7);
-                cp_async4(&s.sc_g[kMaxGuRows + i], Parts<NS>::gate_s(L, p.dense, pp) + row);
-                cp_async4(&s.sc_u[kMaxGuRows + i], Parts<NS>::up_s(L, p.dense, pp) + row);
+                cp_async4(&s.sc_g[kMaxGuRows + i], Parts<NS>::gate_s(L, p.dense[l], pp) + row);
+                cp_async4(&s.sc_u[kMaxGuRows + i], Parts<NS>::up_s(L, p.dense[l], pp) + row);
             }
             cp_async_commit();
             if (l == 0) {
@@ -1996,7 +1996,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_fused(const __grid_constant__ P
                     const int pos = rd.begin + k;
                     const int si = pos / kH;
                     const float *ds = si < U ? L.down_s + (size_t)s.experts[pb][si] * kH
-                                             : Parts<NS>::down_s(L, p.dense, si - U);
+                                             : Parts<NS>::down_s(L, p.dense[l], si - U);
                     cp_async4(&s.sc_d[k], ds + pos % kH);
                 }
             }

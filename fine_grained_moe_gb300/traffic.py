@@ -53,13 +53,18 @@ def layer_dense_bytes(unique: int, width: int = 3 * FFN, with_bias: bool = True)
 
 
 def step_bytes(unique_per_layer, *, vocab: int = VOCAB, with_lm_head: bool = True,
-               n_shared: int = 1, with_bias: bool = True, fp8_lm_head: bool = False) -> int:
+               n_shared: int = 1, with_bias: bool = True, fp8_lm_head: bool = False,
+               dense_width: int = 0) -> int:
     """Unique bytes of one step: for each layer the router and (unique routed +
-    shared) experts; then the tied embedding once (bf16, or E4M3 with row
-    scales)."""
+    shared) experts, or with ``dense_width`` the unique routed experts and a
+    dense MLP of that width in place of the shared expert; then the tied
+    embedding once (bf16, or E4M3 with row scales)."""
     total = 0
     for u in unique_per_layer:
-        total += (int(u) + n_shared) * expert_bytes() + router_bytes(with_bias=with_bias)
+        if dense_width:
+            total += layer_dense_bytes(u, dense_width, with_bias=with_bias)
+        else:
+            total += (int(u) + n_shared) * expert_bytes() + router_bytes(with_bias=with_bias)
     if with_lm_head:
         total += lm_head_fp8_bytes(vocab) if fp8_lm_head else lm_head_bytes(vocab)
     return total

@@ -190,6 +190,18 @@ int fgm_moe_layer_dense_fwd(const fgm_layer *layer, const fgm_mlp *dense, const 
 int fgm_moe_stack_fwd(const fgm_layer *layers, int n_layers, const uint16_t *x, uint16_t *y,
                       int M, int32_t *ids_trace, void *ws, size_t ws_bytes, void *stream);
 
+/* The stack with an always-on dense MLP in every layer in place of the
+ * shared expert (layer l: h <- h + moe_layer_dense(RMSNorm(h)) with MLP
+ * mlps[l], as fgm_moe_layer_dense_fwd): the model whose byte list has a
+ * 2816 x 2112 dense MLP per layer ("llm-decoding" §"Where the 7.36 GB goes").
+ * When every MLP is 2112 wide the fused paths run it in the persistent
+ * kernel (the MLP's three parts as its always-on slots); otherwise, and on
+ * the staged path, the per-stage kernels.
+ *  mlps   HOST array of n_layers fgm_mlp (device weights)
+ *  other arguments as fgm_moe_stack_fwd */
+int fgm_moe_stack_dense_fwd(const fgm_layer *layers, const fgm_mlp *mlps, int n_layers, const uint16_t *x,
+                            uint16_t *y, int M, int32_t *ids_trace, void *ws, size_t ws_bytes, void *stream);
+
 /* Tied lm_head fused with argmax: z_{t,v} = sum_j emb[v][j] * h[t][j]
  * (fp32 accumulation), argmax over v with ties to the lower index.
  * Source: "llm-decoding" §"The exact architecture" (262,144-word tied
@@ -243,6 +255,12 @@ int fgm_spec_verify(const int32_t *target, const int32_t *draft, int M, int32_t 
 int fgm_verify_step(const fgm_layer *layers, int n_layers, const uint16_t *emb, int64_t V,
                     const uint16_t *x, const int32_t *draft, int M, int32_t *argmax, int32_t *out,
                     void *ws, size_t ws_bytes, void *stream);
+
+/* fgm_verify_step on the stack with a dense MLP per layer (see
+ * fgm_moe_stack_dense_fwd); mlps is a HOST array of n_layers fgm_mlp. */
+int fgm_verify_step_dense(const fgm_layer *layers, const fgm_mlp *mlps, int n_layers, const uint16_t *emb,
+                          int64_t V, const uint16_t *x, const int32_t *draft, int M, int32_t *argmax, int32_t *out,
+                          void *ws, size_t ws_bytes, void *stream);
 
 /* fgm_verify_step with the FP8 lm_head of fgm_lm_head_argmax_fp8 in place of
  * the bf16 one (same stack, final norm and acceptance). Two launches: the

@@ -85,3 +85,19 @@ def test_binding_fails_loudly_without_library(monkeypatch, tmp_path):
     monkeypatch.setattr(fgm, "LIB_PATH", str(tmp_path / "missing.so"))
     with pytest.raises(fgm.FgmError):
         fgm.lib()
+
+
+def test_dense_stack_argument_checks(lib):
+    """The dense stack and verify step reject a missing MLP table and a width
+    that is not a multiple of 704 before any launch."""
+    arr = (fgm.fgm_layer * 1)()
+    buf = (ctypes.c_uint8 * 4096)()
+    assert lib.fgm_moe_stack_dense_fwd(arr, None, 1, buf, buf, 1, None, buf, 4096, None) == -1
+    mlps = (fgm.fgm_mlp * 1)()
+    mlps[0].width = 700
+    # (the layer struct is checked first: fill it with aligned dummies)
+    for name in ("router_w", "gate_q", "gate_s", "up_q", "up_s", "down_q", "down_s"):
+        setattr(arr[0], name, ctypes.addressof(buf))
+    assert lib.fgm_moe_stack_dense_fwd(arr, mlps, 1, buf, buf, 1, None, buf, 4096, None) == -1
+    assert b"width 700" in lib.fgm_last_error()
+    assert lib.fgm_verify_step_dense(arr, None, 1, buf, 16, buf, None, 1, None, buf, buf, 4096, None) == -1

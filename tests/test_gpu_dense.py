@@ -1,11 +1,12 @@
-"""GPU parity of the MoE layer with the always-on 2816 x 2112 dense MLP in
-place of the shared expert ("llm-decoding" §"Where the 7.36 GB goes") against
-the oracle's `fgmo_moe_layer_dense`, at full size: 128 routed experts of the
-benchmark layer (seed 0, Zipf bias) and a 2112-wide E4M3 MLP with fp32 row
-scales in its natural layout (down rows 2112 wide). Same rules as the layer
-test: router ids bit-exact where the oracle's margin exceeds 1e-2 (else a
-valid choice), rows within 1e-2 and elementwise within 2e-2 of the
-bf16-rounded oracle. Both the persistent kernel and the per-stage kernels."""
+"""GPU parity of the MoE layer, the stack and the verify step with the
+always-on 2816 x 2112 dense MLP in place of the shared expert ("llm-decoding"
+§"Where the 7.36 GB goes") against the oracle's `fgmo_moe_layer_dense`, at
+full size: 128 routed experts of the benchmark layers (Zipf bias) and
+2112-wide E4M3 MLPs with fp32 row scales in their natural layout (down rows
+2112 wide). Same rules as the layer test: router ids bit-exact where the
+oracle's margin exceeds 1e-2 (else a valid choice), rows within 1e-2 and
+elementwise within 2e-2 of the bf16-rounded oracle. Both the persistent
+kernel and the per-stage kernels."""
 
 import numpy as np
 import pytest
@@ -13,7 +14,7 @@ import torch
 
 import oracle
 import synth
-from helpers import (ELEM_TOL, MARGIN, REL_TOL, bf16_values, elementwise_rel_err, id_sets_agree,
+from helpers import (ELEM_TOL, MARGIN, REL_TOL, bf16_bits, bf16_values, elementwise_rel_err, id_sets_agree,
                      ids_valid_at_tie, rowwise_rel_err, to_oracle_layer)
 
 pytestmark = pytest.mark.gpu
@@ -99,3 +100,98 @@ def test_dense_width_checked(fgm, case):
            "down_q": d["down_q"][:, :W].contiguous(), "down_s": d["down_s"]}
     with pytest.raises(fgm.FgmError):
         fgm.moe_layer_dense_fwd(p, bad, x)
+
+
+# ------------------------------------------------------------------ stack and verify step
+def _dense_stack_reference(host, mlps_host, h):
+    """The oracle's stack with a dense MLP per layer: h <- h + layer(RMSNorm(h))
+    (the decomposition `test_stack_layer_is_residual_of_normed_layer` pins),
+    each layer the oracle's dense layer. Returns h and the trajectory."""
+    traj = []
+    for L, D in zip(host, mlps_host):
+        out = oracle.moe_layer(L, oracle.rmsnorm(h), dense_shared=D)
+        traj.append((out.ids.copy(), out.margin.copy(), h.copy()))
+        h = h + out.y
+    return h, traj
+
+
+@pytest.mark.parametrize("n_layers,M", [(4, 5), (3, 8)])
+def test_dense_stack_matches_oracle(fgm, n_layers, M):
+    """A stack whose every layer carries a 2112-wide dense MLP in place of the
+    shared expert (the persistent kernel with the MLP parts as always-on
+    slots, or the per-stage kernels), per token against the oracle's stack:
+    routing layer by layer (a first difference only at a near tie), final
+    rows within 1e-2 for tokens that never diverge."""
+    from test_gpu_parity import _compare_stack
+    layers = [synth.layer(l + 1, device="cuda", s=1.1) for l in range(n_layers)]
+    mlps = [synth.dense_mlp(20 + l, device="cuda") for l in range(n_layers)]
+    ws = fgm.Workspace("cuda")
+    x = synth.hidden_states(3300 + M, M, device="cuda")
+    trace = torch.empty((n_layers, M, 8), dtype=torch.int32, device="cuda")
+    y = fgm.moe_stack_dense_fwd(layers, mlps, x, ids_trace=trace, ws=ws)
+    torch.cuda.synchronize()
+    host = [to_oracle_layer(p) for p in layers]
+    mlps_host = [oracle.MlpParams(**{k: v.cpu().numpy() for k, v in d.items()}) for d in mlps]
+    h_ref, traj = _dense_stack_reference(host, mlps_host, bf16_values(x))
+    full = _compare_stack(trace.cpu().numpy(), y, h_ref, traj, host, M)
+    print(f"{n_layers} layers, M={M}: {len(full)} tokens compared to the end")
+    assert len(full) >= 1
+    assert ws.status() == 0
+
+
+@pytest.fixture(scope="module")
+def dense_verify_case():
+    """30 benchmark layers, each with its own 2112-wide dense MLP, the
+    262,144-word embedding, one input batch at M = 5 with drafts that copy the
+    oracle's argmax with probability 0.7; the oracle's trajectory and argmax,
+    one layer's host copy at a time."""
+    n = 30
+    layers = [synth.layer(l + 1, device="cuda", s=1.1) for l in range(n)]
+    mlps = [synth.dense_mlp(40 + l, device="cuda") for l in range(n)]
+    emb = synth.embedding(32, device="cuda")
+    x = synth.hidden_states(3400, 5, device="cuda")
+    h = bf16_values(x)
+    traj, host = [], []
+    for p, d in zip(layers, mlps):
+        L = to_oracle_layer(p)
+        D = oracle.MlpParams(**{k: v.cpu().numpy() for k, v in d.items()})
+        out = oracle.moe_layer(L, oracle.rmsnorm(h), dense_shared=D)
+        traj.append((out.ids.copy(), out.margin.copy(), h.copy()))
+        host.append(L)
+        h = h + out.y
+    hn = oracle.bf16_to_f64(oracle.bf16_round(oracle.rmsnorm(h)))
+    am, _, mg = oracle.lm_head(bf16_bits(emb), hn)
+    draft = synth.drafts(35, am)
+    return dict(layers=layers, mlps=mlps, emb=emb, x=x, h_ref=h, traj=traj, host=host, am=am, mg=mg,
+                draft=draft)
+
+
+def test_dense_verify_step_matches_oracle(fgm, dense_verify_case):
+    """The full verify step (30 layers with dense MLPs, final norm, bf16
+    lm_head, greedy accept): routing per layer, the argmax of every token whose
+    trajectory matched the oracle and whose argmax margin exceeds 1e-2, and the
+    accepted count and next token whenever the oracle's own accepted prefix is
+    comparable."""
+    from test_gpu_parity import _compare_stack
+    c = dense_verify_case
+    M = 5
+    ws = fgm.Workspace("cuda")
+    trace = torch.empty((30, M, 8), dtype=torch.int32, device="cuda")
+    y = fgm.moe_stack_dense_fwd(c["layers"], c["mlps"], c["x"], ids_trace=trace, ws=ws)
+    am = torch.empty(M, dtype=torch.int32, device="cuda")
+    out = fgm.verify_step_dense(c["layers"], c["mlps"], c["emb"], c["x"], c["draft"].cuda(), argmax=am, ws=ws)
+    torch.cuda.synchronize()
+    full = set(_compare_stack(trace.cpu().numpy(), y, c["h_ref"], c["traj"], c["host"], M))
+    ok = [t in full and c["mg"][t] > MARGIN for t in range(M)]
+    gam = am.cpu().numpy()
+    for t in range(M):
+        if ok[t]:
+            assert gam[t] == c["am"][t], (t, gam[t], c["am"][t])
+    a, nxt = out.cpu().tolist()
+    assert (a, nxt) == oracle.spec_verify(gam, c["draft"].numpy())
+    a_ref, nxt_ref = oracle.spec_verify(c["am"], c["draft"].numpy())
+    if all(ok[:a_ref + 1]):
+        assert (a, nxt) == (a_ref, nxt_ref)
+    print(f"dense verify: {len(full)} tokens matched through 30 layers, comparable {ok}, accept {a, nxt}")
+    assert sum(ok) >= 2
+    assert ws.status() == 0

@@ -62,3 +62,14 @@ def test_fp8_lm_head_halves_the_embedding_bytes():
     assert traffic.lm_head_bytes() - b == 262144 * (2816 - 4)
     assert (traffic.step_bytes([20] * 30, fp8_lm_head=True)
             == traffic.step_bytes([20] * 30) - traffic.lm_head_bytes() + b)
+
+
+def test_dense_step_replaces_the_shared_expert_by_the_mlp():
+    # per layer: the distinct routed experts, the 2816 x 2112 MLP (E4M3 + fp32
+    # row scales 2 x 2112 + 2816) and the router; no shared expert
+    mlp = 3 * 2816 * 2112 + 4 * (2 * 2112 + 2816)
+    assert traffic.dense_mlp_bytes() == mlp
+    assert (traffic.step_bytes([20] * 30, dense_width=2112)
+            == 30 * (20 * 5964288 + mlp + 721408) + 1476395008)
+    assert (traffic.step_bytes([20] * 30, dense_width=2112) - traffic.step_bytes([20] * 30)
+            == 30 * (mlp - 5964288))
