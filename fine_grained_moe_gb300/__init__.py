@@ -87,6 +87,7 @@ def lib() -> ctypes.CDLL:
             "fgm_select_path": (ci, [ci]),
             "fgm_set_phase_trace": (ci, [vp, sz]),
             "fgm_debug_stall_next_launch": (ci, []),
+            "fgm_debug_stall_next_launch_at": (ci, [ci]),
             "fgm_read_wait_report": (ci, [vp, sz, vp, vp]),
             "fgm_set_wait_limit_ns": (ctypes.c_longlong, [ctypes.c_longlong]),
             "fgm_last_error": (ctypes.c_char_p, []),
@@ -163,10 +164,14 @@ def set_phase_trace(buf: torch.Tensor | None) -> None:
         _check(lib().fgm_set_phase_trace(_ptr(buf), buf.numel()))
 
 
-def debug_stall_next_launch() -> None:
-    """Test hook: the next persistent-kernel launch waits on a barrier that can
-    never complete, so its wait limit must run out."""
-    _check(lib().fgm_debug_stall_next_launch())
+def debug_stall_next_launch(layer: int = 0) -> None:
+    """Test hook: the next persistent-kernel launch waits, at the start of
+    ``layer``, on a barrier that can never complete, so its wait limit must run
+    out."""
+    if layer == 0:
+        _check(lib().fgm_debug_stall_next_launch())
+    else:
+        _check(lib().fgm_debug_stall_next_launch_at(int(layer)))
 
 
 def workspace_bytes(M: int = MAX_M, V: int = 0) -> int:

@@ -933,6 +933,14 @@ int fgm_debug_stall_next_launch(void)
     return FGM_OK;
 }
 
+int fgm_debug_stall_next_launch_at(int layer)
+{
+    if (layer < 0 || layer >= FGM_MAX_LAYERS)
+        return fail(FGM_ERR_INVALID_ARG, "layer %d outside [0, %d)", layer, FGM_MAX_LAYERS);
+    g_debug_stall = layer + 1;
+    return FGM_OK;
+}
+
 int fgm_set_phase_trace(long long *buf, size_t n)
 {
     g_trace = buf;

@@ -106,7 +106,8 @@ struct Params {
     Ws ws;
     long long timeout_ns;
     long long *trace;       // optional: %globaltimer stamps (see kTracePoints)
-    int debug_stall;        // test hook: add one grid barrier that can never complete
+    int debug_stall;        // test hook: 1 + the layer that adds one grid barrier that can never
+                            // complete (0: none)
 };
 
 // Profiling aid (Params::trace): per layer kTracePoints phase stamps for every
@@ -1591,7 +1592,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_fused(const __grid_constant__ P
         if (detail && tid == 0)
             detail[((size_t)l * kTraceStages) * kTraceDetail + 7] = clock64();
         stamp(0);
-        if (l == 0 && p.debug_stall && tid == 0)
+        if (p.debug_stall == l + 1 && tid == 0)
             bar_target += 1;   // the next grid barrier can never complete
         if constexpr (TCD) {
             // The down-tile counters: at layer 0 this layer's (whatever an earlier
@@ -1605,7 +1606,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_fused(const __grid_constant__ P
                     ws.sync[kSyncTileCount + tid] = 0u;
             }
         }
-        if (l == 0 && p.debug_stall)
+        if (p.debug_stall == l + 1)
             grid_barrier();
         // -------------------------------------------------------- phase A
         // this CTA's always-on tiles: list indices cta, cta + G, ... below NS * kGuTiles

@@ -353,6 +353,11 @@ int fgm_set_phase_trace(long long *buf, size_t n);
  * raise FGM_STATUS_WAIT_TIMEOUT and let the kernel exit (outputs invalid). */
 int fgm_debug_stall_next_launch(void);
 
+/* The same at the start of the given layer of the next persistent-kernel
+ * launch (layers before it run normally, their down-tile counters and
+ * activation markers left as an interrupted call leaves them). */
+int fgm_debug_stall_next_launch_at(int layer);
+
 /* Reads the status word of a workspace (synchronises the stream) and, if
  * `clear`, resets it. */
 int fgm_read_status(void *ws, size_t ws_bytes, int clear, int32_t *status, void *stream);
