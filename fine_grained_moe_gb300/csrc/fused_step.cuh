@@ -145,7 +145,7 @@ struct __align__(128) Smem {
     unsigned long long route;
     unsigned long long tfull[2], tempty[2];   // tensor-memory down phase: accumulators full / read
     unsigned long long bready;                // tensor-memory down phase: second home slot's operand built
-    unsigned long long mdone[kStages];        // tensor-memory down phase: products of a ring slot done
+    unsigned long long mdone;                 // tensor-memory down phase: every product issued done
     uint32_t tmem_base;
     uint32_t tc_stage, tc_next;   // tensor-memory down phase: ring stages and tile numbers after it
     float dscale[2][8];         // tensor-memory down phase: activation-term scale per (slot, token)
@@ -1135,8 +1135,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_fused(const __grid_constant__ P
             mbar_init(&s.tfull[i], 1);
             mbar_init(&s.tempty[i], 4);
         }
-        for (int i = 0; i < kStages; ++i)
-            mbar_init(&s.mdone[i], 1);
+        mbar_init(&s.mdone, 1);
         mbar_init(&s.bready, 5);
         s.abort = 0;
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
@@ -1337,7 +1336,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_fused(const __grid_constant__ P
     }
     uint32_t tc_tiles = 0;    // tensor-memory down tiles finished by this CTA (barrier phases)
     uint32_t tc_layers = 0;   // tensor-memory down phases run (phases of s.bready)
-    uint32_t mdone_phase = 0; // bit i: phase parity of s.mdone[i] (the issuing thread; one commit, one wait each)
+    uint32_t mdone_phase = 0; // phase parity of s.mdone (the issuing thread: one commit, one wait per phase)
     uint32_t stage = 0;   // ring stages consumed
     unsigned bar_target = 0;
     unsigned *bar_ctr = ws.sync;
@@ -2163,9 +2162,8 @@ __global__ void __launch_bounds__(kThreads, 1) k_fused(const __grid_constant__ P
             if (warp == kMW - 1) {
                 if (lane == 0) {
                     bool ok = *reinterpret_cast<volatile int *>(&s.abort) == 0;
-                    bool have_prev = false;   // a stage whose slot is still to be released
+                    bool issued = false;      // products issued in this phase
                     bool b1_ready = false;    // the second home slot's operand seen built
-                    int prev_slot = 0;
                     uint32_t gt = tc_tiles;
                     s.tc_next = gt;   // (after an abort: where it stopped)
                     for (; ok; ++gt) {
@@ -2200,30 +2198,27 @@ __global__ void __launch_bounds__(kThreads, 1) k_fused(const __grid_constant__ P
                                 break;
                             }
                             tc_fence_after();
-                            const uint32_t b0 = su32(bop + inf.y * kTcBBytes);
-                            const uint32_t a0 = su32(s.ring[slot]);
+                            // descriptors of the stage's first A and B blocks; the others
+                            // differ in the start address field only (shared-memory
+                            // addresses stay below 2^18 bytes, so the field never carries)
+                            const uint64_t bdesc = tc_desc_nosw(su32(bop + inf.y * kTcBBytes));
+                            const uint64_t adesc = tc_desc_sw128(su32(s.ring[slot]));
 #pragma unroll
                             for (int b = 0; b < 2; ++b)
 #pragma unroll
                                 for (int kk = 0; kk < 4; ++kk) {
                                     const int kg = 256 * ks + 128 * b + 32 * kk;
                                     if (kg < kF)
-                                        tc_mma(d, tc_desc_sw128(a0 + b * kTcBoxBytes + kk * 32), tc_desc_nosw(b0 + kg * 16),
-                                               kg > 0);
+                                        tc_mma(d, adesc + static_cast<uint64_t>((b * kTcBoxBytes + kk * 32) >> 4),
+                                               bdesc + static_cast<uint64_t>((kg * 16) >> 4), kg > 0);
                                 }
-                            // this slot is released once its products are done: the
-                            // previous stage's slot is released here, after this
-                            // stage's products are issued
-                            tc_commit(&s.mdone[slot]);
+                            // the slot goes back to the producer when its products are
+                            // done: kMW - 1 of its arrivals now, the last one the commit's
+                            // (the issuing thread does not wait)
+                            tc_commit(&s.empty[slot]);
+                            mbar_arrive_n(&s.empty[slot], kMW - 1);
+                            issued = true;
                             dstamp(stage, layer_stage0, 2);
-                            if (have_prev) {
-                                ok = mbar_wait(&s.mdone[prev_slot], (mdone_phase >> prev_slot) & 1u, s, deadline,
-                                               status, 9, (int)stage);
-                                mdone_phase ^= 1u << prev_slot;
-                                mbar_arrive_n(&s.empty[prev_slot], kMW);
-                            }
-                            have_prev = true;
-                            prev_slot = slot;
                             dstamp(stage, layer_stage0, 3);
                             ++stage;
                         }
@@ -2234,12 +2229,15 @@ __global__ void __launch_bounds__(kThreads, 1) k_fused(const __grid_constant__ P
                         if (ok)
                             tc_commit(&s.tfull[buf]);
                     }
-                    // the last stage's slot, once its products are done (also after an
-                    // abort: nothing may be in flight when tensor memory is released)
-                    if (have_prev) {
-                        mbar_wait(&s.mdone[prev_slot], (mdone_phase >> prev_slot) & 1u, s, deadline, status, 9, -1);
-                        mdone_phase ^= 1u << prev_slot;
-                        mbar_arrive_n(&s.empty[prev_slot], kMW);
+                    // every product issued is done before the phase ends (also after
+                    // an abort: nothing may be in flight when tensor memory is
+                    // released); products always finish, so the wait only counts tries
+                    if (issued) {
+                        tc_commit(&s.mdone);
+                        for (int it = 0; it < (1 << 22); ++it)
+                            if (mbar_try(&s.mdone, mdone_phase))
+                                break;
+                        mdone_phase ^= 1u;
                     }
                     s.tc_stage = stage;
                 }
@@ -2394,7 +2392,8 @@ __global__ void __launch_bounds__(kThreads, 1) k_fused(const __grid_constant__ P
         grid_barrier();
     }
     if constexpr (TCD) {
-        // every product has completed (each stage's commit was waited for)
+        // every product has completed (the issuing thread waited for a commit
+        // after its last products of each phase)
         consumer_sync();
         if (warp == 0) {
             tc_fence_after();
