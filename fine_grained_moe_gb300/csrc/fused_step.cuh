@@ -338,6 +338,35 @@ __device__ __forceinline__ void mbar_arrive_n(unsigned long long *b, uint32_t n)
     asm volatile("mbarrier.arrive.shared.b64 _, [%0], %1;" ::"r"(su32(b)), "r"(n) : "memory");
 }
 
+// Warp-wide forms for the issuing warp: every lane executes them with the
+// same operands and one elected lane (the same one each time: the lowest)
+// acts, so no lane branches off around the tensor-core instructions.
+__device__ __forceinline__ void tc_mma_elect(uint32_t d, uint64_t a, uint64_t b, uint32_t accumulate)
+{
+    asm volatile(
+        "{\n\t.reg .pred p, e;\n\tsetp.ne.u32 p, %4, 0;\n\telect.sync _|e, 0xffffffff;\n\t"
+        "@e tcgen05.mma.cta_group::1.kind::f8f6f4 [%0], %1, %2, %3, p;\n\t}" ::"r"(d),
+        "l"(a), "l"(b), "r"(kTcIdesc), "r"(accumulate)
+        : "memory");
+}
+
+__device__ __forceinline__ void tc_commit_elect(unsigned long long *bar)
+{
+    asm volatile(
+        "{\n\t.reg .pred e;\n\telect.sync _|e, 0xffffffff;\n\t"
+        "@e tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];\n\t}" ::"r"(su32(bar))
+        : "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive_n_elect(unsigned long long *b, uint32_t n)
+{
+    asm volatile(
+        "{\n\t.reg .pred e;\n\telect.sync _|e, 0xffffffff;\n\t@e mbarrier.arrive.shared.b64 _, [%0], %1;\n\t}" ::"r"(
+            su32(b)),
+        "r"(n)
+        : "memory");
+}
+
 // A down tile of the tensor-memory phase: rows [pos, pos + nr) of the CTA's
 // flattened (slot, row) range, within one slot and at most 128 rows. Each
 // slot's part of the range starts with its remainder (length mod 128), then
@@ -2160,87 +2189,99 @@ __global__ void __launch_bounds__(kThreads, 1) k_fused(const __grid_constant__ P
             //    stream. The issuing thread publishes the stage and tile counts
             //    after the phase (the tile count is known only to it).
             if (warp == kMW - 1) {
-                if (lane == 0) {
-                    bool ok = *reinterpret_cast<volatile int *>(&s.abort) == 0;
-                    bool issued = false;      // products issued in this phase
-                    bool b1_ready = false;    // the second home slot's operand seen built
-                    uint32_t gt = tc_tiles;
+                // the whole warp runs the issuing loop and one elected lane issues
+                // (measured a little faster than one lane's loop, 0.3 % per step);
+                // waits agree across lanes through lane 0
+                auto wait_all = [&](unsigned long long *b, uint32_t parity, int site, int index) -> bool {
+                    const bool r = mbar_wait(b, parity, s, deadline, status, site, index);
+                    return __shfl_sync(0xFFFFFFFFu, r ? 1 : 0, 0) != 0;
+                };
+                bool ok = __shfl_sync(0xFFFFFFFFu, *reinterpret_cast<volatile int *>(&s.abort) == 0 ? 1 : 0, 0) != 0;
+                bool issued = false;      // products issued in this phase
+                bool b1_ready = false;    // the second home slot's operand seen built
+                uint32_t gt = tc_tiles;
+                if (lane == 0)
                     s.tc_next = gt;   // (after an abort: where it stopped)
-                    for (; ok; ++gt) {
-                        const int buf = gt & 1;
-                        // the epilogue has read this accumulator two tiles ago
-                        if (gt >= 2 && !(ok = mbar_wait(&s.tempty[buf], ((gt >> 1) - 1) & 1, s, deadline, status, 8,
-                                                        (int)gt)))
-                            break;
-                        tc_fence_after();
-                        const uint32_t d = s.tmem_base + static_cast<uint32_t>(buf * kTcN);
-                        bool end_marker = false;
-                        for (int ks = 0; ks < kTcStagesPerTile && ok; ++ks) {
-                            const int slot = stage % kStages;
+                __syncwarp();
+                for (; ok; ++gt) {
+                    const int buf = gt & 1;
+                    // the epilogue has read this accumulator two tiles ago
+                    if (gt >= 2 && !(ok = wait_all(&s.tempty[buf], ((gt >> 1) - 1) & 1, 8, (int)gt)))
+                        break;
+                    tc_fence_after();
+                    const uint32_t d = s.tmem_base + static_cast<uint32_t>(buf * kTcN);
+                    bool end_marker = false;
+                    for (int ks = 0; ks < kTcStagesPerTile && ok; ++ks) {
+                        const int slot = stage % kStages;
+                        if (lane == 0)
                             dstamp(stage, layer_stage0, 5);
-                            if (!(ok = mbar_wait(&s.full[slot], (stage / kStages) & 1, s, deadline, status, 3,
-                                                 (int)stage)))
-                                break;
+                        if (!(ok = wait_all(&s.full[slot], (stage / kStages) & 1, 3, (int)stage)))
+                            break;
+                        if (lane == 0)
                             dstamp(stage, layer_stage0, 1);
-                            const int2 inf = s.tinfo[gt % kTcInfo];
-                            if (inf.y == 1 && !b1_ready) {
-                                if (!(ok = mbar_wait(&s.bready, tc_layers & 1, s, deadline, status, 12, (int)gt)))
-                                    break;
-                                b1_ready = true;
-                            }
-                            if (inf.x < 0) {
-                                // the end marker's empty stage: its slot back, then the
-                                // epilogue told through this accumulator's barrier
-                                mbar_arrive_n(&s.empty[slot], kMW);
-                                ++stage;
-                                mbar_arrive(&s.tfull[buf]);
-                                end_marker = true;
+                        const int2 inf = s.tinfo[gt % kTcInfo];
+                        if (inf.y == 1 && !b1_ready) {
+                            if (!(ok = wait_all(&s.bready, tc_layers & 1, 12, (int)gt)))
                                 break;
+                            b1_ready = true;
+                        }
+                        if (inf.x < 0) {
+                            // the end marker's empty stage: its slot back, then the
+                            // epilogue told through this accumulator's barrier
+                            mbar_arrive_n_elect(&s.empty[slot], kMW);
+                            ++stage;
+                            mbar_arrive_n_elect(&s.tfull[buf], 1);
+                            end_marker = true;
+                            break;
+                        }
+                        tc_fence_after();
+                        // descriptors of the stage's first A and B blocks; the others
+                        // differ in the start address field only (shared-memory
+                        // addresses stay below 2^18 bytes, so the field never carries)
+                        const uint64_t bdesc = __shfl_sync(0xFFFFFFFFu, tc_desc_nosw(su32(bop + inf.y * kTcBBytes)), 0);
+                        const uint64_t adesc = __shfl_sync(0xFFFFFFFFu, tc_desc_sw128(su32(s.ring[slot])), 0);
+                        const uint32_t du = __shfl_sync(0xFFFFFFFFu, d, 0);
+#pragma unroll
+                        for (int b = 0; b < 2; ++b)
+#pragma unroll
+                            for (int kk = 0; kk < 4; ++kk) {
+                                const int kg = 256 * ks + 128 * b + 32 * kk;
+                                if (kg < kF)
+                                    tc_mma_elect(du, adesc + static_cast<uint64_t>((b * kTcBoxBytes + kk * 32) >> 4),
+                                                 bdesc + static_cast<uint64_t>((kg * 16) >> 4), kg > 0);
                             }
-                            tc_fence_after();
-                            // descriptors of the stage's first A and B blocks; the others
-                            // differ in the start address field only (shared-memory
-                            // addresses stay below 2^18 bytes, so the field never carries)
-                            const uint64_t bdesc = tc_desc_nosw(su32(bop + inf.y * kTcBBytes));
-                            const uint64_t adesc = tc_desc_sw128(su32(s.ring[slot]));
-#pragma unroll
-                            for (int b = 0; b < 2; ++b)
-#pragma unroll
-                                for (int kk = 0; kk < 4; ++kk) {
-                                    const int kg = 256 * ks + 128 * b + 32 * kk;
-                                    if (kg < kF)
-                                        tc_mma(d, adesc + static_cast<uint64_t>((b * kTcBoxBytes + kk * 32) >> 4),
-                                               bdesc + static_cast<uint64_t>((kg * 16) >> 4), kg > 0);
-                                }
-                            // the slot goes back to the producer when its products are
-                            // done: kMW - 1 of its arrivals now, the last one the commit's
-                            // (the issuing thread does not wait)
-                            tc_commit(&s.empty[slot]);
-                            mbar_arrive_n(&s.empty[slot], kMW - 1);
-                            issued = true;
+                        // the slot goes back to the producer when its products are
+                        // done: kMW - 1 of its arrivals now, the last one the commit's
+                        // (the issuing warp does not wait)
+                        tc_commit_elect(&s.empty[slot]);
+                        mbar_arrive_n_elect(&s.empty[slot], kMW - 1);
+                        issued = true;
+                        if (lane == 0) {
                             dstamp(stage, layer_stage0, 2);
                             dstamp(stage, layer_stage0, 3);
-                            ++stage;
                         }
-                        if (end_marker) {
+                        ++stage;
+                    }
+                    if (end_marker) {
+                        if (lane == 0)
                             s.tc_next = gt + 1;
-                            break;
-                        }
-                        if (ok)
-                            tc_commit(&s.tfull[buf]);
+                        break;
                     }
-                    // every product issued is done before the phase ends (also after
-                    // an abort: nothing may be in flight when tensor memory is
-                    // released); products always finish, so the wait only counts tries
-                    if (issued) {
-                        tc_commit(&s.mdone);
-                        for (int it = 0; it < (1 << 22); ++it)
-                            if (mbar_try(&s.mdone, mdone_phase))
-                                break;
-                        mdone_phase ^= 1u;
-                    }
-                    s.tc_stage = stage;
+                    if (ok)
+                        tc_commit_elect(&s.tfull[buf]);
                 }
+                // every product issued is done before the phase ends (also after
+                // an abort: nothing may be in flight when tensor memory is
+                // released); products always finish, so the wait only counts tries
+                if (issued) {
+                    tc_commit_elect(&s.mdone);
+                    for (int it = 0; it < (1 << 22); ++it)
+                        if (__shfl_sync(0xFFFFFFFFu, mbar_try(&s.mdone, mdone_phase) ? 1 : 0, 0))
+                            break;
+                    mdone_phase ^= 1u;
+                }
+                if (lane == 0)
+                    s.tc_stage = stage;
                 __syncwarp();
             } else if (warp < 4) {
                 for (uint32_t gt = tc_tiles;; ++gt) {
