@@ -256,6 +256,26 @@ __device__ __forceinline__ void bulk_g2s(void *dst, const void *src, uint32_t by
         : "memory");
 }
 
+// L2 policy for data read once per step (the weight streams): evicted first,
+// so that the small data the layers re-read (activations, the residual, the
+// next layer's router rows) stays in L2.
+__device__ __forceinline__ uint64_t l2_evict_first()
+{
+    uint64_t pol;
+    asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(pol));
+    return pol;
+}
+
+__device__ __forceinline__ void bulk_g2s_stream(void *dst, const void *src, uint32_t bytes, unsigned long long *bar,
+                                                uint64_t pol)
+{
+    asm volatile(
+        "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes.L2::cache_hint [%0], [%1], %2, [%3], %4;" ::"r"(
+            su32(dst)),
+        "l"(src), "r"(bytes), "r"(su32(bar)), "l"(pol)
+        : "memory");
+}
+
 // ---------------------------------------------------------------- tcgen05
 // The tensor-memory down phase (TCD): weights by TMA tensor copies into the
 // ring, activations as E4M3 terms in shared memory, full-K accumulators in
@@ -324,12 +344,13 @@ __device__ __forceinline__ void tc_ld16(uint32_t taddr, float (&v)[16])
         v[i] = __uint_as_float(r[i]);
 }
 
-__device__ __forceinline__ void tma_2d(uint32_t dst, const CUtensorMap *map, int x, int y, unsigned long long *bar)
+__device__ __forceinline__ void tma_2d(uint32_t dst, const CUtensorMap *map, int x, int y, unsigned long long *bar,
+                                       uint64_t pol)
 {
     asm volatile(
-        "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3}], [%4];" ::"r"(
-            dst),
-        "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(su32(bar))
+        "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes.L2::cache_hint [%0], [%1, {%2, %3}], "
+        "[%4], %5;" ::"r"(dst),
+        "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(su32(bar)), "l"(pol)
         : "memory");
 }
 
@@ -1178,6 +1199,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_fused(const __grid_constant__ P
         if (lane == 0) {
             uint32_t stage = 0;
             bool ok = true;
+            const uint64_t pol = l2_evict_first();
             long long *pdetail = (TRACE && p.trace && cta == G / 2)
                                      ? p.trace + (size_t)(n_layers * kTracePoints + 2) * G : nullptr;
             int p_layer = 0;
@@ -1203,8 +1225,9 @@ __global__ void __launch_bounds__(kThreads, 1) k_fused(const __grid_constant__ P
                 const uint8_t *gsrc = gbase + (size_t)i * kH;
                 const uint8_t *usrc = ubase + (size_t)i * kH;
                 for (int rr = 0; rr < nv; ++rr) {
-                    bulk_g2s(dst + rr * kRowStride, gsrc + (size_t)rr * kH, kH, &s.full[stage % kStages]);
-                    bulk_g2s(dst + (8 + rr) * kRowStride, usrc + (size_t)rr * kH, kH, &s.full[stage % kStages]);
+                    bulk_g2s_stream(dst + rr * kRowStride, gsrc + (size_t)rr * kH, kH, &s.full[stage % kStages], pol);
+                    bulk_g2s_stream(dst + (8 + rr) * kRowStride, usrc + (size_t)rr * kH, kH, &s.full[stage % kStages],
+                                    pol);
                 }
                 ++stage;
             };
@@ -1286,7 +1309,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_fused(const __grid_constant__ P
                                     bulk_g2s(sc, dsc + row, kTcRows * 4u, &s.full[stage % kStages]);
                                 for (int b = 0; b < 2; ++b)
                                     tma_2d(d0 + b * kTcBoxBytes, &p.dmap[l], 256 * ks + 128 * b, e * kH + row,
-                                           &s.full[stage % kStages]);
+                                           &s.full[stage % kStages], pol);
                                 ++stage;
                             }
                             if (!ok)
@@ -1316,13 +1339,14 @@ __global__ void __launch_bounds__(kThreads, 1) k_fused(const __grid_constant__ P
                                     slot < U ? L.down_q + ((size_t)s.experts[pb][slot] * kH + row) * kF
                                              : Parts<NS>::down_row(L, p.dense[l], 0, row);
                                 for (int r4 = 0; r4 < nv; r4 += 4)
-                                    bulk_g2s(dst + r4 * kF, src + (size_t)r4 * kF,
-                                             static_cast<uint32_t>(min(4, nv - r4)) * kF, &s.full[stage % kStages]);
+                                    bulk_g2s_stream(dst + r4 * kF, src + (size_t)r4 * kF,
+                                                    static_cast<uint32_t>(min(4, nv - r4)) * kF, &s.full[stage % kStages],
+                                                    pol);
                             } else {
                                 // a dense part's rows are kF-byte pieces of wider rows
                                 for (int rr = 0; rr < nv; ++rr)
-                                    bulk_g2s(dst + rr * kF, Parts<NS>::down_row(L, p.dense[l], slot - U, row + rr), kF,
-                                             &s.full[stage % kStages]);
+                                    bulk_g2s_stream(dst + rr * kF, Parts<NS>::down_row(L, p.dense[l], slot - U, row + rr),
+                                                    kF, &s.full[stage % kStages], pol);
                             }
                             ++stage;
                         }
@@ -1338,7 +1362,8 @@ __global__ void __launch_bounds__(kThreads, 1) k_fused(const __grid_constant__ P
                             break;
                         const uint8_t *src = reinterpret_cast<const uint8_t *>(p.emb + (size_t)v0 * kH) + half * kH;
                         for (int rr = 0; rr < nv; ++rr)
-                            bulk_g2s(dst + rr * kRowStride, src + (size_t)rr * 2 * kH, kH, &s.full[stage % kStages]);
+                            bulk_g2s_stream(dst + rr * kRowStride, src + (size_t)rr * 2 * kH, kH, &s.full[stage % kStages],
+                                            pol);
                         ++stage;
                     }
                 }
