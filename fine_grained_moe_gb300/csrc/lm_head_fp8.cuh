@@ -72,10 +72,15 @@ __device__ __forceinline__ uint32_t smem_u32(const void *p)
     return static_cast<uint32_t>(__cvta_generic_to_shared(p));
 }
 
-// 16 bytes global -> shared, bypassing L1; L2 fetches the surrounding 256 bytes.
+// 16 bytes global -> shared, bypassing L1; L2 fetches the surrounding 256 bytes
+// and marks them evict-first: the rows are read once per step, and the small
+// data that the next launch reads again stays in L2.
 __device__ __forceinline__ void cp_async16(uint32_t dst, const uint8_t *src)
 {
-    asm volatile("cp.async.cg.shared.global.L2::256B [%0], [%1], 16;" ::"r"(dst), "l"(src) : "memory");
+    uint64_t pol;
+    asm("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(pol));
+    asm volatile("cp.async.cg.shared.global.L2::cache_hint.L2::256B [%0], [%1], 16, %2;" ::"r"(dst), "l"(src), "l"(pol)
+                 : "memory");
 }
 
 __device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }

@@ -219,14 +219,17 @@ __global__ void __launch_bounds__(kThreads, 1) k_lmhead_fp8_tc(const __grid_cons
             return false;
         mbar_expect_tx(full, kStageBytes);
         const int y = (t_begin + ti) * kRows;
+        // rows read once per step: evict-first in L2
+        uint64_t pol;
+        asm("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(pol));
 #pragma unroll
         for (int b = 0; b < kChunksPerStage; ++b) {
             const uint32_t dst = ring + slot * kStageBytes + b * kBoxBytes;
             const int x = (ks * kChunksPerStage + b) * kChunk;
             asm volatile(
-                "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3}], "
-                "[%4];" ::"r"(dst),
-                "l"(reinterpret_cast<uint64_t>(&tmap)), "r"(x), "r"(y), "r"(full)
+                "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes.L2::cache_hint [%0], [%1, "
+                "{%2, %3}], [%4], %5;" ::"r"(dst),
+                "l"(reinterpret_cast<uint64_t>(&tmap)), "r"(x), "r"(y), "r"(full), "l"(pol)
                 : "memory");
         }
         ++p_stage;
