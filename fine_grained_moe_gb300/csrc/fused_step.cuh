@@ -2208,11 +2208,11 @@ __global__ void __launch_bounds__(kThreads, 1) k_fused(const __grid_constant__ P
                     mbar_arrive(&s.bready);
             }
             // 2. the tiles, in the order the producer took them (its tile records,
-            //    then an end marker): one thread issues the products, warps 0..3
-            //    (tensor-memory lanes 32 w .. 32 w + 31) read the accumulators,
-            //    combine the terms, apply the row scales and add into the residual
-            //    stream. The issuing thread publishes the stage and tile counts
-            //    after the phase (the tile count is known only to it).
+            //    then an end marker): warp kMW - 1 issues the products (one
+            //    elected lane), warps 0..3 (tensor-memory lanes 32 w .. 32 w + 31)
+            //    read the accumulators, combine the terms, apply the row scales and
+            //    add into the residual stream. The issuing warp publishes the stage
+            //    and tile counts after the phase (the tile count is known only to it).
             if (warp == kMW - 1) {
                 // the whole warp runs the issuing loop and one elected lane issues
                 // (measured a little faster than one lane's loop, 0.3 % per step);
