@@ -98,14 +98,15 @@ int device_ready(int *sms)
             FGM_SMEM(fp8tc::k_lmhead_fp8_tc<false>, fp8tc::kSmemBytes);
             FGM_SMEM(fp8tc::k_lmhead_fp8_tc<true>, fp8tc::kSmemBytes);
 #undef FGM_SMEM
-            const void *kerns[8] = {reinterpret_cast<const void *>(fused::k_fused<2, false>),
+            const void *kerns[9] = {reinterpret_cast<const void *>(fused::k_fused<2, false>),
                                     reinterpret_cast<const void *>(fused::k_fused<3, false>),
                                     reinterpret_cast<const void *>(fused::k_fused<2, true>),
                                     reinterpret_cast<const void *>(fused::k_fused<3, true>),
                                     reinterpret_cast<const void *>(fused::k_fused<2, false, 3>),
                                     reinterpret_cast<const void *>(fused::k_fused<3, false, 3>),
                                     reinterpret_cast<const void *>(fused::k_fused<2, false, 1, true>),
-                                    reinterpret_cast<const void *>(fused::k_fused<2, true, 1, true>)};
+                                    reinterpret_cast<const void *>(fused::k_fused<2, true, 1, true>),
+                                    reinterpret_cast<const void *>(fused::k_fused<2, false, 3, true>)};
             int per_sm = 1 << 30;
             for (const void *k : kerns) {
                 FGM_CUDA(cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kFusedSmemBytes));
@@ -135,7 +136,7 @@ int fused_grid()
 }
 
 // Launches the persistent kernel (cooperative: all CTAs co-resident).
-int tc_down_map(const uint8_t *down_q, CUtensorMap *map);
+int tc_down_map(const uint8_t *down_q, CUtensorMap *map, bool dense);
 
 int launch_fused(fused::Params &prm, cudaStream_t st)
 {
@@ -145,16 +146,21 @@ int launch_fused(fused::Params &prm, cudaStream_t st)
     // the tensor-memory path runs the down phase on tcgen05 (M <= 5, one shared expert)
     // (its bulk copies of row scales want 16-byte aligned scale arrays; else the
     // mma.sync down phase runs)
-    bool tcd = (g_path == FGM_PATH_FUSED || g_path == FGM_PATH_FUSED_TC) && prm.M <= 5 && prm.dense_parts == 0 &&
-               prm.mode != fused::kModeLmHead;
+    bool tcd = (g_path == FGM_PATH_FUSED || g_path == FGM_PATH_FUSED_TC) && prm.M <= 5 &&
+               (prm.dense_parts == 0 || prm.dense_parts == 3) && prm.mode != fused::kModeLmHead;
     const int n_tc = prm.mode == fused::kModeLayer ? 1 : prm.n_layers;
     for (int l = 0; tcd && l < n_tc; ++l)
-        if (reinterpret_cast<uintptr_t>(prm.layers[l].down_s) & 15u)
+        if ((reinterpret_cast<uintptr_t>(prm.layers[l].down_s) & 15u) ||
+            (prm.dense_parts && ((reinterpret_cast<uintptr_t>(prm.dense[l].ds) & 15u) ||
+                                 (reinterpret_cast<uintptr_t>(prm.dense[l].dq) & 15u))))
             tcd = false;
+    fused::ParamsDense pd;   // the dense variant's parameter block (NS = 3)
     if (tcd) {
         const int n_l = n_tc;
         for (int l = 0; l < n_l; ++l) {
-            const int rc = tc_down_map(prm.layers[l].down_q, &prm.dmap[l]);
+            int rc = tc_down_map(prm.layers[l].down_q, &prm.dmap[l], false);
+            if (rc == FGM_OK && prm.dense_parts)
+                rc = tc_down_map(prm.dense[l].dq, &pd.dmap_dense[l], true);
             if (rc != FGM_OK)
                 return rc;
         }
@@ -169,8 +175,9 @@ int launch_fused(fused::Params &prm, cudaStream_t st)
     // packed activation columns: 2 blocks of 8 hold M <= 5 tokens x 3 terms, 3 blocks M <= 8
     const bool traced = prm.trace != nullptr && prm.dense_parts == 0;
     const void *kern = prm.dense_parts == 3
-                           ? (prm.M <= 5 ? reinterpret_cast<const void *>(fused::k_fused<2, false, 3>)
-                                         : reinterpret_cast<const void *>(fused::k_fused<3, false, 3>))
+                           ? (tcd ? reinterpret_cast<const void *>(fused::k_fused<2, false, 3, true>)
+                              : prm.M <= 5 ? reinterpret_cast<const void *>(fused::k_fused<2, false, 3>)
+                                           : reinterpret_cast<const void *>(fused::k_fused<3, false, 3>))
                        : tcd ? (traced ? reinterpret_cast<const void *>(fused::k_fused<2, true, 1, true>)
                                        : reinterpret_cast<const void *>(fused::k_fused<2, false, 1, true>))
                        : prm.M <= 5 ? (traced ? reinterpret_cast<const void *>(fused::k_fused<2, true>)
@@ -179,6 +186,10 @@ int launch_fused(fused::Params &prm, cudaStream_t st)
                                               : reinterpret_cast<const void *>(fused::k_fused<3, false>));
     if (!traced)
         prm.trace = nullptr;
+    if (prm.dense_parts == 3) {
+        static_cast<fused::Params &>(pd) = prm;
+        args[0] = &pd;
+    }
     FGM_CUDA(cudaLaunchCooperativeKernel(kern, dim3(G),
                                          dim3(fused::kThreads), args, kFusedSmemBytes, st));
     return FGM_OK;
@@ -418,13 +429,15 @@ int run_lmhead_fp8_tc(const uint8_t *emb_q, const float *emb_s, int64_t V, const
     return FGM_OK;
 }
 
-// Tensor maps of one layer's down matrices ([129 * 2816 rows][704 bytes]):
-// 128 x 128-byte and 16 x 128-byte boxes in the 128-byte swizzle, zeros past
-// the 704 bytes of a row. Encoded once per weight address and kept.
-int tc_down_map(const uint8_t *down_q, CUtensorMap *map)
+// Tensor maps of one layer's down matrices ([129 * 2816 rows][704 bytes]), or
+// with `dense` of a dense MLP's down matrix ([2816 rows][3 * 704 bytes]):
+// 128 x 128-byte boxes in the 128-byte swizzle, zeros past the row's end.
+// Encoded once per weight address and kept.
+int tc_down_map(const uint8_t *down_q, CUtensorMap *map, bool dense)
 {
     struct Entry {
         const void *ptr;
+        bool dense;
         CUtensorMap map;
     };
     static Entry cache[2 * FGM_MAX_LAYERS];
@@ -432,7 +445,7 @@ int tc_down_map(const uint8_t *down_q, CUtensorMap *map)
     static std::mutex mu;
     std::lock_guard<std::mutex> lock(mu);
     for (int i = 0; i < n; ++i)
-        if (cache[i].ptr == down_q) {
+        if (cache[i].ptr == down_q && cache[i].dense == dense) {
             *map = cache[i].map;
             return FGM_OK;
         }
@@ -440,8 +453,10 @@ int tc_down_map(const uint8_t *down_q, CUtensorMap *map)
     FGM_TRY(encode_tiled_fn(&encode));
     Entry e;
     e.ptr = down_q;
-    const cuuint64_t dims[2] = {static_cast<cuuint64_t>(kF), static_cast<cuuint64_t>(kNE) * kH};
-    const cuuint64_t strides[1] = {static_cast<cuuint64_t>(kF)};
+    e.dense = dense;
+    const cuuint64_t width = dense ? 3u * kF : kF;
+    const cuuint64_t dims[2] = {width, dense ? static_cast<cuuint64_t>(kH) : static_cast<cuuint64_t>(kNE) * kH};
+    const cuuint64_t strides[1] = {width};
     const cuuint32_t estr[2] = {1, 1};
     const cuuint32_t box[2] = {128, 128};
     const CUresult r = encode(&e.map, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<uint8_t *>(down_q), dims, strides,

@@ -110,6 +110,17 @@ struct Params {
                             // complete (0: none)
 };
 
+// The dense variant's parameters (NS = 3): each layer's dense down matrix as
+// [2816 rows][3 * 704 bytes] for the tensor-memory down phase, the same boxes
+// (a part's tile starts at byte 704 p of its rows). A type of its own keeps
+// the other instantiations' parameter block as small as it was.
+struct ParamsDense : Params {
+    CUtensorMap dmap_dense[FGM_MAX_LAYERS];
+};
+
+template <int NS>
+using ParamsFor = typename std::conditional<(NS > 1), ParamsDense, Params>::type;
+
 // Profiling aid (Params::trace): per layer kTracePoints phase stamps for every
 // CTA, [(l * kTracePoints + k) * G + cta], then two end stamps per CTA, then
 // for CTA G/2 only a per-stage timeline [l][kTraceStages][8] of SM clock64
@@ -288,7 +299,7 @@ constexpr int kTcBBytes = (kF / 16) * 256;   // B operand of one slot: 44 K-colu
 constexpr uint32_t kTcTmemCols = 32;         // two 16-column accumulators
 constexpr int kTcInfo = 8;                   // tile records in flight (producer at most 4 tiles ahead of the epilogue)
 static_assert(kTcInfo * kTcRows <= kMaxDownRows, "tile scales do not fit");
-static_assert(5 * kK + 1 <= kSyncTileStride, "down-tile counters: slots at M <= 5 (one shared expert)");
+static_assert(5 * kK + 3 <= kSyncTileStride, "down-tile counters: slots at M <= 5 (up to three always-on parts)");
 // instruction descriptor, kind::f8f6f4: D fp32, A and B E4M3, both K-major, N >> 3, M >> 4
 constexpr uint32_t kTcIdesc = (1u << 4) | (static_cast<uint32_t>(kTcN >> 3) << 17) |
                               (static_cast<uint32_t>(kTcRows >> 4) << 24);
@@ -1160,9 +1171,9 @@ struct Parts {
 // (1: the shared expert; 3: a 2112-wide dense MLP in every layer). TCD: the down
 // phase on tcgen05 (NB = 2, NS = 1; tensor maps in Params::dmap).
 template <int NB, bool TRACE, int NS = 1, bool TCD = false>
-__global__ void __launch_bounds__(kThreads, 1) k_fused(const __grid_constant__ Params p)
+__global__ void __launch_bounds__(kThreads, 1) k_fused(const __grid_constant__ ParamsFor<NS> p)
 {
-    static_assert(!TCD || (NB == 2 && NS == 1), "the tensor-memory down phase covers M <= 5 with one shared expert");
+    static_assert(!TCD || (NB == 2 && (NS == 1 || NS == 3)), "the tensor-memory down phase covers M <= 5");
     // the shared-memory block starts 1024-byte aligned (swizzled TMA boxes in the ring)
     extern __shared__ __align__(128) uint8_t smem_raw[];
     Smem &s = *reinterpret_cast<Smem *>(smem_raw + ((1024u - (su32(smem_raw) & 1023u)) & 1023u));
@@ -1292,6 +1303,16 @@ __global__ void __launch_bounds__(kThreads, 1) k_fused(const __grid_constant__ P
                         const int si = hs0 + h2;
                         const int e = si < U ? s.experts[pb][si] : kShared;
                         const float *dsc = si < U ? L.down_s + (size_t)e * kH : Parts<NS>::down_s(L, p.dense[l], si - U);
+                        // a dense part's tile: its 704 bytes of the dense down rows
+                        const CUtensorMap *dmap = &p.dmap[l];
+                        int x0 = 0, y0 = e * kH;
+                        if constexpr (NS > 1) {
+                            if (si >= U) {
+                                dmap = &p.dmap_dense[l];
+                                x0 = kF * (si - U);
+                                y0 = 0;
+                            }
+                        }
                         for (;;) {
                             const unsigned t = atomicAdd(cnt + si, 1u);
                             if (t >= static_cast<unsigned>(kH / kTcRows))
@@ -1308,7 +1329,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_fused(const __grid_constant__ P
                                 if (ks == 0)
                                     bulk_g2s(sc, dsc + row, kTcRows * 4u, &s.full[stage % kStages]);
                                 for (int b = 0; b < 2; ++b)
-                                    tma_2d(d0 + b * kTcBoxBytes, &p.dmap[l], 256 * ks + 128 * b, e * kH + row,
+                                    tma_2d(d0 + b * kTcBoxBytes, dmap, x0 + 256 * ks + 128 * b, y0 + row,
                                            &s.full[stage % kStages], pol);
                                 ++stage;
                             }

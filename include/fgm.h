@@ -62,8 +62,9 @@ enum {
 enum {
     FGM_PATH_FUSED = 0,  /* default: one persistent cooperative kernel per call; weight rows stream
                             through a TMA-bulk shared-memory ring into FP8/bf16 mma.sync tiles, and
-                            at M <= 5 with the shared expert the down products run on tcgen05.mma
-                            (TMA tensor copies, tensor-memory accumulators) */
+                            at M <= 5 the down products (routed experts and the shared expert or
+                            the dense MLP's parts) run on tcgen05.mma (TMA tensor copies,
+                            tensor-memory accumulators) */
     FGM_PATH_STAGED = 1, /* one launch per stage with fp32 CUDA-core arithmetic (comparison path) */
     FGM_PATH_FUSED_TC = 2, /* as FGM_PATH_FUSED, with the FP8 lm_head on tcgen05.mma as well */
     FGM_PATH_FUSED_MMA = 3, /* as FGM_PATH_FUSED, with the down products on mma.sync at every M
@@ -367,9 +368,11 @@ int fgm_read_status(void *ws, size_t ws_bytes, int clear, int32_t *status, void 
  * (producer), 2 = routing known (producer), 3 = ring data landed, 6 = grid
  * barrier (warp = counter value, index = target), 7 = activation rows of an
  * expert written (index = its slot); the tcgen05 down phase: 8 =
- * accumulator read, 9 = products of a ring slot done, 10 = accumulator
- * full, 11 = activation rows written (index = slot), 12 = second home
- * slot's operand built. Synchronises the stream. */
+ * accumulator read, 10 = accumulator full, 11 = activation rows written
+ * (index = slot), 12 = second home slot's operand built (9 is no longer
+ * reported). When every CTA stops at a grid barrier, the first report may
+ * come from the barrier (6) or from a producer waiting for the routing that
+ * the barrier holds back (2). Synchronises the stream. */
 int fgm_read_wait_report(void *ws, size_t ws_bytes, int32_t *report, void *stream);
 
 /* Message describing the last error returned on the calling thread. */

@@ -62,7 +62,9 @@ def test_stall_in_a_later_layer_then_recovers():
         m.moe_stack_fwd(layers, x, ws=ws)
         torch.cuda.synchronize()
         assert ws.status() & m.STATUS_WAIT_TIMEOUT
-        assert ws.wait_report()[0] == 6   # the grid barrier
+        # the grid barrier, or a producer waiting for the routing that the
+        # barrier holds back: whichever checked the deadline first
+        assert ws.wait_report()[0] in (6, 2)
         again = m.moe_stack_fwd(layers, x, ws=ws)
         torch.cuda.synchronize()
         assert ws.status() == 0
