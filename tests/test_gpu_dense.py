@@ -5,8 +5,9 @@ full size: 128 routed experts of the benchmark layers (Zipf bias) and
 2112-wide E4M3 MLPs with fp32 row scales in their natural layout (down rows
 2112 wide). Same rules as the layer test: router ids bit-exact where the
 oracle's margin exceeds 1e-2 (else a valid choice), rows within 1e-2 and
-elementwise within 2e-2 of the bf16-rounded oracle. Both the persistent
-kernel and the per-stage kernels."""
+elementwise within 2e-2 of the bf16-rounded oracle. The persistent kernel
+(its down products on tcgen05 at M <= 5 on the default path, on mma.sync on
+FGM_PATH_FUSED_MMA and at M > 5) and the per-stage kernels."""
 
 import numpy as np
 import pytest
@@ -20,10 +21,11 @@ from helpers import (ELEM_TOL, MARGIN, REL_TOL, bf16_bits, bf16_values, elementw
 pytestmark = pytest.mark.gpu
 
 
-@pytest.fixture(scope="module", params=[0, 1], ids=["fused", "staged"])
+@pytest.fixture(scope="module", params=[0, 3, 1], ids=["fused", "fused_mma", "staged"])
 def fgm(request):
     """fused: the persistent kernel with the MLP's three parts as its always-on
-    slots; staged: the per-stage kernels."""
+    slots (tcgen05 down products at M <= 5); fused_mma: the same with the
+    mma.sync down products at every M; staged: the per-stage kernels."""
     import fine_grained_moe_gb300 as m
     m.lib()
     prev = m.select_path(request.param)
