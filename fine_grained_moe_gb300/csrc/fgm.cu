@@ -155,6 +155,8 @@ int launch_fused(fused::Params &prm, cudaStream_t st)
                                  (reinterpret_cast<uintptr_t>(prm.dense[l].dq) & 15u))))
             tcd = false;
     fused::ParamsDense pd;   // the dense variant's parameter block (NS = 3)
+    if (prm.dense_parts == 3)
+        memset(&pd, 0, sizeof pd);
     if (tcd) {
         const int n_l = n_tc;
         for (int l = 0; l < n_l; ++l) {
