@@ -69,6 +69,40 @@ def test_dense_layer_matches_oracle(fgm, case, M):
     assert ws.status() == 0
 
 
+def test_dense_layer_with_unaligned_down_scales(fgm, case):
+    """The MLP's down-row scales 4 bytes off a 16-byte boundary (the ABI asks
+    for 4-byte alignment): the tensor-memory down phase copies scales in
+    16-byte units, so the call takes the mma.sync down products; the result
+    still matches the oracle at M = 5."""
+    p, L, d, D = case
+    M = 5
+    buf = torch.empty(d["down_s"].numel() + 1, dtype=torch.float32, device="cuda")
+    buf[1:].copy_(d["down_s"].reshape(-1))
+    d2 = dict(d)
+    d2["down_s"] = buf[1:].view_as(d["down_s"])
+    assert d2["down_s"].data_ptr() % 16 == 4
+    ws = fgm.Workspace("cuda")
+    x = synth.hidden_states(3000 + M, M, device="cuda")
+    ids = torch.empty((M, 8), dtype=torch.int32, device="cuda")
+    y = fgm.moe_layer_dense_fwd(p, d2, x, topk_ids=ids, ws=ws)
+    torch.cuda.synchronize()
+    ref = oracle.moe_layer(L, bf16_values(x), dense_shared=D)
+    gid = ids.cpu().numpy()
+    row, elem = rowwise_rel_err(y, ref.y), elementwise_rel_err(y, ref.y)
+    compared = 0
+    for t in range(M):
+        if ref.margin[t] > MARGIN:
+            assert id_sets_agree(gid[t], ref.ids[t]), (t, gid[t], ref.ids[t])
+        elif not id_sets_agree(gid[t], ref.ids[t]):
+            assert ids_valid_at_tie(gid[t], ref.logits[t])
+            continue
+        assert row[t] <= REL_TOL, (t, row[t])
+        assert elem[t] <= ELEM_TOL, (t, elem[t])
+        compared += 1
+    assert compared >= 1
+    assert ws.status() == 0
+
+
 def test_dense_layer_is_routed_part_plus_mlp(fgm, case):
     """The dense call minus the plain layer call with the shared expert zeroed
     is the MLP alone (checked against the oracle's MLP per token)."""
